@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Throughput of the QSA indexer hot path on GB300: one step = K1a q-prep over
+every row, K1b K-compress over every block, K2 block scoring of every row
+(one-shot), on the B=8, S=16384 bf16 scoring workload (indexQk ~ N(0,1),
+contextLengths = S).  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain C restatement, single thread)
+on a bounded sample of the same workload and reports the same metric.
+With N > 1 (torchrun) every rank runs its own replica of the workload: the rows
+are independent, there is no exchange step (weak scaling); rank 0 prints
+rows of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "indexer rows/s and achieved HBM GB/s (K1a, K1b) vs 8 TB/s at 1 GB300"
+UNIT = "rows/s"
+WORKLOAD = "qsa indexer prefill step (K1a+K1b+K2), B=8 S=16384 bf16, ctx=S, N(0,1) indexQk"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- bookkeeping
+
+def algorithmic_bytes(ctx: np.ndarray, B: int, S: int, NB: int) -> dict:
+    """Bytes each kernel must move (T = 2 bytes), from the layouts on the
+    "Qsa Indexer Kernels" page; see the design doc for the per-unit figures."""
+    ctx = np.clip(ctx.astype(np.int64), 0, None)
+    valid_rows = int(np.minimum(ctx, S).sum())
+    pad_rows = B * S - valid_rows
+    positions = int(min(S, ctx.max()))
+    k1a = valid_rows * 2048 + pad_rows * 1024 + positions * 256
+    valid_blocks = int(np.minimum(ctx // 4, NB).sum())
+    k1b = valid_blocks * (1024 + 256) + (B * NB - valid_blocks) * 256 + int(min(NB, ctx.max() // 4)) * 256
+    vis_blocks = int(np.minimum(ctx // 4, NB).sum())
+    k2 = valid_rows * 1024 + vis_blocks * 256 + B * S * NB * 4
+    # causal MMA work: row t of a sequence scores floor((t+1)/4) blocks x 4 heads x 128 dims
+    flops = 0
+    for c in ctx:
+        t = np.arange(int(min(c, S)))
+        flops += int(((t + 1) // 4).sum()) * 4 * 128 * 2
+    return {"k1a": k1a, "k1b": k1b, "k2": k2, "k2_causal_flops": flops}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk.get("bf16_tflops", 1934.3)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str):
+        self.proc = None
+        self.device_id = device_id
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.device_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons, pw = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                pw.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        top = max(sm)
+        loaded = [s for s, p in zip(sm, pw) if p >= 0.5 * max(pw)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "sm_mhz_peak_seen": top, "power_w_max": max(pw)}
+
+
+def smi_device_id(local: int) -> str:
+    """nvidia-smi id of torch's device `local`: its UUID if nvidia-smi accepts it."""
+    import torch
+    try:
+        cand = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+        r = subprocess.run(["nvidia-smi", "-i", cand, "--query-gpu=uuid", "--format=csv,noheader"],
+                           capture_output=True, text=True, timeout=20)
+        if r.returncode == 0 and r.stdout.strip():
+            return cand
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v for v in vis.split(",") if v.strip()]
+    return ids[local] if local < len(ids) else str(local)
+
+
+# ------------------------------------------------------------------ oracle leg
+
+def oracle_sample(wl, budget_s: float = 12.0, seed: int = 0) -> dict:
+    """Time the CPU oracle (single thread, as it stands) on a bounded sample of the
+    workload and extrapolate to one full step: K1a on whole rows, K1b on whole
+    blocks, K2 on rows spread evenly over every position t (its cost grows with t)."""
+    import oracle
+    B, S, NB = wl.B, wl.S, wl.num_blocks
+    dtype = wl.dtype
+    # K1a: a contiguous slab of rows
+    n1 = min(S, 4096)
+    t0 = time.perf_counter()
+    oracle.q_prep(dtype, wl.index_qk[:1, :n1], wl.cos_sin, np.array([n1], np.int32), wl.w_q, wl.eps)
+    k1a_per_row = (time.perf_counter() - t0) / n1
+    # K1b: the blocks of that slab
+    nb1 = n1 // 4
+    t0 = time.perf_counter()
+    oracle.k_compress(dtype, wl.index_qk[:1, :n1], wl.cos_sin, np.array([n1], np.int32), wl.w_k, wl.eps,
+                      nb1, 0, nb1, 0)
+    k1b_per_block = (time.perf_counter() - t0) / nb1
+    # K2: rows at evenly spaced positions, on oracle-made qNormed/kbar of sequence 0
+    q0 = oracle.q_prep(dtype, wl.index_qk[:1], wl.cos_sin, wl.context_lengths[:1], wl.w_q, wl.eps)[0]
+    kb0 = oracle.k_compress(dtype, wl.index_qk[:1], wl.cos_sin, wl.context_lengths[:1], wl.w_k, wl.eps,
+                            NB, 0, NB, 0)[0]
+    ctx0 = int(wl.context_lengths[0])
+    rows_done, k2_time = 0, 0.0
+    stride_order = np.random.default_rng(seed).permutation(S)
+    t_start = time.perf_counter()
+    for t in stride_order:
+        a = time.perf_counter()
+        oracle.scores_row(dtype, q0[t], kb0, int(t), ctx0)
+        k2_time += time.perf_counter() - a
+        rows_done += 1
+        if time.perf_counter() - t_start > budget_s and rows_done >= 64:
+            break
+    k2_per_row = k2_time / rows_done
+    rows = B * S
+    step_s = k1a_per_row * rows + k1b_per_block * B * NB + k2_per_row * rows
+    return {
+        "value": rows / step_s,
+        "unit": UNIT,
+        "cores": 1,
+        "kind": "oracle",
+        "sample": (f"K1a on {n1} rows, K1b on {nb1} blocks, K2 on {rows_done} rows at random positions "
+                   f"of sequence 0 (S={S}); per-row/per-block times scaled to one full step of "
+                   f"{rows} rows and {B * NB} blocks"),
+        "est_step_s": step_s,
+    }
+
+
+# ------------------------------------------------------------------ main legs
+
+def run_reference(args, rank: int) -> None:
+    if rank != 0:
+        return
+    import workloads
+    wl = workloads.scoring("bf16", full_context=True)
+    budget = max(1.0, 100.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup):
+        oracle_sample(wl, budget_s=budget, seed=i)
+    vals, t_total = [], 0.0
+    res = None
+    for i in range(args.steps):
+        a = time.perf_counter()
+        res = oracle_sample(wl, budget_s=budget, seed=1000 + i)
+        t_total += time.perf_counter() - a
+        vals.append(res["value"])
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * wl.B * wl.S / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": wl.B, "S": wl.S, "num_blocks": wl.num_blocks},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": res["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank: int, world: int) -> None:
+    import torch
+    import sparse_attention_indexer_qsa_gb300 as qsa
+    import workloads
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    wl = workloads.scoring("bf16", seed=4 + rank, full_context=True)
+    B, S, NB = wl.B, wl.S, wl.num_blocks
+    rows = B * S
+    def host(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+
+    dev = lambda a: host(a).cuda()
+    iq = dev(wl.index_qk).view(torch.bfloat16)
+    cs, ctx = dev(wl.cos_sin), dev(wl.context_lengths)
+    wq, wk = dev(wl.w_q).view(torch.bfloat16), dev(wl.w_k).view(torch.bfloat16)
+    qn = torch.empty((B, S, 4, 128), dtype=torch.bfloat16, device="cuda")
+    kb = torch.empty((B, NB, 128), dtype=torch.bfloat16, device="cuda")
+    logits = torch.empty((rows, NB), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    lib = qsa.load()
+    eps = wl.eps
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        st = lib.qsa_index_q_prep(qsa.QSA_BF16, qn.data_ptr(), iq.data_ptr(), cs.data_ptr(), ctx.data_ptr(),
+                                  wq.data_ptr(), eps, B, S, sp)
+        if ev is not None:
+            ev[1].record(stream)
+        st |= lib.qsa_index_k_compress(qsa.QSA_BF16, kb.data_ptr(), iq.data_ptr(), cs.data_ptr(), ctx.data_ptr(),
+                                       wk.data_ptr(), eps, B, S, NB, 0, NB, 0, sp)
+        if ev is not None:
+            ev[2].record(stream)
+        st |= lib.qsa_index_scores(qsa.QSA_BF16, logits.data_ptr(), qn.data_ptr(), kb.data_ptr(), ctx.data_ptr(),
+                                   B, S, NB, 0, rows, sp)
+        if ev is not None:
+            ev[3].record(stream)
+        if st != 0:
+            raise RuntimeError(qsa.qsa_last_error())
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert qsa.qsa_device_fault_flags() == 0
+
+    dev_id = smi_device_id(local)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    with ClockSampler(dev_id) as clk:
+        # ---- device-timed region: inputs resident in HBM
+        barrier()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(K):
+            step(evs[i])
+        end.record(stream)
+        end.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+        ms_total = start.elapsed_time(end)
+
+        # ---- end-to-end through the public API with host buffers
+        K_e2e = max(3, min(K, 20))
+        h_iq = host(wl.index_qk).pin_memory()
+        h_cs = host(wl.cos_sin).pin_memory()
+        h_ctx = host(wl.context_lengths).pin_memory()
+        h_wq = host(wl.w_q).pin_memory()
+        h_wk = host(wl.w_k).pin_memory()
+        h_logits = torch.empty((rows, NB), dtype=torch.float32).pin_memory()
+        d_iq = torch.empty_like(h_iq, device="cuda")
+        d_cs = torch.empty_like(h_cs, device="cuda")
+        d_ctx = torch.empty_like(h_ctx, device="cuda")
+        d_wq = torch.empty_like(h_wq, device="cuda")
+        d_wk = torch.empty_like(h_wk, device="cuda")
+        h2d = sum(t.numel() * t.element_size() for t in (h_iq, h_cs, h_ctx, h_wq, h_wk))
+        d2h = h_logits.numel() * h_logits.element_size()
+
+        def e2e_step():
+            for h, d in ((h_iq, d_iq), (h_cs, d_cs), (h_ctx, d_ctx), (h_wq, d_wq), (h_wk, d_wk)):
+                d.copy_(h, non_blocking=True)
+            qsa.qsa_index_q_prep(qn, d_iq, d_cs, d_ctx, d_wq, eps, B, S, stream=sp, dtype="bf16")
+            qsa.qsa_index_k_compress(kb, d_iq, d_cs, d_ctx, d_wk, eps, B, S, NB, 0, NB, 0, stream=sp, dtype="bf16")
+            qsa.qsa_index_scores(logits, qn, kb, d_ctx, B, S, NB, 0, rows, stream=sp, dtype="bf16")
+            h_logits.copy_(logits, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K_e2e):
+            e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        barrier()
+        ms_e2e = e0.elapsed_time(e1) / K_e2e
+    torch.cuda.synchronize()
+    faults = qsa.qsa_device_fault_flags()
+
+    ms_step = max_over_ranks(ms_total / K)
+    ms_e2e = max_over_ranks(ms_e2e)
+    per_kernel = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+                  for j, n in enumerate(("k1a", "k1b", "k2"))}
+    if rank != 0:
+        return
+
+    hbm_peak, tf_peak, peak_src = load_peaks()
+    ab = algorithmic_bytes(wl.context_lengths, B, S, NB)
+    kernels = {}
+    for n in ("k1a", "k1b", "k2"):
+        gbs = ab[n] / (per_kernel[n] * 1e-3) / 1e9
+        kernels[n] = {"ms": per_kernel[n], "alg_bytes": ab[n], "gbs": gbs,
+                      "frac_of_measured_hbm": gbs / hbm_peak, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS}
+    kernels["k1a"]["rows_per_s"] = rows / (per_kernel["k1a"] * 1e-3)
+    kernels["k1b"]["blocks_per_s"] = B * NB / (per_kernel["k1b"] * 1e-3)
+    kernels["k1b"]["token_rows_per_s"] = 4 * B * NB / (per_kernel["k1b"] * 1e-3)
+    kernels["k2"]["rows_per_s"] = rows / (per_kernel["k2"] * 1e-3)
+    kernels["k2"]["causal_tflops"] = ab["k2_causal_flops"] / (per_kernel["k2"] * 1e-3) / 1e12
+    kernels["k2"]["frac_of_measured_bf16_peak"] = kernels["k2"]["causal_tflops"] / tf_peak
+
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "k2_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            with open(tpath) as f:
+                traffic = json.load(f).get("dram_bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    k2_gbs = kernels["k2"]["gbs"]
+    line = {
+        "metric": METRIC,
+        "value": world * rows / (ms_step * 1e-3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "S": S, "num_blocks": NB, "rows_per_step": rows,
+                   "k2_row_chunk": rows,
+                   "l2": "inputs larger than L2 (indexQk 168 MB, qNormed 134 MB) and each step writes "
+                         "2.15 GB of logits, which evicts L2 between steps"},
+        "roofline": {"bound": "hbm", "kernel": "k2_scores_tc", "achieved": k2_gbs, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": k2_gbs / hbm_peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} hbm_gbs"},
+        "kernels": kernels,
+        "e2e": {"value": world * rows / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": K_e2e},
+        "gpu_launches": 3 * K,
+        "clocks": clk.summary(),
+        "device_fault_flags": faults,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(wl)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank)
+        else:
+            run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+/*
+ * qsa_indexer.h -- C ABI of the GB300 (sm_103a) QSA sparse-attention indexer.
+ *
+ * Operations are those of the "Qsa Indexer Kernels" page (TensorRT-Edge-LLM C++
+ * API, cpp_api/kernels/qsaIndexerKernels.html): launchQsaIndexQPrep (K1a),
+ * launchQsaIndexKCompress (K1b) and launchQsaIndexScores (K2).  Arguments mirror
+ * the page one for one; a dtype enum replaces the C++ template parameter T and a
+ * status code replaces std::runtime_error.
+ *
+ * Conventions shared by every entry point
+ *  - T is the 2-byte activation type named by `dtype`: QSA_BF16 or QSA_F16.
+ *  - Every array argument is a DEVICE pointer owned by the caller; scalars are
+ *    host values.  The library allocates nothing, never synchronises, and
+ *    enqueues its kernels on `stream` only (0 = the legacy default stream), so
+ *    every call can be captured into a CUDA graph.  Kernels are compiled ahead
+ *    of time for sm_103a: there is no warm-up call.
+ *  - Arguments are validated on the host before anything is enqueued; device
+ *    data (contextLengths) is never read on the host.  On a non-zero status
+ *    nothing was enqueued (except QSA_E_CUDA from a failed launch) and
+ *    qsa_last_error() returns a message for the calling thread.
+ *  - Every array must be 16-byte aligned (torch allocations are); a misaligned
+ *    pointer returns QSA_E_ALIGN.
+ *  - Empty work (blockBegin == blockEnd, numRows == 0) returns QSA_OK and
+ *    enqueues nothing.
+ *  - "Exact zeros" are +0.0 in every element.  -FLT_MAX is the binary32 pattern
+ *    0xFF7FFFFF.
+ */
+#ifndef QSA_INDEXER_H
+#define QSA_INDEXER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* qsa_stream_t;
+
+typedef enum {
+  QSA_BF16 = 0, /* __nv_bfloat16 */
+  QSA_F16 = 1   /* half */
+} qsa_dtype_t;
+
+typedef enum {
+  QSA_OK = 0,
+  QSA_E_NULL = -1,  /* a required pointer is null */
+  QSA_E_SHAPE = -2, /* a size is out of range (batchSize, seqLen, numBlocks) */
+  QSA_E_RANGE = -3, /* a block/row range or pastLen is out of range */
+  QSA_E_DTYPE = -4, /* dtype is not QSA_BF16 or QSA_F16 */
+  QSA_E_ALIGN = -5, /* a pointer is not 16-byte aligned */
+  QSA_E_CUDA = -6,  /* a CUDA runtime call or kernel launch failed */
+  QSA_E_DEVICE = -7 /* the current device is not an sm_103 GPU */
+} qsa_status_t;
+
+#define QSA_ABI_VERSION 1
+#define QSA_HEAD_DIM 128
+#define QSA_NUM_Q_HEADS 4
+#define QSA_INDEX_QK_WIDTH 640 /* 4 q heads x 128, then the raw index-K x 128 */
+#define QSA_COMPRESS_RATIO 4   /* tokens per compressed block */
+
+/* QSA_ABI_VERSION of the loaded library. */
+int qsa_abi_version(void);
+
+/* Message for the calling thread's most recent non-OK status ("" if none). */
+const char* qsa_last_error(void);
+
+/*
+ * K1a, launchQsaIndexQPrep: Gemma-style q-norm plus partial neox rope.
+ *
+ *  qNormed        [out] T [batchSize, seqLen, 4, 128], contiguous.
+ *  indexQk        [in]  T [batchSize, seqLen, 640]; per row 4 q heads x 128, then
+ *                       the raw k x 128 (unused here).
+ *  cosSin         [in]  FP32 [maxPositions, 64], maxPositions >= seqLen; cos in
+ *                       columns 0..31, sin in 32..63; row t is rope position t.
+ *  contextLengths [in]  INT32 [batchSize], 0 <= contextLengths[b] <= seqLen.
+ *  wQ             [in]  T [128], the RAW checkpoint gamma (the kernel applies 1+w).
+ *  rmsEps         RMS-norm epsilon.
+ *
+ * Per row (b, t) with t < contextLengths[b] and per head h, in FP32:
+ *   meanSq = sum_d x_d^2 / 128 (warp reduction), r = rsqrtf(meanSq + rmsEps),
+ *   y_d = x_d * r * (1 + w_d); for i < 32 the pair (y_i, y_{i+32}) becomes
+ *   (y_i*cos - y_{i+32}*sin, y_{i+32}*cos + y_i*sin) with cos = cosSin[t][i],
+ *   sin = cosSin[t][32+i]; dims 64..127 pass through; one cast to T at the end.
+ * Rows with t >= contextLengths[b] are written as exact zeros and never read.
+ *
+ * Errors: QSA_E_NULL, QSA_E_DTYPE, QSA_E_SHAPE (batchSize < 1, seqLen < 1),
+ *         QSA_E_ALIGN, QSA_E_CUDA.
+ */
+int qsa_index_q_prep(qsa_dtype_t dtype, void* qNormed, const void* indexQk,
+                     const float* cosSin, const int32_t* contextLengths, const void* wQ,
+                     float rmsEps, int32_t batchSize, int32_t seqLen, qsa_stream_t stream);
+
+/*
+ * K1b, launchQsaIndexKCompress: 4-token block compression of the raw index-K,
+ * then the K1a norm (with wK) and rope at position 4g.
+ *
+ *  kbar           [out] T [batchSize, numBlocks, 128]; only rows g in
+ *                       [blockBegin, blockEnd) are written, the rest untouched.
+ *  indexQk        [in]  T [batchSize, seqLen, 640]; the raw k is columns 512..639.
+ *                       Row i holds token pastLen + i.
+ *  cosSin         [in]  FP32 [maxPositions, 64], maxPositions >= 4*blockEnd - 3.
+ *  contextLengths [in]  INT32 [batchSize], the TOTAL length (past + new).
+ *  wK             [in]  T [128], raw checkpoint gamma.
+ *  numBlocks      row stride of kbar: ceilDiv(maxTotalLen, 4).
+ *  blockBegin, blockEnd  0 <= blockBegin <= blockEnd <= numBlocks.
+ *  pastLen        tokens already cached before indexQk row 0 (0 in prefill), >= 0.
+ *
+ * Block (b, g) is valid iff 4g+3 < contextLengths[b], 4g >= pastLen and
+ * 4g+3-pastLen < seqLen (complete and fully inside the provided rows).  A valid
+ * block computes per dim m = T((((k0+k1)+k2)+k3) * 0.25f) in FP32 in that fixed
+ * order, with k_j the raw k of indexQk row 4g+j-pastLen; then the K1a math on
+ * the re-loaded m with wK at rope position 4g; one cast.  Invalid blocks are
+ * exact zeros and their rows are never read.  The result of a block does not
+ * depend on the range or pastLen it was computed in (sub-range bit-parity).
+ *
+ * Errors: QSA_E_NULL, QSA_E_DTYPE, QSA_E_SHAPE (batchSize < 1, seqLen < 1,
+ *         numBlocks < 1), QSA_E_RANGE (block range, pastLen < 0), QSA_E_ALIGN,
+ *         QSA_E_CUDA.
+ */
+int qsa_index_k_compress(qsa_dtype_t dtype, void* kbar, const void* indexQk,
+                         const float* cosSin, const int32_t* contextLengths, const void* wK,
+                         float rmsEps, int32_t batchSize, int32_t seqLen, int32_t numBlocks,
+                         int32_t blockBegin, int32_t blockEnd, int32_t pastLen,
+                         qsa_stream_t stream);
+
+/*
+ * K2, launchQsaIndexScores: causal block-relevance logits for a chunk of rows,
+ * on the tcgen05 tensor cores (FP32 accumulation of T products).
+ *
+ *  logits         [out] FP32 [numRows, numBlocks], chunk-local: row r - rowStart.
+ *  qNormed        [in]  T [batchSize, seqLen, 4, 128] (from qsa_index_q_prep).
+ *  kbar           [in]  T [batchSize, numBlocks, 128] (from qsa_index_k_compress).
+ *  contextLengths [in]  INT32 [batchSize].
+ *  numBlocks      ceilDiv(seqLen, 4) or more (extra columns are masked).
+ *  rowStart, numRows  global rows r = b*seqLen + t in [rowStart, rowStart+numRows),
+ *                 rowStart >= 0, rowStart + numRows <= batchSize*seqLen.
+ *
+ * For a row with 0 < contextLengths[b] and t < contextLengths[b]:
+ *   logits[g] = (1/sqrtf(128)) * sum_{h=0..3, ascending} max(0, q_h . kbar[b][g])
+ *   for g < (t+1)/4 (block fully before or at t), else -FLT_MAX.
+ * Padded rows are -FLT_MAX everywhere and their q rows are ignored.
+ *
+ * Errors: QSA_E_NULL, QSA_E_DTYPE, QSA_E_SHAPE (batchSize < 1, seqLen < 1,
+ *         numBlocks < ceilDiv(seqLen, 4)), QSA_E_RANGE (row range), QSA_E_ALIGN,
+ *         QSA_E_CUDA, QSA_E_DEVICE.
+ */
+int qsa_index_scores(qsa_dtype_t dtype, float* logits, const void* qNormed, const void* kbar,
+                     const int32_t* contextLengths, int32_t batchSize, int32_t seqLen,
+                     int32_t numBlocks, int32_t rowStart, int32_t numRows,
+                     qsa_stream_t stream);
+
+/*
+ * Device-side fault flags.  Kernels that wait on their own asynchronous copies
+ * bound every wait (about a second); a wait that runs out sets a bit here
+ * instead of hanging, the kernel drains and returns, and the outputs of that
+ * launch are undefined.  This call synchronises `stream`, copies the flags of
+ * the current device into *flags (0 = no fault since the last clear) and clears
+ * them when `clear` is non-zero.
+ *
+ * Errors: QSA_E_NULL (flags), QSA_E_CUDA.
+ */
+int qsa_device_fault_flags(uint32_t* flags, int clear, qsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_INDEXER_H */

@@ -1,0 +1,162 @@
+"""GB300 (sm_103a) QSA sparse-attention indexer: K1a q-prep, K1b K-compress, K2 scores.
+
+A thin ctypes binding over the C ABI in ``include/qsa_indexer.h``; every step of
+the computation runs in the library's CUDA kernels.  The functions keep the C
+names and argument order.  Array arguments are torch CUDA tensors (or raw
+device addresses as ints, with ``dtype`` given); the stream defaults to torch's
+current stream.  A non-zero status raises :class:`QsaError`.
+
+There is no CPU fallback: if ``_build/libqsa_indexer.so`` is missing, every call
+(and ``load()``) raises.  Build it with ``python -m sparse_attention_indexer_qsa_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+__all__ = [
+    "QsaError", "QSA_BF16", "QSA_F16", "load", "lib", "qsa_abi_version", "qsa_last_error",
+    "qsa_index_q_prep", "qsa_index_k_compress", "qsa_index_scores", "qsa_device_fault_flags",
+    "qsa_testing_index_scores_cuda_core", "LIB_PATH",
+]
+
+QSA_BF16 = 0
+QSA_F16 = 1
+STATUS_NAMES = {0: "QSA_OK", -1: "QSA_E_NULL", -2: "QSA_E_SHAPE", -3: "QSA_E_RANGE",
+                -4: "QSA_E_DTYPE", -5: "QSA_E_ALIGN", -6: "QSA_E_CUDA", -7: "QSA_E_DEVICE"}
+EXPORTED = ["qsa_abi_version", "qsa_last_error", "qsa_index_q_prep", "qsa_index_k_compress",
+            "qsa_index_scores", "qsa_device_fault_flags", "qsa_testing_index_scores_cuda_core"]
+
+
+class QsaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load():
+    """Load the CUDA library (once).  Raises if it has not been built: no fallback."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run "
+                          "`python -m sparse_attention_indexer_qsa_gb300.build` (nvcc, sm_103a)")
+    L = ctypes.CDLL(LIB_PATH)
+    p = ctypes.c_void_p
+    i32 = ctypes.c_int32
+    f32 = ctypes.c_float
+    L.qsa_abi_version.argtypes = []
+    L.qsa_abi_version.restype = ctypes.c_int
+    L.qsa_last_error.argtypes = []
+    L.qsa_last_error.restype = ctypes.c_char_p
+    L.qsa_index_q_prep.argtypes = [ctypes.c_int, p, p, p, p, p, f32, i32, i32, p]
+    L.qsa_index_q_prep.restype = ctypes.c_int
+    L.qsa_index_k_compress.argtypes = [ctypes.c_int, p, p, p, p, p, f32, i32, i32, i32,
+                                       i32, i32, i32, p]
+    L.qsa_index_k_compress.restype = ctypes.c_int
+    L.qsa_index_scores.argtypes = [ctypes.c_int, p, p, p, p, i32, i32, i32, i32, i32, p]
+    L.qsa_index_scores.restype = ctypes.c_int
+    L.qsa_testing_index_scores_cuda_core.argtypes = list(L.qsa_index_scores.argtypes)
+    L.qsa_testing_index_scores_cuda_core.restype = ctypes.c_int
+    L.qsa_device_fault_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, p]
+    L.qsa_device_fault_flags.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def __getattr__(name):
+    if name == "lib":
+        return load()
+    raise AttributeError(name)
+
+
+def qsa_abi_version() -> int:
+    return int(load().qsa_abi_version())
+
+
+def qsa_last_error() -> str:
+    return load().qsa_last_error().decode()
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _dtype(dtype, *tensors) -> int:
+    if dtype is not None:
+        if isinstance(dtype, str):
+            return {"bf16": QSA_BF16, "fp16": QSA_F16}[dtype]
+        return int(dtype)
+    import torch
+    for t in tensors:
+        if isinstance(t, torch.Tensor):
+            if t.dtype == torch.bfloat16:
+                return QSA_BF16
+            if t.dtype == torch.float16:
+                return QSA_F16
+    raise ValueError("dtype not given and not inferable from the tensors")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int):
+    if status != 0:
+        raise QsaError(status, qsa_last_error())
+
+
+def qsa_index_q_prep(qNormed, indexQk, cosSin, contextLengths, wQ, rmsEps, batchSize, seqLen,
+                     stream=None, dtype=None):
+    """K1a: indexQk [B, S, 640] -> qNormed [B, S, 4, 128] (see include/qsa_indexer.h)."""
+    _check(load().qsa_index_q_prep(_dtype(dtype, indexQk, qNormed), _addr(qNormed), _addr(indexQk),
+                                _addr(cosSin), _addr(contextLengths), _addr(wQ), float(rmsEps),
+                                int(batchSize), int(seqLen), _stream(stream)))
+
+
+def qsa_index_k_compress(kbar, indexQk, cosSin, contextLengths, wK, rmsEps, batchSize, seqLen,
+                         numBlocks, blockBegin, blockEnd, pastLen, stream=None, dtype=None):
+    """K1b: rows [blockBegin, blockEnd) of kbar [B, numBlocks, 128] (see include/qsa_indexer.h)."""
+    _check(load().qsa_index_k_compress(_dtype(dtype, indexQk, kbar), _addr(kbar), _addr(indexQk),
+                                    _addr(cosSin), _addr(contextLengths), _addr(wK), float(rmsEps),
+                                    int(batchSize), int(seqLen), int(numBlocks), int(blockBegin),
+                                    int(blockEnd), int(pastLen), _stream(stream)))
+
+
+def qsa_index_scores(logits, qNormed, kbar, contextLengths, batchSize, seqLen, numBlocks,
+                     rowStart, numRows, stream=None, dtype=None):
+    """K2: FP32 logits [numRows, numBlocks] on the tensor cores (see include/qsa_indexer.h)."""
+    _check(load().qsa_index_scores(_dtype(dtype, qNormed, kbar), _addr(logits), _addr(qNormed),
+                                _addr(kbar), _addr(contextLengths), int(batchSize), int(seqLen),
+                                int(numBlocks), int(rowStart), int(numRows), _stream(stream)))
+
+
+def qsa_testing_index_scores_cuda_core(logits, qNormed, kbar, contextLengths, batchSize, seqLen,
+                                       numBlocks, rowStart, numRows, stream=None, dtype=None):
+    """K2 on CUDA cores (include/qsa_indexer_testing.h): a test-only cross-check."""
+    _check(load().qsa_testing_index_scores_cuda_core(
+        _dtype(dtype, qNormed, kbar), _addr(logits), _addr(qNormed), _addr(kbar),
+        _addr(contextLengths), int(batchSize), int(seqLen), int(numBlocks), int(rowStart),
+        int(numRows), _stream(stream)))
+
+
+def qsa_device_fault_flags(clear: bool = True, stream=None) -> int:
+    """Synchronise ``stream`` and return (and optionally clear) the device fault bits."""
+    flags = ctypes.c_uint32(0)
+    _check(load().qsa_device_fault_flags(ctypes.byref(flags), 1 if clear else 0, _stream(stream)))
+    return int(flags.value)

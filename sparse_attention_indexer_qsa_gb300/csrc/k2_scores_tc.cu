@@ -1,0 +1,458 @@
+// K2: causal block-relevance logits on the tcgen05 tensor cores
+// ("Qsa Indexer Kernels", launchQsaIndexScores):
+//   logits[r][g] = (1/sqrtf(128)) * sum_{h ascending} max(0, q[r][h] . kbar[b][g])
+// for g < (t+1)/4 on rows with t < contextLengths[b]; -FLT_MAX elsewhere.
+//
+// GEMM mapping (roles chosen so the epilogue needs no shuffles and stores coalesce):
+//   A (M = 128)  = 128 kbar blocks g of one sequence, K-major, 128 dims
+//   B (N = 256)  = 64 tokens x 4 heads of qNormed ([.., 4, 128] rows are exactly
+//                  the K-major B rows), so TMEM lane = block g, column = 4*token + head
+//   D            = FP32 in TMEM, two 256-column accumulators (all 512 columns)
+// An epilogue thread owns one block g (one TMEM lane): it reads 4 heads of a token
+// from 4 consecutive columns, applies relu per head, sums them in ascending h, scales
+// and masks, and the 32 lanes of a warp write 32 consecutive logits (128 bytes).
+//
+// Persistent CTA per SM, warp-specialised:
+//   warp 0     TMA producer (q tile once per work unit, kbar tiles per MMA g-tile)
+//   warp 1     TMEM allocator + single-thread MMA issuer
+//   warps 2-9  epilogue (two warps per TMEM sub-partition, one per token half)
+// A work unit is (sequence b, 64-token tile, up to 8 g-tiles of 128 blocks).  Tiles
+// whose blocks are all masked for every stored row skip the MMA and only store
+// -FLT_MAX.  Rows outside the chunk or the sequence are computed but never stored;
+// TMA reads past the end of a sequence's q or kbar rows return zeros.
+//
+// Every mbarrier wait is bounded (about two seconds of %globaltimer).  A wait that
+// runs out sets a bit in the device fault word and a CTA-wide abort flag; the CTA
+// then waits (bounded) for its own TMA copies and MMAs in flight, frees TMEM and exits.
+#include <cfloat>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "qsa_launch.h"
+#include "tc_ptx.cuh"
+
+namespace qsa {
+
+__device__ uint32_t g_fault_flags;
+
+namespace k2 {
+
+constexpr int kTokTile = 64;                  // tokens per tile
+constexpr int kN = kTokTile * 4;              // MMA N: token x head rows
+constexpr int kGTile = 128;                   // MMA M: kbar blocks per tile
+constexpr int kGTilesPerUnit = 8;
+constexpr int kQStages = 2;
+constexpr int kKStages = 3;
+constexpr int kAccStages = 2;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 256;
+constexpr uint32_t kQHalfBytes = kN * 64 * 2;       // one 64-element K half of the q tile
+constexpr uint32_t kQBytes = 2 * kQHalfBytes;
+constexpr uint32_t kKHalfBytes = kGTile * 64 * 2;
+constexpr uint32_t kKBytes = 2 * kKHalfBytes;
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kQStages * kQBytes;
+constexpr uint32_t kOffBar = kOffK + kKStages * kKBytes;
+constexpr int kBarQFull = 0;
+constexpr int kBarQEmpty = kBarQFull + kQStages;
+constexpr int kBarKFull = kBarQEmpty + kQStages;
+constexpr int kBarKEmpty = kBarKFull + kKStages;
+constexpr int kBarAccFull = kBarKEmpty + kKStages;
+constexpr int kBarAccEmpty = kBarAccFull + kAccStages;
+constexpr int kBarDrain = kBarAccEmpty + kAccStages;
+constexpr int kNumBars = kBarDrain + 1;
+constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1024
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+enum : uint32_t {
+  kFaultProducer = 1u,
+  kFaultMma = 2u,
+  kFaultEpilogue = 4u,
+  kFaultDrain = 8u,
+};
+
+struct Params {
+  float* logits;
+  const int32_t* ctx;
+  int32_t batch, seq_len, num_blocks, row_start, num_rows;
+  int32_t tiles_per_batch;  // ceilDiv(seq_len, 64)
+  int32_t tile_lo;          // first global token tile (b * tiles_per_batch + i) of the chunk
+  int32_t n_gtiles;         // ceilDiv(num_blocks, 128)
+  int32_t n_groups;         // ceilDiv(n_gtiles, 8)
+  int32_t units;
+  uint32_t idesc;
+  float scale;
+};
+
+struct Unit {
+  int32_t b, t0;
+  int32_t gt_begin, gt_end, gt_mma_end;  // g-tiles [gt_begin, gt_end); MMA on [gt_begin, gt_mma_end)
+  int32_t t_lo, t_hi;                    // stored rows [t_lo, t_hi)
+  int32_t t_vis_hi;                      // rows below this (and >= t_lo) are unpadded
+  int64_t row_base;                      // chunk-local row of (b, t = 0)
+};
+
+__device__ __forceinline__ Unit unit_info(const Params& p, int32_t u) {
+  Unit x;
+  const int32_t tq = u / p.n_groups;
+  const int32_t grp = u - tq * p.n_groups;
+  const int32_t tile = p.tile_lo + tq;
+  x.b = tile / p.tiles_per_batch;
+  x.t0 = (tile - x.b * p.tiles_per_batch) * kTokTile;
+  x.gt_begin = grp * kGTilesPerUnit;
+  x.gt_end = min(p.n_gtiles, x.gt_begin + kGTilesPerUnit);
+  const int64_t bs = static_cast<int64_t>(x.b) * p.seq_len;
+  const int64_t c_lo = static_cast<int64_t>(p.row_start) - bs;
+  const int64_t c_hi = static_cast<int64_t>(p.row_start) + p.num_rows - bs;
+  x.t_lo = static_cast<int32_t>(max(static_cast<int64_t>(x.t0), max(c_lo, int64_t{0})));
+  x.t_hi = static_cast<int32_t>(min(static_cast<int64_t>(x.t0 + kTokTile),
+                                    min(c_hi, static_cast<int64_t>(p.seq_len))));
+  const int32_t ctx = max(__ldg(p.ctx + x.b), 0);
+  x.t_vis_hi = min(x.t_hi, ctx);
+  // The last unpadded row t_vis_hi - 1 sees blocks g < t_vis_hi / 4; visibility only
+  // shrinks with g, so the MMA g-tiles are a prefix of the unit's g-tiles.
+  int32_t mma_end = x.gt_begin;
+  if (x.t_vis_hi > x.t_lo) {
+    const int32_t nvis = x.t_vis_hi / 4;
+    mma_end = min(x.gt_end, (nvis + kGTile - 1) / kGTile);
+    mma_end = max(mma_end, x.gt_begin);
+  }
+  x.gt_mma_end = mma_end;
+  x.row_base = bs - p.row_start;
+  return x;
+}
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             uint32_t fault_code) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t start = ptx::global_timer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::global_timer_ns() - start > kWaitLimitNs) {
+      atomicOr(&g_fault_flags, fault_code);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Used only while draining after an abort: ignores the abort flag, shorter limit.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t start = ptx::global_timer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::global_timer_ns() - start > kDrainLimitNs) {
+      atomicOr(&g_fault_flags, kFaultDrain);
+      return;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                    const __grid_constant__ CUtensorMap tmap_k, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bars = base + kOffBar;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base_ptr + kOffTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + kOffAbort);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQStages; ++s) {
+      ptx::mbar_init(bar(kBarQFull + s), 1);
+      ptx::mbar_init(bar(kBarQEmpty + s), 1);
+    }
+    for (int s = 0; s < kKStages; ++s) {
+      ptx::mbar_init(bar(kBarKFull + s), 1);
+      ptx::mbar_init(bar(kBarKEmpty + s), 1);
+    }
+    for (int s = 0; s < kAccStages; ++s) {
+      ptx::mbar_init(bar(kBarAccFull + s), 1);
+      ptx::mbar_init(bar(kBarAccEmpty + s), kEpiWarps);
+    }
+    ptx::mbar_init(bar(kBarDrain), 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tmap_q);
+    ptx::prefetch_tensormap(&tmap_k);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tmem_alloc(base + kOffTmemSlot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int qcnt = 0, kcnt = 0;
+      for (int32_t u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const Unit x = unit_info(p, u);
+        if (x.gt_mma_end <= x.gt_begin) continue;
+        const int qs = qcnt % kQStages;
+        if (!wait_bounded(bar(kBarQEmpty + qs), ((qcnt / kQStages) & 1) ^ 1, abort_flag, kFaultProducer)) break;
+        ptx::mbar_arrive_expect_tx(bar(kBarQFull + qs), kQBytes);
+        const uint32_t qdst = base + kOffQ + qs * kQBytes;
+        ptx::tma_load_3d(qdst, &tmap_q, bar(kBarQFull + qs), 0, 4 * x.t0, x.b);
+        ptx::tma_load_3d(qdst + kQHalfBytes, &tmap_q, bar(kBarQFull + qs), 64, 4 * x.t0, x.b);
+        ++qcnt;
+        bool ok = true;
+        for (int gt = x.gt_begin; gt < x.gt_mma_end; ++gt) {
+          const int ks = kcnt % kKStages;
+          if (!wait_bounded(bar(kBarKEmpty + ks), ((kcnt / kKStages) & 1) ^ 1, abort_flag, kFaultProducer)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(bar(kBarKFull + ks), kKBytes);
+          const uint32_t kdst = base + kOffK + ks * kKBytes;
+          ptx::tma_load_3d(kdst, &tmap_k, bar(kBarKFull + ks), 0, gt * kGTile, x.b);
+          ptx::tma_load_3d(kdst + kKHalfBytes, &tmap_k, bar(kBarKFull + ks), 64, gt * kGTile, x.b);
+          ++kcnt;
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) {
+        // wait for the last copy issued into each stage before the CTA can exit
+        for (int s = 0; s < kQStages; ++s) {
+          if (qcnt > s) {
+            const int n = ((qcnt - 1 - s) / kQStages) * kQStages + s;
+            drain_wait(bar(kBarQFull + s), (n / kQStages) & 1);
+          }
+        }
+        for (int s = 0; s < kKStages; ++s) {
+          if (kcnt > s) {
+            const int n = ((kcnt - 1 - s) / kKStages) * kKStages + s;
+            drain_wait(bar(kBarKFull + s), (n / kKStages) & 1);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int qcnt = 0, kcnt = 0, acnt = 0;
+      bool ok = true;
+      for (int32_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        const Unit x = unit_info(p, u);
+        if (x.gt_mma_end <= x.gt_begin) continue;
+        const int qs = qcnt % kQStages;
+        if (!wait_bounded(bar(kBarQFull + qs), (qcnt / kQStages) & 1, abort_flag, kFaultMma)) break;
+        ptx::tc_fence_after();
+        const uint32_t qaddr = base + kOffQ + qs * kQBytes;
+        for (int gt = x.gt_begin; gt < x.gt_mma_end; ++gt) {
+          const int ks = kcnt % kKStages;
+          const int as = acnt % kAccStages;
+          if (!wait_bounded(bar(kBarKFull + ks), (kcnt / kKStages) & 1, abort_flag, kFaultMma) ||
+              !wait_bounded(bar(kBarAccEmpty + as), ((acnt / kAccStages) & 1) ^ 1, abort_flag, kFaultMma)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t kaddr = base + kOffK + ks * kKBytes;
+          const uint32_t d = tmem + static_cast<uint32_t>(as) * kAccCols;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t koff = static_cast<uint32_t>(kk & 3) * 32u;
+            const uint64_t adesc = ptx::smem_desc_sw128(kaddr + (kk >> 2) * kKHalfBytes + koff);
+            const uint64_t bdesc = ptx::smem_desc_sw128(qaddr + (kk >> 2) * kQHalfBytes + koff);
+            ptx::mma_f16(d, adesc, bdesc, p.idesc, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(bar(kBarKEmpty + ks));
+          ptx::mma_commit(bar(kBarAccFull + as));
+          ++kcnt;
+          ++acnt;
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(kBarQEmpty + qs));
+        ++qcnt;
+      }
+      // every MMA (and the arrivals committed after it) completes before TMEM is freed
+      ptx::mma_commit(bar(kBarDrain));
+      drain_wait(bar(kBarDrain), 0);
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue
+    const int ew = warp - 2;
+    const int sp = warp & 3;       // TMEM sub-partition this warp may access
+    const int half = ew >> 2;      // token half: tokens [32*half, 32*half + 32) of the tile
+    const int32_t g_in_tile = 32 * sp + lane;
+    const float neg_max = -FLT_MAX;
+    const int64_t nb = p.num_blocks;
+    int acnt = 0;
+    bool ok = true;
+    for (int32_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      const Unit x = unit_info(p, u);
+      const int32_t tb = x.t0 + 32 * half;  // first token of this warp's half
+      for (int gt = x.gt_begin; gt < x.gt_end; ++gt) {
+        const int32_t g = gt * kGTile + g_in_tile;
+        const bool g_ok = g < p.num_blocks;
+        float* out = p.logits + x.row_base * nb + g;
+        if (gt < x.gt_mma_end) {
+          const int as = acnt % kAccStages;
+          if (!wait_bounded(bar(kBarAccFull + as), (acnt / kAccStages) & 1, abort_flag, kFaultEpilogue)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * sp) << 16) +
+                                 static_cast<uint32_t>(as) * kAccCols + 128u * half;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(taddr + 32u * c, r);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int32_t t = tb + 8 * c + k;
+              if (g_ok && t >= x.t_lo && t < x.t_hi) {
+                float v = __fadd_rn(fmaxf(0.0f, __uint_as_float(r[4 * k + 0])),
+                                    fmaxf(0.0f, __uint_as_float(r[4 * k + 1])));
+                v = __fadd_rn(v, fmaxf(0.0f, __uint_as_float(r[4 * k + 2])));
+                v = __fadd_rn(v, fmaxf(0.0f, __uint_as_float(r[4 * k + 3])));
+                const bool vis = t < x.t_vis_hi && g < (t + 1) / 4;
+                out[static_cast<int64_t>(t) * nb] = vis ? __fmul_rn(v, p.scale) : neg_max;
+              }
+            }
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(kBarAccEmpty + as));
+          ++acnt;
+        } else if (g_ok) {
+#pragma unroll 4
+          for (int k = 0; k < 32; ++k) {
+            const int32_t t = tb + k;
+            if (t >= x.t_lo && t < x.t_hi) out[static_cast<int64_t>(t) * nb] = neg_max;
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace k2
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn(cudaError_t* err) {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static cudaError_t status = cudaSuccess;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                              cudaEnableDefault, &q);
+    if (status == cudaSuccess && q != cudaDriverEntryPointSuccess) status = cudaErrorNotSupported;
+    if (status == cudaSuccess) fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  *err = status;
+  return fn;
+}
+
+// 3-D map over [dim2][dim1][128] two-byte elements, box {64, box1, 1}, 128-byte swizzle.
+cudaError_t encode_rows(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* map,
+                        const void* ptr, uint64_t dim1, uint64_t dim2, uint32_t box1) {
+  cuuint64_t dims[3] = {128, dim1, dim2};
+  cuuint64_t strides[2] = {256, dim1 * 256};
+  cuuint32_t box[3] = {64, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(ptr), dims, strides,
+                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+std::mutex g_attr_mu;
+bool g_attr_set[64] = {};
+
+}  // namespace
+
+cudaError_t launch_scores_tc(const LaunchScores& a) {
+  using namespace k2;
+  cudaError_t e;
+  auto encode = get_encode_fn(&e);
+  if (e != cudaSuccess) return e;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!g_attr_set[dev]) {
+      e = cudaFuncSetAttribute(k2_scores_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmemBytes));
+      if (e != cudaSuccess) return e;
+      g_attr_set[dev] = true;
+    }
+  }
+  CUtensorMap tq, tk;
+  if ((e = encode_rows(encode, &tq, a.q_normed, 4ull * a.seq_len, a.batch, kN)) != cudaSuccess) return e;
+  if ((e = encode_rows(encode, &tk, a.kbar, a.num_blocks, a.batch, kGTile)) != cudaSuccess) return e;
+
+  Params p{};
+  p.logits = a.logits;
+  p.ctx = a.context_lengths;
+  p.batch = a.batch;
+  p.seq_len = a.seq_len;
+  p.num_blocks = a.num_blocks;
+  p.row_start = a.row_start;
+  p.num_rows = a.num_rows;
+  p.tiles_per_batch = (a.seq_len + kTokTile - 1) / kTokTile;
+  const int64_t first = a.row_start;
+  const int64_t last = static_cast<int64_t>(a.row_start) + a.num_rows - 1;
+  const int64_t b_first = first / a.seq_len, b_last = last / a.seq_len;
+  const int64_t tile_lo = b_first * p.tiles_per_batch + (first - b_first * a.seq_len) / kTokTile;
+  const int64_t tile_hi = b_last * p.tiles_per_batch + (last - b_last * a.seq_len) / kTokTile + 1;
+  p.tile_lo = static_cast<int32_t>(tile_lo);
+  p.n_gtiles = (a.num_blocks + kGTile - 1) / kGTile;
+  p.n_groups = (p.n_gtiles + kGTilesPerUnit - 1) / kGTilesPerUnit;
+  const int64_t units = (tile_hi - tile_lo) * p.n_groups;
+  if (units > INT32_MAX) return cudaErrorInvalidValue;
+  p.units = static_cast<int32_t>(units);
+  p.idesc = ptx::idesc_f16(a.bf16, kGTile, kN);
+  p.scale = a.scale;
+  const int grid = static_cast<int>(units < a.num_sms ? units : a.num_sms);
+  k2_scores_tc_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, p);
+  return cudaGetLastError();
+}
+
+cudaError_t read_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(flags, g_fault_flags, sizeof(uint32_t), 0,
+                                            cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
+  if (clear && *flags != 0u) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_fault_flags, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+  }
+  return e;
+}
+
+}  // namespace qsa

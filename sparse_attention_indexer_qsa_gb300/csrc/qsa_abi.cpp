@@ -1,0 +1,238 @@
+// The C ABI (include/qsa_indexer.h): host-side validation, device checks,
+// dtype dispatch and error reporting.  Every check here runs before anything is
+// enqueued; device data is never read on the host.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/qsa_indexer.h"
+#include "../../include/qsa_indexer_testing.h"
+#include "qsa_launch.h"
+
+#define QSA_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct DeviceInfo {
+  bool known = false;
+  int num_sms = 0;
+  int major = 0, minor = 0;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+// SM count and compute capability of the current device (cached per device).
+int current_device(const char* fn, DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(QSA_E_CUDA, "%s: cudaGetDevice: %s", fn, cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(QSA_E_DEVICE, "%s: device ordinal %d unsupported", fn, dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.known) {
+    if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return fail(QSA_E_CUDA, "%s: cudaDeviceGetAttribute: %s", fn, cudaGetErrorString(e));
+    d.known = true;
+  }
+  if (d.major != 10 || d.minor != 3)
+    return fail(QSA_E_DEVICE, "%s: the library is built for sm_103a only; device %d is sm_%d%d", fn,
+                dev, d.major, d.minor);
+  *out = d;
+  return QSA_OK;
+}
+
+int check_dtype(const char* fn, qsa_dtype_t dt) {
+  if (dt != QSA_BF16 && dt != QSA_F16) return fail(QSA_E_DTYPE, "%s: unknown dtype %d", fn, static_cast<int>(dt));
+  return QSA_OK;
+}
+
+int launched(const char* fn, cudaError_t e) {
+  if (e != cudaSuccess) return fail(QSA_E_CUDA, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  g_last_error[0] = '\0';
+  return QSA_OK;
+}
+
+int validate_scores(const char* fn, qsa_dtype_t dtype, const float* logits, const void* qNormed,
+                    const void* kbar, const int32_t* ctx, int32_t B, int32_t S, int32_t NB,
+                    int32_t rowStart, int32_t numRows) {
+  int st;
+  if ((st = check_dtype(fn, dtype)) != QSA_OK) return st;
+  if (!logits || !qNormed || !kbar || !ctx) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  if (B < 1 || S < 1) return fail(QSA_E_SHAPE, "%s: batchSize=%d seqLen=%d must be >= 1", fn, B, S);
+  if (static_cast<int64_t>(B) * S > INT32_MAX) return fail(QSA_E_SHAPE, "%s: batchSize*seqLen exceeds INT32_MAX", fn);
+  if (NB < (S + 3) / 4) return fail(QSA_E_SHAPE, "%s: numBlocks=%d < ceilDiv(seqLen=%d, 4)", fn, NB, S);
+  if (rowStart < 0 || numRows < 0 || static_cast<int64_t>(rowStart) + numRows > static_cast<int64_t>(B) * S)
+    return fail(QSA_E_RANGE, "%s: rows [%d, %d + %d) outside [0, %lld)", fn, rowStart, rowStart, numRows,
+                static_cast<long long>(B) * S);
+  if (!aligned(qNormed, 16) || !aligned(kbar, 16) || !aligned(logits, 4) || !aligned(ctx, 4))
+    return fail(QSA_E_ALIGN, "%s: qNormed/kbar must be 16-byte aligned, logits/contextLengths 4-byte", fn);
+  return QSA_OK;
+}
+
+float score_scale() {
+  volatile float root = std::sqrt(128.0f);  // binary32 sqrt, then a binary32 division
+  return 1.0f / root;
+}
+
+}  // namespace
+
+QSA_API int qsa_abi_version(void) { return QSA_ABI_VERSION; }
+
+QSA_API const char* qsa_last_error(void) { return g_last_error; }
+
+QSA_API int qsa_index_q_prep(qsa_dtype_t dtype, void* qNormed, const void* indexQk, const float* cosSin,
+                             const int32_t* contextLengths, const void* wQ, float rmsEps,
+                             int32_t batchSize, int32_t seqLen, qsa_stream_t stream) {
+  static const char* fn = "qsa_index_q_prep";
+  int st;
+  if ((st = check_dtype(fn, dtype)) != QSA_OK) return st;
+  if (!qNormed || !indexQk || !cosSin || !contextLengths || !wQ) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  if (batchSize < 1 || seqLen < 1)
+    return fail(QSA_E_SHAPE, "%s: batchSize=%d seqLen=%d must be >= 1", fn, batchSize, seqLen);
+  if (static_cast<int64_t>(batchSize) * seqLen > INT32_MAX)
+    return fail(QSA_E_SHAPE, "%s: batchSize*seqLen exceeds INT32_MAX", fn);
+  if (!aligned(qNormed, 16) || !aligned(indexQk, 16) || !aligned(cosSin, 16) || !aligned(wQ, 16) ||
+      !aligned(contextLengths, 4))
+    return fail(QSA_E_ALIGN, "%s: T and FP32 arrays must be 16-byte aligned, contextLengths 4-byte", fn);
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  qsa::LaunchQPrep a{dtype == QSA_BF16, qNormed, indexQk, cosSin, contextLengths, wQ, rmsEps,
+                     batchSize, seqLen, d.num_sms, reinterpret_cast<cudaStream_t>(stream)};
+  return launched(fn, qsa::launch_q_prep(a));
+}
+
+QSA_API int qsa_index_k_compress(qsa_dtype_t dtype, void* kbar, const void* indexQk, const float* cosSin,
+                                 const int32_t* contextLengths, const void* wK, float rmsEps,
+                                 int32_t batchSize, int32_t seqLen, int32_t numBlocks, int32_t blockBegin,
+                                 int32_t blockEnd, int32_t pastLen, qsa_stream_t stream) {
+  static const char* fn = "qsa_index_k_compress";
+  int st;
+  if ((st = check_dtype(fn, dtype)) != QSA_OK) return st;
+  if (!kbar || !indexQk || !cosSin || !contextLengths || !wK) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  if (batchSize < 1 || seqLen < 1 || numBlocks < 1)
+    return fail(QSA_E_SHAPE, "%s: batchSize=%d seqLen=%d numBlocks=%d must be >= 1", fn, batchSize, seqLen, numBlocks);
+  if (static_cast<int64_t>(batchSize) * seqLen > INT32_MAX)
+    return fail(QSA_E_SHAPE, "%s: batchSize*seqLen exceeds INT32_MAX", fn);
+  if (blockBegin < 0 || blockBegin > blockEnd || blockEnd > numBlocks || pastLen < 0)
+    return fail(QSA_E_RANGE, "%s: need 0 <= blockBegin=%d <= blockEnd=%d <= numBlocks=%d and pastLen=%d >= 0", fn,
+                blockBegin, blockEnd, numBlocks, pastLen);
+  if (static_cast<int64_t>(numBlocks) * 4 > INT32_MAX)
+    return fail(QSA_E_SHAPE, "%s: 4*numBlocks exceeds INT32_MAX", fn);
+  if (!aligned(kbar, 16) || !aligned(indexQk, 16) || !aligned(cosSin, 16) || !aligned(wK, 16) ||
+      !aligned(contextLengths, 4))
+    return fail(QSA_E_ALIGN, "%s: T and FP32 arrays must be 16-byte aligned, contextLengths 4-byte", fn);
+  if (blockBegin == blockEnd) {
+    g_last_error[0] = '\0';
+    return QSA_OK;
+  }
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  qsa::LaunchKCompress a{dtype == QSA_BF16, kbar, indexQk, cosSin, contextLengths, wK, rmsEps, batchSize, seqLen,
+                         numBlocks, blockBegin, blockEnd, pastLen, d.num_sms,
+                         reinterpret_cast<cudaStream_t>(stream)};
+  return launched(fn, qsa::launch_k_compress(a));
+}
+
+QSA_API int qsa_index_scores(qsa_dtype_t dtype, float* logits, const void* qNormed, const void* kbar,
+                             const int32_t* contextLengths, int32_t batchSize, int32_t seqLen,
+                             int32_t numBlocks, int32_t rowStart, int32_t numRows, qsa_stream_t stream) {
+  static const char* fn = "qsa_index_scores";
+  int st = validate_scores(fn, dtype, logits, qNormed, kbar, contextLengths, batchSize, seqLen, numBlocks,
+                           rowStart, numRows);
+  if (st != QSA_OK) return st;
+  if (numRows == 0) {
+    g_last_error[0] = '\0';
+    return QSA_OK;
+  }
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  qsa::LaunchScores a{dtype == QSA_BF16, logits, qNormed, kbar, contextLengths, batchSize, seqLen,
+                      numBlocks, rowStart, numRows, score_scale(), d.num_sms,
+                      reinterpret_cast<cudaStream_t>(stream)};
+  return launched(fn, qsa::launch_scores_tc(a));
+}
+
+QSA_API int qsa_testing_index_scores_cuda_core(qsa_dtype_t dtype, float* logits, const void* qNormed,
+                                               const void* kbar, const int32_t* contextLengths,
+                                               int32_t batchSize, int32_t seqLen, int32_t numBlocks,
+                                               int32_t rowStart, int32_t numRows, qsa_stream_t stream) {
+  static const char* fn = "qsa_testing_index_scores_cuda_core";
+  int st = validate_scores(fn, dtype, logits, qNormed, kbar, contextLengths, batchSize, seqLen, numBlocks,
+                           rowStart, numRows);
+  if (st != QSA_OK) return st;
+  if (numRows == 0) {
+    g_last_error[0] = '\0';
+    return QSA_OK;
+  }
+  if (numBlocks > 65535 * 128) return fail(QSA_E_SHAPE, "%s: numBlocks too large for the CUDA-core grid", fn);
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  qsa::LaunchScores a{dtype == QSA_BF16, logits, qNormed, kbar, contextLengths, batchSize, seqLen,
+                      numBlocks, rowStart, numRows, score_scale(), d.num_sms,
+                      reinterpret_cast<cudaStream_t>(stream)};
+  return launched(fn, qsa::launch_scores_cc(a));
+}
+
+QSA_API int qsa_device_fault_flags(uint32_t* flags, int clear, qsa_stream_t stream) {
+  static const char* fn = "qsa_device_fault_flags";
+  if (!flags) return fail(QSA_E_NULL, "%s: null flags pointer", fn);
+  DeviceInfo d;
+  int st = current_device(fn, &d);
+  if (st != QSA_OK) return st;
+  cudaError_t e = qsa::read_fault_flags(flags, clear != 0, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(QSA_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  g_last_error[0] = '\0';
+  return QSA_OK;
+}
+
+namespace qsa {
+
+cudaError_t occupancy_blocks_per_sm(const void* kernel, int threads, size_t smem, int* out) {
+  struct Entry {
+    const void* kernel;
+    int device, threads;
+    size_t smem;
+    int blocks;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int used = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  for (int i = 0; i < used; ++i) {
+    if (cache[i].kernel == kernel && cache[i].device == dev && cache[i].threads == threads && cache[i].smem == smem) {
+      *out = cache[i].blocks;
+      return cudaSuccess;
+    }
+  }
+  int blocks = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (blocks < 1) blocks = 1;
+  if (used < 64) cache[used++] = Entry{kernel, dev, threads, smem, blocks};
+  *out = blocks;
+  return cudaSuccess;
+}
+
+}  // namespace qsa

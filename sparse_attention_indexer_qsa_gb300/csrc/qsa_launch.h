@@ -1,0 +1,59 @@
+// Internal launcher interface between the C ABI (qsa_abi.cpp) and the kernels.
+// Arguments arrive here already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace qsa {
+
+struct LaunchQPrep {
+  bool bf16;
+  void* q_normed;
+  const void* index_qk;
+  const float* cos_sin;
+  const int32_t* context_lengths;
+  const void* w_q;
+  float eps;
+  int32_t batch, seq_len;
+  int num_sms;
+  cudaStream_t stream;
+};
+
+struct LaunchKCompress {
+  bool bf16;
+  void* kbar;
+  const void* index_qk;
+  const float* cos_sin;
+  const int32_t* context_lengths;
+  const void* w_k;
+  float eps;
+  int32_t batch, seq_len, num_blocks, block_begin, block_end, past_len;
+  int num_sms;
+  cudaStream_t stream;
+};
+
+struct LaunchScores {
+  bool bf16;
+  float* logits;
+  const void* q_normed;
+  const void* kbar;
+  const int32_t* context_lengths;
+  int32_t batch, seq_len, num_blocks, row_start, num_rows;
+  float scale;  // 1.0f / sqrtf(128.0f), evaluated on the host in binary32
+  int num_sms;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_q_prep(const LaunchQPrep& a);
+cudaError_t launch_k_compress(const LaunchKCompress& a);
+cudaError_t launch_scores_tc(const LaunchScores& a);
+cudaError_t launch_scores_cc(const LaunchScores& a);  // CUDA-core cross-check (testing only)
+
+// Device fault flags (k2_scores_tc.cu): bits set by bounded waits that ran out.
+cudaError_t read_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
+
+// Cached cudaOccupancyMaxActiveBlocksPerMultiprocessor for (kernel, device).
+cudaError_t occupancy_blocks_per_sm(const void* kernel, int threads, size_t smem, int* out);
+
+}  // namespace qsa

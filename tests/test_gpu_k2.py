@@ -1,0 +1,192 @@
+"""GPU parity of K2 (tcgen05 block scoring) against the CPU oracle.
+
+Masks (-FLT_MAX cells, padded rows) must match bit for bit; visible logits within
+the tolerance of tolerance.py ("Qsa Indexer Kernels", launchQsaIndexScores).
+Small shapes are compared element by element on every row; the B=8, S=16384
+scoring workload is compared on sampled rows against the oracle, on every
+element against the independent CUDA-core kernel, and on its mask structure.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tolerance import check_logits, logits_floor
+
+pytestmark = pytest.mark.gpu
+NEG_MAX = np.float32(-np.finfo(np.float32).max)
+
+
+def _gpu():
+    import gpu_util
+    return gpu_util
+
+
+def _rand_inputs(dtype, B, S, NB, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    q = workloads.round_to_t(rng.standard_normal((B, S, 4, 128)) * scale, dtype)
+    kb = workloads.round_to_t(rng.standard_normal((B, NB, 128)) * scale, dtype)
+    return q, kb
+
+
+def _compare(dtype, got, q, kb, ctx, row_start, num_rows):
+    B, S = q.shape[:2]
+    ref = oracle.scores(dtype, q, kb, ctx, row_start, num_rows)
+    rows = np.arange(row_start, row_start + num_rows)
+    b = rows // S
+    fl = logits_floor(q.reshape(B * S, 4, 128)[rows], kb[b], dtype)
+    ok, st = check_logits(got, ref, dtype, fl)
+    print(f"K2 {dtype} B={B} S={S} NB={kb.shape[1]} rows=[{row_start},+{num_rows}): {st}")
+    assert ok, st
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("B,S,NB,ctx", [
+    (1, 64, 16, [50]),            # tiny
+    (2, 1000, 250, [1000, 377]),  # ragged: S % 64 != 0, NB % 128 != 0
+    (1, 777, 300, [700]),         # NB > ceilDiv(S, 4): extra masked columns
+    (3, 130, 33, [130, 0, 1]),    # empty and one-token sequences
+    (1, 4, 1, [4]),
+    (2, 2048, 512, [2048, 1500]), # several g-tiles and token tiles
+])
+def test_scores_match_oracle(dtype, B, S, NB, ctx):
+    g_ = _gpu()
+    q, kb = _rand_inputs(dtype, B, S, NB, seed=S + NB)
+    ctx = np.asarray(ctx, np.int32)
+    qd, kd, cd = g_.dev(q), g_.dev(kb), g_.dev(ctx)
+    got = g_.scores(dtype, qd, kd, cd, B, S, NB, 0, B * S)
+    _compare(dtype, got, q, kb, ctx, 0, B * S)
+    g_.assert_no_device_faults()
+
+
+def test_chunks_equal_one_shot_bitwise():
+    g_ = _gpu()
+    dtype = "bf16"
+    B, S, NB = 3, 700, 175
+    q, kb = _rand_inputs(dtype, B, S, NB, seed=5)
+    ctx = np.array([700, 333, 699], np.int32)
+    qd, kd, cd = g_.dev(q), g_.dev(kb), g_.dev(ctx)
+    full = g_.scores(dtype, qd, kd, cd, B, S, NB, 0, B * S)
+    _compare(dtype, full, q, kb, ctx, 0, B * S)
+    for start, n in ((0, 1), (1, 63), (37, 700), (699, 2), (700, 700), (1337, 763), (2099, 1)):
+        part = g_.scores(dtype, qd, kd, cd, B, S, NB, start, n)
+        assert np.array_equal(part.view(np.uint32), full[start:start + n].view(np.uint32)), (start, n)
+    again = g_.scores(dtype, qd, kd, cd, B, S, NB, 0, B * S)
+    assert np.array_equal(again.view(np.uint32), full.view(np.uint32)), "not deterministic"
+    g_.assert_no_device_faults()
+
+
+def test_nan_in_unread_rows_is_harmless():
+    g_ = _gpu()
+    dtype = "bf16"
+    B, S, NB = 2, 300, 80
+    q, kb = _rand_inputs(dtype, B, S, NB, seed=9)
+    ctx = np.array([250, 0], np.int32)
+    clean = g_.scores(dtype, g_.dev(q), g_.dev(kb), g_.dev(ctx), B, S, NB, 0, B * S)
+    qn, kn = q.copy(), kb.copy()
+    qn[0, 250:] = workloads.NAN_BITS[dtype]
+    qn[1] = workloads.NAN_BITS[dtype]
+    kn[0, 250 // 4:] = workloads.NAN_BITS[dtype]
+    kn[1] = workloads.NAN_BITS[dtype]
+    dirty = g_.scores(dtype, g_.dev(qn), g_.dev(kn), g_.dev(ctx), B, S, NB, 0, B * S)
+    assert np.array_equal(dirty.view(np.uint32), clean.view(np.uint32))
+
+
+@pytest.fixture(scope="module")
+def scoring_pipeline():
+    """B=8, S=16384: indexQk ~ N(0,1) -> GPU K1a/K1b -> qNormed, kbar (as the
+    scoring workload specifies), for ctx = S and for ctx ~ U{1..S}."""
+    import sparse_attention_indexer_qsa_gb300 as qsa
+    g_ = _gpu()
+    out = {}
+    for full in (True, False):
+        wl = workloads.scoring("bf16", full_context=full)
+        d = g_.DevWorkload(wl)
+        B, S, NB = wl.B, wl.S, wl.num_blocks
+        qn = torch.empty((B, S, 4, 128), dtype=torch.bfloat16, device="cuda")
+        kb = torch.empty((B, NB, 128), dtype=torch.bfloat16, device="cuda")
+        qsa.qsa_index_q_prep(qn, d.index_qk, d.cos_sin, d.ctx, d.w_q, wl.eps, B, S)
+        qsa.qsa_index_k_compress(kb, d.index_qk, d.cos_sin, d.ctx, d.w_k, wl.eps, B, S, NB, 0, NB, 0)
+        out[full] = (wl, d, qn, kb)
+    return out
+
+
+@pytest.mark.parametrize("full", [True, False])
+def test_scoring_workload_sampled_rows_and_cross_check(scoring_pipeline, full):
+    import sparse_attention_indexer_qsa_gb300 as qsa
+    wl, d, qn, kb = scoring_pipeline[full]
+    B, S, NB = wl.B, wl.S, wl.num_blocks
+    rows = B * S
+    logits = torch.empty((rows, NB), dtype=torch.float32, device="cuda")
+    qsa.qsa_index_scores(logits, qn, kb, d.ctx, B, S, NB, 0, rows)
+    torch.cuda.synchronize()
+    assert qsa.qsa_device_fault_flags() == 0
+    q_host = qn.view(torch.int16).cpu().numpy().view(np.uint16)
+    kb_host = kb.view(torch.int16).cpu().numpy().view(np.uint16)
+    ctx = wl.context_lengths
+    # sampled rows, element by element against the oracle (edges of tiles and sequences)
+    rng = np.random.default_rng(44)
+    picks = set(rng.integers(0, rows, 96).tolist())
+    for b in (0, B - 1):
+        for t in (0, 1, 2, 3, 4, 63, 64, 65, 511, 512, S // 2, S - 2, S - 1):
+            picks.add(b * S + t)
+        c = int(ctx[b])
+        for t in (c - 2, c - 1, c, c + 1):
+            if 0 <= t < S:
+                picks.add(b * S + t)
+    picks = sorted(picks)
+    got = logits[picks].cpu().numpy()
+    for i, r in enumerate(picks):
+        b, t = divmod(r, S)
+        ref = oracle.scores_row("bf16", q_host[b, t], kb_host[b], t, int(ctx[b]))
+        fl = logits_floor(q_host[b, t][None], kb_host[b], "bf16")
+        ok, st = check_logits(got[i][None], ref[None], "bf16", fl)
+        assert ok, (r, st)
+    # structure on every row: row t shows min(NB, (t+1)//4) visible blocks iff t < ctx_b
+    t = torch.arange(S, device="cuda")
+    masked = logits.view(B, S, NB) == float(NEG_MAX)
+    nvis = torch.where(t[None, :] < d.ctx[:, None].long(), torch.clamp((t + 1) // 4, max=NB)[None, :],
+                       torch.zeros_like(t)[None, :])
+    assert torch.equal((~masked).sum(-1), nvis), "visible-count structure differs"
+    g_idx = torch.arange(NB, device="cuda")
+    assert torch.equal(~masked, g_idx[None, None, :] < nvis[:, :, None]), "mask positions differ"
+    vis_vals = logits.view(B, S, NB)[~masked]
+    assert bool(torch.isfinite(vis_vals).all()) and bool((vis_vals >= 0).all())
+    # every element against the independent CUDA-core kernel
+    cc = torch.empty_like(logits)
+    qsa.qsa_testing_index_scores_cuda_core(cc, qn, kb, d.ctx, B, S, NB, 0, rows)
+    torch.cuda.synchronize()
+    assert torch.equal(cc == float(NEG_MAX), masked.view(rows, NB))
+    qa = qn.float().abs().sum(2)                                       # [B, S, 128]
+    ka = kb.float().abs()                                              # [B, NB, 128]
+    worst = 0.0
+    for b in range(B):
+        fl = torch.matmul(qa[b], ka[b].T) * (2.0 ** -16) / np.sqrt(128.0)   # [S, NB]
+        x = logits.view(B, S, NB)[b]
+        y = cc.view(B, S, NB)[b]
+        vis = x != float(NEG_MAX)
+        # both sides carry their own reordering error: twice the floor, plus one bf16 ulp
+        tol = (2.0 ** -7) * y.abs() + 2 * fl
+        err = (x - y).abs()
+        assert bool((err[vis] <= tol[vis]).all()), f"sequence {b}: tcgen05 vs CUDA-core mismatch"
+        worst = max(worst, float((err[vis] / torch.clamp(y[vis].abs(), min=1e-30)).max()))
+    print(f"K2 scoring full={full}: max rel diff tcgen05 vs CUDA-core {worst:.3e}")
+    del cc, logits
+    torch.cuda.empty_cache()
+
+
+def test_scoring_workload_chunked_equals_one_shot(scoring_pipeline):
+    import sparse_attention_indexer_qsa_gb300 as qsa
+    wl, d, qn, kb = scoring_pipeline[False]
+    B, S, NB = wl.B, wl.S, wl.num_blocks
+    rows = B * S
+    one = torch.empty((rows, NB), dtype=torch.float32, device="cuda")
+    qsa.qsa_index_scores(one, qn, kb, d.ctx, B, S, NB, 0, rows)
+    chunk = 8192
+    part = torch.empty((chunk, NB), dtype=torch.float32, device="cuda")
+    for start in range(0, rows, chunk * 5):       # every fifth 8192-row chunk
+        qsa.qsa_index_scores(part, qn, kb, d.ctx, B, S, NB, start, chunk)
+        torch.cuda.synchronize()
+        assert torch.equal(part.view(torch.int32), one[start:start + chunk].view(torch.int32)), start
+    assert qsa.qsa_device_fault_flags() == 0
