@@ -29,7 +29,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "indexer rows/s and achieved HBM GB/s (K1a, K1b) vs 8 TB/s at 1 GB300"
 UNIT = "rows/s"
-WORKLOAD = "qsa indexer prefill step (K1a+K1b+K2), B=8 S=16384 bf16, ctx=S, N(0,1) indexQk"
+WORKLOAD = "qsa indexer prefill step (K1a+K1b+K2), B={B} S=16384 bf16, ctx=S, N(0,1) indexQk"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -213,7 +213,7 @@ def run_reference(args, rank: int) -> None:
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * wl.B * wl.S / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": wl.B, "S": wl.S, "num_blocks": wl.num_blocks},
+        "config": {"workload": WORKLOAD.format(B=wl.B), "B": wl.B, "S": wl.S, "num_blocks": wl.num_blocks},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": res["sample"]},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -228,7 +228,7 @@ def run_ours(args, rank: int, world: int) -> None:
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
-    wl = workloads.scoring("bf16", seed=4 + rank, full_context=True)
+    wl = workloads.scoring("bf16", seed=4 + rank, B=args.batch, full_context=True)
     B, S, NB = wl.B, wl.S, wl.num_blocks
     rows = B * S
     def host(a):
@@ -303,7 +303,7 @@ def run_ours(args, rank: int, world: int) -> None:
         ms_total = start.elapsed_time(end)
 
         # ---- end-to-end through the public API with host buffers
-        K_e2e = max(3, min(K, 20))
+        K_e2e = 0 if args.no_e2e else max(3, min(K, 20))
         h_iq = host(wl.index_qk).pin_memory()
         h_cs = host(wl.cos_sin).pin_memory()
         h_ctx = host(wl.context_lengths).pin_memory()
@@ -326,7 +326,8 @@ def run_ours(args, rank: int, world: int) -> None:
             qsa.qsa_index_scores(logits, qn, kb, d_ctx, B, S, NB, 0, rows, stream=sp, dtype="bf16")
             h_logits.copy_(logits, non_blocking=True)
 
-        e2e_step()
+        if K_e2e:
+            e2e_step()
         torch.cuda.synchronize()
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -337,7 +338,7 @@ def run_ours(args, rank: int, world: int) -> None:
         e1.record(stream)
         e1.synchronize()
         barrier()
-        ms_e2e = e0.elapsed_time(e1) / K_e2e
+        ms_e2e = e0.elapsed_time(e1) / K_e2e if K_e2e else float("nan")
     torch.cuda.synchronize()
     faults = qsa.qsa_device_fault_flags()
 
@@ -385,7 +386,7 @@ def run_ours(args, rank: int, world: int) -> None:
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "S": S, "num_blocks": NB, "rows_per_step": rows,
+        "config": {"workload": WORKLOAD.format(B=B), "B": B, "S": S, "num_blocks": NB, "rows_per_step": rows,
                    "k2_row_chunk": rows,
                    "l2": "inputs larger than L2 (indexQk 168 MB, qNormed 134 MB) and each step writes "
                          "2.15 GB of logits, which evicts L2 between steps"},
@@ -411,6 +412,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--batch", type=int, default=8,
+                    help="sequences per step (8 is the scoring workload; smaller for profiler captures)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
