@@ -11,8 +11,15 @@
 
 namespace qsa {
 
+#ifndef QSA_K1A_ROWS
+#define QSA_K1A_ROWS 2
+#endif
+#ifndef QSA_K1A_MINB
+#define QSA_K1A_MINB 3
+#endif
+
 template <class T, int ROWS>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, QSA_K1A_MINB)
 k1a_qprep_kernel(uint16_t* __restrict__ q_normed, const uint16_t* __restrict__ index_qk,
                  const float* __restrict__ cos_sin, const int32_t* __restrict__ context_lengths,
                  const uint16_t* __restrict__ w_q, float eps, int32_t batch, int32_t seq_len) {
@@ -21,8 +28,9 @@ k1a_qprep_kernel(uint16_t* __restrict__ q_normed, const uint16_t* __restrict__ i
   const int j = lane & 7;
   const int ca = chunk_a(j);
   const int cb = chunk_b(j);
-  float ga[8], gb[8];
-  load_gamma<T>(w_q, j, ga, gb);
+  __shared__ __align__(16) float g1[kHeadDim];
+  stage_gamma<T>(w_q, g1);
+  __syncthreads();
 
   const int32_t rows = batch * seq_len;
   const int32_t warp = static_cast<int32_t>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
@@ -30,7 +38,7 @@ k1a_qprep_kernel(uint16_t* __restrict__ q_normed, const uint16_t* __restrict__ i
 
   for (int32_t base = warp * ROWS; base < rows; base += nwarps * ROWS) {
     uint4 va[ROWS], vb[ROWS];
-    RopeCS cs[ROWS];
+    RopeCS cs[ROWS] = {};
     bool valid[ROWS];
 #pragma unroll
     for (int k = 0; k < ROWS; ++k) {
@@ -59,7 +67,7 @@ k1a_qprep_kernel(uint16_t* __restrict__ q_normed, const uint16_t* __restrict__ i
         float a[8], bv[8];
         unpack8<T>(va[k], a);
         unpack8<T>(vb[k], bv);
-        norm_rope_group<T>(a, bv, ga, gb, eps, cs[k], j, oa, ob);
+        norm_rope_group<T>(a, bv, g1, eps, cs[k], j, oa, ob);
       }
       st_v4(dst + ca, oa);
       st_v4(dst + cb, ob);
@@ -68,7 +76,7 @@ k1a_qprep_kernel(uint16_t* __restrict__ q_normed, const uint16_t* __restrict__ i
 }
 
 namespace {
-constexpr int kK1aRows = 2;
+constexpr int kK1aRows = QSA_K1A_ROWS;
 constexpr int kK1aThreads = 256;
 
 template <class T>

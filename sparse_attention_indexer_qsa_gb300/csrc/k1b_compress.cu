@@ -14,8 +14,12 @@
 
 namespace qsa {
 
+#ifndef QSA_K1B_MINB
+#define QSA_K1B_MINB 3
+#endif
+
 template <class T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, QSA_K1B_MINB)
 k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ index_qk,
                     const float* __restrict__ cos_sin, const int32_t* __restrict__ context_lengths,
                     const uint16_t* __restrict__ w_k, float eps, int32_t batch, int32_t seq_len,
@@ -24,8 +28,9 @@ k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ in
   const int j = lane & 7;
   const int ca = chunk_a(j);
   const int cb = chunk_b(j);
-  float ga[8], gb[8];
-  load_gamma<T>(w_k, j, ga, gb);
+  __shared__ __align__(16) float g1[kHeadDim];
+  stage_gamma<T>(w_k, g1);
+  __syncthreads();
 
   const int32_t nb = block_end - block_begin;
   const int64_t units = static_cast<int64_t>(batch) * nb;
@@ -76,7 +81,7 @@ k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ in
       for (int e = 0; e < 8; ++e) { a[e] = 0.0f; bv[e] = 0.0f; }
     }
     uint4 oa, ob;
-    norm_rope_group<T>(a, bv, ga, gb, eps, cs, j, oa, ob);
+    norm_rope_group<T>(a, bv, g1, eps, cs, j, oa, ob);
     if (active) {
       if (!valid) { oa = make_uint4(0u, 0u, 0u, 0u); ob = oa; }
       uint16_t* dst = kbar + (static_cast<int64_t>(b) * num_blocks + g) * kHeadDim;

@@ -15,9 +15,9 @@
 // Persistent CTA per SM, warp-specialised:
 //   warp 0     TMA producer (q tile once per work unit, kbar tiles per MMA g-tile)
 //   warp 1     TMEM allocator + single-thread MMA issuer
-//   warps 2-9  epilogue (two warps per TMEM sub-partition, one per token half)
-// A work unit is (sequence b, 64-token tile, up to 8 g-tiles of 128 blocks).  Tiles
-// whose blocks are all masked for every stored row skip the MMA and only store
+//   warps 2+   epilogue (kEpiWarps: two or four per TMEM sub-partition, each a token slice)
+// A work unit is (sequence b, 64-token tile, every n_groups-th g-tile of 128 blocks).
+// Tiles whose blocks are all masked for every stored row skip the MMA and only store
 // -FLT_MAX.  Rows outside the chunk or the sequence are computed but never stored;
 // TMA reads past the end of a sequence's q or kbar rows return zeros.
 //
@@ -45,7 +45,13 @@ constexpr int kGTilesPerUnit = 8;
 constexpr int kQStages = 2;
 constexpr int kKStages = 3;
 constexpr int kAccStages = 2;
-constexpr int kEpiWarps = 8;
+#ifndef QSA_K2_EPI_WARPS
+#define QSA_K2_EPI_WARPS 8
+#endif
+constexpr int kEpiWarps = QSA_K2_EPI_WARPS;         // 8 or 16
+static_assert(kEpiWarps == 8 || kEpiWarps == 16, "epilogue warps: two or four per TMEM sub-partition");
+constexpr int kTokPerWarp = kTokTile / (kEpiWarps / 4);  // tokens of a tile per epilogue warp
+constexpr int kLdPerWarp = kTokPerWarp / 8;              // 32-column TMEM loads (8 tokens each)
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
@@ -91,9 +97,14 @@ struct Params {
   float scale;
 };
 
+// A work unit is (sequence b, 64-token tile at t0, g-tile group grp).  Group grp owns
+// the interleaved g-tiles gt(i) = grp + n_groups * i, so every group of a token tile
+// gets an even share of the (causal, prefix-shaped) MMA tiles and the persistent
+// CTAs stay balanced.
 struct Unit {
-  int32_t b, t0;
-  int32_t gt_begin, gt_end, gt_mma_end;  // g-tiles [gt_begin, gt_end); MMA on [gt_begin, gt_mma_end)
+  int32_t b, t0, grp;
+  int32_t n_tiles;   // g-tiles of this unit: i in [0, n_tiles)
+  int32_t n_mma;     // the first n_mma of them need the MMA; the rest are fully masked
   int32_t t_lo, t_hi;                    // stored rows [t_lo, t_hi)
   int32_t t_vis_hi;                      // rows below this (and >= t_lo) are unpadded
   int64_t row_base;                      // chunk-local row of (b, t = 0)
@@ -102,12 +113,11 @@ struct Unit {
 __device__ __forceinline__ Unit unit_info(const Params& p, int32_t u) {
   Unit x;
   const int32_t tq = u / p.n_groups;
-  const int32_t grp = u - tq * p.n_groups;
+  x.grp = u - tq * p.n_groups;
   const int32_t tile = p.tile_lo + tq;
   x.b = tile / p.tiles_per_batch;
   x.t0 = (tile - x.b * p.tiles_per_batch) * kTokTile;
-  x.gt_begin = grp * kGTilesPerUnit;
-  x.gt_end = min(p.n_gtiles, x.gt_begin + kGTilesPerUnit);
+  x.n_tiles = (p.n_gtiles - x.grp + p.n_groups - 1) / p.n_groups;
   const int64_t bs = static_cast<int64_t>(x.b) * p.seq_len;
   const int64_t c_lo = static_cast<int64_t>(p.row_start) - bs;
   const int64_t c_hi = static_cast<int64_t>(p.row_start) + p.num_rows - bs;
@@ -116,17 +126,20 @@ __device__ __forceinline__ Unit unit_info(const Params& p, int32_t u) {
                                     min(c_hi, static_cast<int64_t>(p.seq_len))));
   const int32_t ctx = max(__ldg(p.ctx + x.b), 0);
   x.t_vis_hi = min(x.t_hi, ctx);
-  // The last unpadded row t_vis_hi - 1 sees blocks g < t_vis_hi / 4; visibility only
-  // shrinks with g, so the MMA g-tiles are a prefix of the unit's g-tiles.
-  int32_t mma_end = x.gt_begin;
+  // The last unpadded row t_vis_hi - 1 sees blocks g < t_vis_hi / 4, so g-tiles
+  // gt < lim need the MMA; visibility only shrinks with g, so within the unit they
+  // are the prefix i < n_mma.
+  x.n_mma = 0;
   if (x.t_vis_hi > x.t_lo) {
-    const int32_t nvis = x.t_vis_hi / 4;
-    mma_end = min(x.gt_end, (nvis + kGTile - 1) / kGTile);
-    mma_end = max(mma_end, x.gt_begin);
+    const int32_t lim = (x.t_vis_hi / 4 + kGTile - 1) / kGTile;
+    x.n_mma = max(0, min(x.n_tiles, (lim - x.grp + p.n_groups - 1) / p.n_groups));
   }
-  x.gt_mma_end = mma_end;
   x.row_base = bs - p.row_start;
   return x;
+}
+
+__device__ __forceinline__ int32_t unit_gtile(const Params& p, const Unit& x, int32_t i) {
+  return x.grp + p.n_groups * i;
 }
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -151,6 +164,46 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (ptx::global_timer_ns() - start > kDrainLimitNs) {
       atomicOr(&g_fault_flags, kFaultDrain);
       return;
+    }
+  }
+}
+
+// Logits are written once and never re-read by this kernel.  Policy 1 marks them
+// evict-first in L2 (st.global.cs) so q and kbar tiles stay resident.
+#ifndef QSA_K2_STORE_POLICY
+#define QSA_K2_STORE_POLICY 1
+#endif
+__device__ __forceinline__ void st_f32(float* p, float v) {
+#if QSA_K2_STORE_POLICY == 1
+  asm volatile("st.global.cs.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
+#else
+  asm volatile("st.global.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
+#endif
+}
+
+// relu per head, ascending-h sum, scale after the sum ("Qsa Indexer Kernels",
+// launchQsaIndexScores): r holds 8 tokens x 4 heads of one block g.
+__device__ __forceinline__ float head_sum(const uint32_t (&r)[32], int k) {
+  float v = __fadd_rn(fmaxf(0.0f, __uint_as_float(r[4 * k + 0])), fmaxf(0.0f, __uint_as_float(r[4 * k + 1])));
+  v = __fadd_rn(v, fmaxf(0.0f, __uint_as_float(r[4 * k + 2])));
+  return __fadd_rn(v, fmaxf(0.0f, __uint_as_float(r[4 * k + 3])));
+}
+
+// 8 consecutive token rows, all stored and all visible
+__device__ __forceinline__ void store8_visible(float* out, const uint32_t (&r)[32], int64_t nb, float scale) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) st_f32(out + k * nb, __fmul_rn(head_sum(r, k), scale));
+}
+
+// 8 consecutive token rows from t: store only rows of the chunk, mask per element
+__device__ __forceinline__ void store8_checked(float* out, const uint32_t (&r)[32], int64_t nb, float scale,
+                                               int32_t t, int32_t g, const Unit& x) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int32_t tk = t + k;
+    if (tk >= x.t_lo && tk < x.t_hi) {
+      const bool vis = tk < x.t_vis_hi && g < (tk + 1) / 4;
+      st_f32(out + k * nb, vis ? __fmul_rn(head_sum(r, k), scale) : -FLT_MAX);
     }
   }
 }
@@ -205,7 +258,7 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       int qcnt = 0, kcnt = 0;
       for (int32_t u = blockIdx.x; u < p.units; u += gridDim.x) {
         const Unit x = unit_info(p, u);
-        if (x.gt_mma_end <= x.gt_begin) continue;
+        if (x.n_mma == 0) continue;
         const int qs = qcnt % kQStages;
         if (!wait_bounded(bar(kBarQEmpty + qs), ((qcnt / kQStages) & 1) ^ 1, abort_flag, kFaultProducer)) break;
         ptx::mbar_arrive_expect_tx(bar(kBarQFull + qs), kQBytes);
@@ -214,7 +267,8 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         ptx::tma_load_3d(qdst + kQHalfBytes, &tmap_q, bar(kBarQFull + qs), 64, 4 * x.t0, x.b);
         ++qcnt;
         bool ok = true;
-        for (int gt = x.gt_begin; gt < x.gt_mma_end; ++gt) {
+        for (int i = 0; i < x.n_mma; ++i) {
+          const int32_t gt = unit_gtile(p, x, i);
           const int ks = kcnt % kKStages;
           if (!wait_bounded(bar(kBarKEmpty + ks), ((kcnt / kKStages) & 1) ^ 1, abort_flag, kFaultProducer)) {
             ok = false;
@@ -251,12 +305,12 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       bool ok = true;
       for (int32_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         const Unit x = unit_info(p, u);
-        if (x.gt_mma_end <= x.gt_begin) continue;
+        if (x.n_mma == 0) continue;
         const int qs = qcnt % kQStages;
         if (!wait_bounded(bar(kBarQFull + qs), (qcnt / kQStages) & 1, abort_flag, kFaultMma)) break;
         ptx::tc_fence_after();
         const uint32_t qaddr = base + kOffQ + qs * kQBytes;
-        for (int gt = x.gt_begin; gt < x.gt_mma_end; ++gt) {
+        for (int i = 0; i < x.n_mma; ++i) {
           const int ks = kcnt % kKStages;
           const int as = acnt % kAccStages;
           if (!wait_bounded(bar(kBarKFull + ks), (kcnt / kKStages) & 1, abort_flag, kFaultMma) ||
@@ -289,57 +343,70 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
   } else {
     // --------------------------------------------------------------- epilogue
+    // Warp ew reads TMEM sub-partition sp = warp % 4 (blocks g0 + 32*sp + lane) for
+    // the token slice [kTokPerWarp*grp, +kTokPerWarp) of the tile.  The common case, a
+    // warp sub-tile entirely inside the chunk, the sequence's valid rows and the
+    // visible triangle, takes a predicate-free path; edges take the checked path.
     const int ew = warp - 2;
-    const int sp = warp & 3;       // TMEM sub-partition this warp may access
-    const int half = ew >> 2;      // token half: tokens [32*half, 32*half + 32) of the tile
-    const int32_t g_in_tile = 32 * sp + lane;
-    const float neg_max = -FLT_MAX;
+    const int sp = warp & 3;
+    const int grp = ew >> 2;
     const int64_t nb = p.num_blocks;
+    const float scale = p.scale;
     int acnt = 0;
     bool ok = true;
     for (int32_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
       const Unit x = unit_info(p, u);
-      const int32_t tb = x.t0 + 32 * half;  // first token of this warp's half
-      for (int gt = x.gt_begin; gt < x.gt_end; ++gt) {
-        const int32_t g = gt * kGTile + g_in_tile;
+      const int32_t tb = x.t0 + kTokPerWarp * grp;  // first token of this warp's slice
+      const bool rows_full = x.t_lo <= tb && tb + kTokPerWarp <= x.t_hi;
+      for (int i = 0; i < x.n_tiles; ++i) {
+        const int32_t gw = unit_gtile(p, x, i) * kGTile + 32 * sp;    // first block of this warp
+        const int32_t g = gw + lane;
         const bool g_ok = g < p.num_blocks;
-        float* out = p.logits + x.row_base * nb + g;
-        if (gt < x.gt_mma_end) {
+        const bool cols_full = gw + 32 <= p.num_blocks;
+        float* out = p.logits + (x.row_base + tb) * nb + g;  // row of token tb
+        if (i < x.n_mma) {
           const int as = acnt % kAccStages;
           if (!wait_bounded(bar(kBarAccFull + as), (acnt / kAccStages) & 1, abort_flag, kFaultEpilogue)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
+          // every (t, g) of the sub-tile visible: g <= gw+31 < (tb+1)/4 <= (t+1)/4, t < ctx
+          const bool interior = rows_full && cols_full && tb + kTokPerWarp <= x.t_vis_hi &&
+                                gw + 31 < (tb + 1) / 4;
           const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * sp) << 16) +
-                                 static_cast<uint32_t>(as) * kAccCols + 128u * half;
+                                 static_cast<uint32_t>(as) * kAccCols + 4u * kTokPerWarp * grp;
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            ptx::tmem_ld_32x32b_x32(taddr + 32u * c, r);
+          for (int c = 0; c < kLdPerWarp; c += 2) {
+            uint32_t r0[32], r1[32];
+            ptx::tmem_ld_32x32b_x32(taddr + 32u * c, r0);
+            ptx::tmem_ld_32x32b_x32(taddr + 32u * (c + 1), r1);
             ptx::tmem_ld_wait();
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int32_t t = tb + 8 * c + k;
-              if (g_ok && t >= x.t_lo && t < x.t_hi) {
-                float v = __fadd_rn(fmaxf(0.0f, __uint_as_float(r[4 * k + 0])),
-                                    fmaxf(0.0f, __uint_as_float(r[4 * k + 1])));
-                v = __fadd_rn(v, fmaxf(0.0f, __uint_as_float(r[4 * k + 2])));
-                v = __fadd_rn(v, fmaxf(0.0f, __uint_as_float(r[4 * k + 3])));
-                const bool vis = t < x.t_vis_hi && g < (t + 1) / 4;
-                out[static_cast<int64_t>(t) * nb] = vis ? __fmul_rn(v, p.scale) : neg_max;
-              }
+            if (interior) {
+              store8_visible(out, r0, nb, scale);
+              store8_visible(out + 8 * nb, r1, nb, scale);
+            } else if (g_ok) {
+              store8_checked(out, r0, nb, scale, tb + 8 * c, g, x);
+              store8_checked(out + 8 * nb, r1, nb, scale, tb + 8 * c + 8, g, x);
             }
+            out += 16 * nb;
           }
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(bar(kBarAccEmpty + as));
           ++acnt;
+        } else if (rows_full && cols_full) {
+#pragma unroll 8
+          for (int k = 0; k < kTokPerWarp; ++k) {
+            st_f32(out, -FLT_MAX);
+            out += nb;
+          }
         } else if (g_ok) {
 #pragma unroll 4
-          for (int k = 0; k < 32; ++k) {
+          for (int k = 0; k < kTokPerWarp; ++k) {
             const int32_t t = tb + k;
-            if (t >= x.t_lo && t < x.t_hi) out[static_cast<int64_t>(t) * nb] = neg_max;
+            if (t >= x.t_lo && t < x.t_hi) st_f32(out, -FLT_MAX);
+            out += nb;
           }
         }
       }

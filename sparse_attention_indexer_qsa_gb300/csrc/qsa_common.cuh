@@ -21,6 +21,7 @@ constexpr int kCsWidth = 64;
 // ---------------------------------------------------------------- element types
 
 struct Bf16 {
+  static __device__ __forceinline__ float one(uint16_t u) { return __uint_as_float(static_cast<uint32_t>(u) << 16); }
   static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
   static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
   static __device__ __forceinline__ uint32_t pack(float a, float b) {  // a -> low half
@@ -33,6 +34,7 @@ struct Bf16 {
 };
 
 struct F16 {
+  static __device__ __forceinline__ float one(uint16_t u) { return __half2float(__ushort_as_half(u)); }
   static __device__ __forceinline__ float lo(uint32_t w) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
   }
@@ -105,17 +107,11 @@ __device__ __forceinline__ void st_v4(void* p, const uint4& v) {
 __device__ __forceinline__ int chunk_a(int j) { return j < 4 ? 8 * j : 64 + 8 * (j - 4); }
 __device__ __forceinline__ int chunk_b(int j) { return j < 4 ? 32 + 8 * j : 96 + 8 * (j - 4); }
 
-// (1 + w) for the lane's 16 dims; w is the raw checkpoint gamma [128] in T.
+// (1 + w) for all 128 dims into shared memory, once per CTA (w is the raw
+// checkpoint gamma [128] in T).  Call before the CTA's first __syncthreads().
 template <class T>
-__device__ __forceinline__ void load_gamma(const uint16_t* w, int j, float (&ga)[8], float (&gb)[8]) {
-  float wa[8], wb[8];
-  unpack8<T>(ld_cached_v4(w + chunk_a(j)), wa);
-  unpack8<T>(ld_cached_v4(w + chunk_b(j)), wb);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    ga[e] = __fadd_rn(1.0f, wa[e]);
-    gb[e] = __fadd_rn(1.0f, wb[e]);
-  }
+__device__ __forceinline__ void stage_gamma(const uint16_t* w, float* g1) {
+  for (int d = threadIdx.x; d < kHeadDim; d += blockDim.x) g1[d] = __fadd_rn(1.0f, T::one(w[d]));
 }
 
 // The lane's cos/sin values for rope position row `cs` (only lanes j < 4 rotate).
@@ -142,8 +138,7 @@ __device__ __forceinline__ RopeCS load_rope(const float* cs, int j) {
 // Every lane of the warp must call this (it shuffles with a full mask).
 template <class T>
 __device__ __forceinline__ void norm_rope_group(const float (&a)[8], const float (&b)[8],
-                                                const float (&ga)[8], const float (&gb)[8],
-                                                float eps, const RopeCS& cs, int j,
+                                                const float* g1, float eps, const RopeCS& cs, int j,
                                                 uint4& out_a, uint4& out_b) {
   float s = 0.0f;
 #pragma unroll
@@ -155,6 +150,11 @@ __device__ __forceinline__ void norm_rope_group(const float (&a)[8], const float
   s += __shfl_xor_sync(0xffffffffu, s, 1);
   const float mean_sq = __fmul_rn(s, 1.0f / 128.0f);  // exact power-of-two scaling
   const float r = rsqrtf(__fadd_rn(mean_sq, eps));
+  const float4* ga4 = reinterpret_cast<const float4*>(g1 + chunk_a(j));
+  const float4* gb4 = reinterpret_cast<const float4*>(g1 + chunk_b(j));
+  const float4 ga0 = ga4[0], ga1 = ga4[1], gb0 = gb4[0], gb1 = gb4[1];
+  const float ga[8] = {ga0.x, ga0.y, ga0.z, ga0.w, ga1.x, ga1.y, ga1.z, ga1.w};
+  const float gb[8] = {gb0.x, gb0.y, gb0.z, gb0.w, gb1.x, gb1.y, gb1.z, gb1.w};
   float ya[8], yb[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
