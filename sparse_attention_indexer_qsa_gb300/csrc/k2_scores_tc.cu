@@ -12,8 +12,11 @@
 // from 4 consecutive columns, applies relu per head, sums them in ascending h, scales
 // and masks, and the 32 lanes of a warp write 32 consecutive logits (128 bytes).
 //
-// Persistent CTA per SM, warp-specialised:
-//   warp 0     TMA producer (q tile once per work unit, kbar tiles per MMA g-tile)
+// Persistent CTA per SM, warp-specialised, with work units taken dynamically in
+// address order from a device-wide counter (statically assigned persistent CTAs
+// drift apart and spread the live write front over DRAM, which costs ~15% of HBM
+// write bandwidth on GB300):
+//   warp 0     scheduler + TMA producer (q tile once per unit, kbar tiles per MMA g-tile)
 //   warp 1     TMEM allocator + single-thread MMA issuer
 //   warps 2+   epilogue (kEpiWarps: two or four per TMEM sub-partition, each a token slice)
 // A work unit is (sequence b, 64-token tile, every n_groups-th g-tile of 128 blocks).
@@ -36,12 +39,23 @@ namespace qsa {
 
 __device__ uint32_t g_fault_flags;
 
+// Work-unit scheduler state of the scoring kernel: kSchedSlots independent
+// {next unit, CTAs finished} counter pairs.  Each launch takes the next slot of its
+// device (so up to kSchedSlots launches may execute concurrently), CTAs fetch work
+// units from it in address order, and the last CTA to finish puts the slot back to
+// zero for its next user.  Zero-initialised at module load; never allocated.
+constexpr int kSchedSlots = 64;
+__device__ __align__(256) uint32_t g_k2_sched[kSchedSlots * 2];
+
 namespace k2 {
 
 constexpr int kTokTile = 64;                  // tokens per tile
 constexpr int kN = kTokTile * 4;              // MMA N: token x head rows
 constexpr int kGTile = 128;                   // MMA M: kbar blocks per tile
-constexpr int kGTilesPerUnit = 8;
+#ifndef QSA_K2_GTILES_PER_UNIT
+#define QSA_K2_GTILES_PER_UNIT 8
+#endif
+constexpr int kGTilesPerUnit = QSA_K2_GTILES_PER_UNIT;
 constexpr int kQStages = 2;
 constexpr int kKStages = 3;
 constexpr int kAccStages = 2;
@@ -68,12 +82,19 @@ constexpr int kBarKFull = kBarQEmpty + kQStages;
 constexpr int kBarKEmpty = kBarKFull + kKStages;
 constexpr int kBarAccFull = kBarKEmpty + kKStages;
 constexpr int kBarAccEmpty = kBarAccFull + kAccStages;
-constexpr int kBarDrain = kBarAccEmpty + kAccStages;
+constexpr int kSchedStages = 4;                 // work units published ahead by the producer
+constexpr int kBarSchedFull = kBarAccEmpty + kAccStages;
+constexpr int kBarSchedEmpty = kBarSchedFull + kSchedStages;
+constexpr int kBarDrain = kBarSchedEmpty + kSchedStages;
 constexpr int kNumBars = kBarDrain + 1;
-constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr uint32_t kUnitBytes = 48;             // sizeof(Unit), checked below
+constexpr uint32_t kOffRing = (kOffBar + kNumBars * 8 + 15u) & ~15u;  // 16-byte aligned entries
+constexpr uint32_t kOffTmemSlot = kOffRing + kSchedStages * kUnitBytes;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
 constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;  // + slack to align the base to 1024
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+static_assert(kOffRing % 16 == 0 && kOffBar % 8 == 0 && kOffQ % 1024 == 0 && kOffK % 1024 == 0,
+              "shared-memory regions misaligned");
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
@@ -85,6 +106,7 @@ enum : uint32_t {
 };
 
 struct Params {
+  uint32_t* sched;          // this launch's scheduler slot: {next unit, CTAs finished}
   float* logits;
   const int32_t* ctx;
   int32_t batch, seq_len, num_blocks, row_start, num_rows;
@@ -95,14 +117,15 @@ struct Params {
   int32_t units;
   uint32_t idesc;
   float scale;
+  int32_t vec_fill;         // logits rows are 16-byte aligned: fully masked sub-tiles use v4 stores
 };
 
 // A work unit is (sequence b, 64-token tile at t0, g-tile group grp).  Group grp owns
 // the interleaved g-tiles gt(i) = grp + n_groups * i, so every group of a token tile
 // gets an even share of the (causal, prefix-shaped) MMA tiles and the persistent
 // CTAs stay balanced.
-struct Unit {
-  int32_t b, t0, grp;
+struct alignas(16) Unit {
+  int32_t b, t0, grp;       // b < 0: no more work
   int32_t n_tiles;   // g-tiles of this unit: i in [0, n_tiles)
   int32_t n_mma;     // the first n_mma of them need the MMA; the rest are fully masked
   int32_t t_lo, t_hi;                    // stored rows [t_lo, t_hi)
@@ -137,6 +160,8 @@ __device__ __forceinline__ Unit unit_info(const Params& p, int32_t u) {
   x.row_base = bs - p.row_start;
   return x;
 }
+
+static_assert(sizeof(Unit) == kUnitBytes, "scheduler ring entry size");
 
 __device__ __forceinline__ int32_t unit_gtile(const Params& p, const Unit& x, int32_t i) {
   return x.grp + p.n_groups * i;
@@ -173,6 +198,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 #ifndef QSA_K2_STORE_POLICY
 #define QSA_K2_STORE_POLICY 1
 #endif
+__device__ __forceinline__ void st_f32x4_neg_max(float* p) {
+  const float v = -FLT_MAX;
+#if QSA_K2_STORE_POLICY == 1
+  asm volatile("st.global.cs.v4.f32 [%0], {%1,%1,%1,%1};" :: "l"(p), "f"(v) : "memory");
+#else
+  asm volatile("st.global.v4.f32 [%0], {%1,%1,%1,%1};" :: "l"(p), "f"(v) : "memory");
+#endif
+}
+
 __device__ __forceinline__ void st_f32(float* p, float v) {
 #if QSA_K2_STORE_POLICY == 1
   asm volatile("st.global.cs.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
@@ -189,10 +223,44 @@ __device__ __forceinline__ float head_sum(const uint32_t (&r)[32], int k) {
   return __fadd_rn(v, fmaxf(0.0f, __uint_as_float(r[4 * k + 3])));
 }
 
-// 8 consecutive token rows, all stored and all visible
+// Two rounded binary32 operations per instruction (add.rn.f32x2 / mul.rn.f32x2):
+// lane-wise identical to the scalar forms.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+  return v;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t c;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(c) : "l"(a), "l"(b));
+  return c;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t c;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(c) : "l"(a), "l"(b));
+  return c;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ float relu_bits(uint32_t x) { return fmaxf(0.0f, __uint_as_float(x)); }
+
+// 8 consecutive token rows, all stored and all visible.  Tokens k and k+1 share the
+// packed adds: per token the sum is still ((h0 + h1) + h2) + h3, then times scale.
 __device__ __forceinline__ void store8_visible(float* out, const uint32_t (&r)[32], int64_t nb, float scale) {
+  const uint64_t sc = pack2(scale, scale);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) st_f32(out + k * nb, __fmul_rn(head_sum(r, k), scale));
+  for (int k = 0; k < 8; k += 2) {
+    uint64_t v = add2(pack2(relu_bits(r[4 * k + 0]), relu_bits(r[4 * k + 4])),
+                      pack2(relu_bits(r[4 * k + 1]), relu_bits(r[4 * k + 5])));
+    v = add2(v, pack2(relu_bits(r[4 * k + 2]), relu_bits(r[4 * k + 6])));
+    v = add2(v, pack2(relu_bits(r[4 * k + 3]), relu_bits(r[4 * k + 7])));
+    v = mul2(v, sc);
+    float lo, hi;
+    unpack2(v, lo, hi);
+    st_f32(out + k * nb, lo);
+    st_f32(out + (k + 1) * nb, hi);
+  }
 }
 
 // 8 consecutive token rows from t: store only rows of the chunk, mask per element
@@ -219,6 +287,7 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base_ptr + kOffTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + kOffAbort);
+  Unit* ring = reinterpret_cast<Unit*>(base_ptr + kOffRing);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -235,6 +304,10 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     for (int s = 0; s < kAccStages; ++s) {
       ptx::mbar_init(bar(kBarAccFull + s), 1);
       ptx::mbar_init(bar(kBarAccEmpty + s), kEpiWarps);
+    }
+    for (int s = 0; s < kSchedStages; ++s) {
+      ptx::mbar_init(bar(kBarSchedFull + s), 1);
+      ptx::mbar_init(bar(kBarSchedEmpty + s), 1 + kEpiWarps);
     }
     ptx::mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
@@ -255,9 +328,24 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int qcnt = 0, kcnt = 0;
-      for (int32_t u = blockIdx.x; u < p.units; u += gridDim.x) {
-        const Unit x = unit_info(p, u);
+      // Work units are taken in increasing order (increasing logits address) from a
+      // device-wide counter, so the CTAs' write fronts advance together.
+      int qcnt = 0, kcnt = 0, scnt = 0;
+      while (true) {
+        const uint32_t u = atomicAdd(p.sched, 1u);
+        Unit x;
+        if (u < static_cast<uint32_t>(p.units)) {
+          x = unit_info(p, static_cast<int32_t>(u));
+        } else {
+          x = Unit{};
+          x.b = -1;
+        }
+        const int ss = scnt % kSchedStages;
+        if (!wait_bounded(bar(kBarSchedEmpty + ss), ((scnt / kSchedStages) & 1) ^ 1, abort_flag, kFaultProducer)) break;
+        ring[ss] = x;
+        ptx::mbar_arrive(bar(kBarSchedFull + ss));
+        ++scnt;
+        if (x.b < 0) break;
         if (x.n_mma == 0) continue;
         const int qs = qcnt % kQStages;
         if (!wait_bounded(bar(kBarQEmpty + qs), ((qcnt / kQStages) & 1) ^ 1, abort_flag, kFaultProducer)) break;
@@ -297,14 +385,25 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
           }
         }
       }
+      // This CTA takes no more units; the last CTA to get here resets the slot.
+      __threadfence();
+      if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+        atomicExch(p.sched, 0u);
+        atomicExch(p.sched + 1, 0u);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int qcnt = 0, kcnt = 0, acnt = 0;
+      int qcnt = 0, kcnt = 0, acnt = 0, scnt = 0;
       bool ok = true;
-      for (int32_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const Unit x = unit_info(p, u);
+      while (ok) {
+        const int ss = scnt % kSchedStages;
+        if (!wait_bounded(bar(kBarSchedFull + ss), (scnt / kSchedStages) & 1, abort_flag, kFaultMma)) break;
+        const Unit x = ring[ss];
+        ptx::mbar_arrive(bar(kBarSchedEmpty + ss));
+        ++scnt;
+        if (x.b < 0) break;
         if (x.n_mma == 0) continue;
         const int qs = qcnt % kQStages;
         if (!wait_bounded(bar(kBarQFull + qs), (qcnt / kQStages) & 1, abort_flag, kFaultMma)) break;
@@ -352,10 +451,16 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const int grp = ew >> 2;
     const int64_t nb = p.num_blocks;
     const float scale = p.scale;
-    int acnt = 0;
+    int acnt = 0, scnt = 0;
     bool ok = true;
-    for (int32_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      const Unit x = unit_info(p, u);
+    while (ok) {
+      const int ss = scnt % kSchedStages;
+      if (!wait_bounded(bar(kBarSchedFull + ss), (scnt / kSchedStages) & 1, abort_flag, kFaultEpilogue)) break;
+      const Unit x = ring[ss];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(kBarSchedEmpty + ss));
+      ++scnt;
+      if (x.b < 0) break;
       const int32_t tb = x.t0 + kTokPerWarp * grp;  // first token of this warp's slice
       const bool rows_full = x.t_lo <= tb && tb + kTokPerWarp <= x.t_hi;
       for (int i = 0; i < x.n_tiles; ++i) {
@@ -376,25 +481,36 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                                 gw + 31 < (tb + 1) / 4;
           const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * sp) << 16) +
                                  static_cast<uint32_t>(as) * kAccCols + 4u * kTokPerWarp * grp;
-#pragma unroll 1
-          for (int c = 0; c < kLdPerWarp; c += 2) {
-            uint32_t r0[32], r1[32];
-            ptx::tmem_ld_32x32b_x32(taddr + 32u * c, r0);
-            ptx::tmem_ld_32x32b_x32(taddr + 32u * (c + 1), r1);
-            ptx::tmem_ld_wait();
+          // 8 tokens per 32-column load; the next load is in flight while the
+          // current 8 tokens are reduced and stored
+          auto emit = [&](const uint32_t (&r)[32], int c) {
             if (interior) {
-              store8_visible(out, r0, nb, scale);
-              store8_visible(out + 8 * nb, r1, nb, scale);
+              store8_visible(out + 8 * c * nb, r, nb, scale);
             } else if (g_ok) {
-              store8_checked(out, r0, nb, scale, tb + 8 * c, g, x);
-              store8_checked(out + 8 * nb, r1, nb, scale, tb + 8 * c + 8, g, x);
+              store8_checked(out + 8 * c * nb, r, nb, scale, tb + 8 * c, g, x);
             }
-            out += 16 * nb;
+          };
+          uint32_t ra[32], rb[32];
+          ptx::tmem_ld_32x32b_x32(taddr, ra);
+          ptx::tmem_ld_wait(ra);
+#pragma unroll
+          for (int c = 0; c < kLdPerWarp; c += 2) {
+            ptx::tmem_ld_32x32b_x32(taddr + 32u * (c + 1), rb);
+            emit(ra, c);
+            ptx::tmem_ld_wait(rb);
+            if (c + 2 < kLdPerWarp) ptx::tmem_ld_32x32b_x32(taddr + 32u * (c + 2), ra);
+            emit(rb, c + 1);
+            if (c + 2 < kLdPerWarp) ptx::tmem_ld_wait(ra);
           }
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(bar(kBarAccEmpty + as));
           ++acnt;
+        } else if (rows_full && cols_full && p.vec_fill) {
+          // lanes re-mapped for the fill: 4 rows x 128 bytes per store instruction
+          float* o = out - lane + (lane >> 3) * nb + 4 * (lane & 7);
+#pragma unroll
+          for (int k = 0; k < kTokPerWarp; k += 4) st_f32x4_neg_max(o + k * nb);
         } else if (rows_full && cols_full) {
 #pragma unroll 8
           for (int k = 0; k < kTokPerWarp; ++k) {
@@ -457,6 +573,8 @@ cudaError_t encode_rows(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m
 
 std::mutex g_attr_mu;
 bool g_attr_set[64] = {};
+uint32_t* g_sched_base[64] = {};      // device address of g_k2_sched, per device
+uint32_t g_launch_seq[64] = {};       // launches so far, per device (guarded by g_attr_mu)
 
 }  // namespace
 
@@ -467,6 +585,8 @@ cudaError_t launch_scores_tc(const LaunchScores& a) {
   if (e != cudaSuccess) return e;
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  uint32_t slot = 0;
+  uint32_t* sched_base = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -474,14 +594,22 @@ cudaError_t launch_scores_tc(const LaunchScores& a) {
       e = cudaFuncSetAttribute(k2_scores_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(kSmemBytes));
       if (e != cudaSuccess) return e;
+      // the symbol's name is only a host-side stand-in: ask the runtime for the
+      // device address, once per device, with that device current
+      void* sched = nullptr;
+      if ((e = cudaGetSymbolAddress(&sched, g_k2_sched)) != cudaSuccess) return e;
+      g_sched_base[dev] = static_cast<uint32_t*>(sched);
       g_attr_set[dev] = true;
     }
+    slot = g_launch_seq[dev]++ % kSchedSlots;
+    sched_base = g_sched_base[dev];
   }
   CUtensorMap tq, tk;
   if ((e = encode_rows(encode, &tq, a.q_normed, 4ull * a.seq_len, a.batch, kN)) != cudaSuccess) return e;
   if ((e = encode_rows(encode, &tk, a.kbar, a.num_blocks, a.batch, kGTile)) != cudaSuccess) return e;
 
   Params p{};
+  p.sched = sched_base + 2 * slot;
   p.logits = a.logits;
   p.ctx = a.context_lengths;
   p.batch = a.batch;
@@ -503,6 +631,7 @@ cudaError_t launch_scores_tc(const LaunchScores& a) {
   p.units = static_cast<int32_t>(units);
   p.idesc = ptx::idesc_f16(a.bf16, kGTile, kN);
   p.scale = a.scale;
+  p.vec_fill = (a.num_blocks % 4 == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0) ? 1 : 0;
   const int grid = static_cast<int>(units < a.num_sms ? units : a.num_sms);
   k2_scores_tc_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, p);
   return cudaGetLastError();
