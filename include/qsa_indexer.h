@@ -10,10 +10,11 @@
  * Conventions shared by every entry point
  *  - T is the 2-byte activation type named by `dtype`: QSA_BF16 or QSA_F16.
  *  - Every array argument is a DEVICE pointer owned by the caller; scalars are
- *    host values.  The library allocates nothing, never synchronises, and
- *    enqueues its kernels on `stream` only (0 = the legacy default stream), so
- *    every call can be captured into a CUDA graph.  Kernels are compiled ahead
- *    of time for sm_103a: there is no warm-up call.
+ *    host values.  The library allocates nothing, never synchronises (except
+ *    qsa_device_fault_flags), and enqueues its kernels on `stream` only
+ *    (0 = the legacy default stream).  Kernels are compiled ahead of time for
+ *    sm_103a: there is no JIT step.  The first scoring call on a device does a
+ *    one-time host-side set-up (kernel attribute, static-array address).
  *  - Arguments are validated on the host before anything is enqueued; device
  *    data (contextLengths) is never read on the host.  On a non-zero status
  *    nothing was enqueued (except QSA_E_CUDA from a failed launch) and
@@ -149,6 +150,38 @@ int qsa_index_scores(qsa_dtype_t dtype, float* logits, const void* qNormed, cons
                      const int32_t* contextLengths, int32_t batchSize, int32_t seqLen,
                      int32_t numBlocks, int32_t rowStart, int32_t numRows,
                      qsa_stream_t stream);
+
+/*
+ * qsa_index_scores_no_alloc: the K2 scores of qsa_index_scores, for callers that
+ * must not allocate device memory.  (No counterpart on the "Qsa Indexer Kernels"
+ * page; an addition of this library.)
+ *
+ * Who needs it: code that cannot call cudaMalloc at the point of the call, such
+ * as an inference engine whose memory manager owns every device allocation, code
+ * recording work into a stream that is being captured (cudaMalloc is not a stream
+ * operation and may synchronise the device), or a latency-critical path that
+ * cannot afford the implicit synchronisation of cudaMalloc/cudaFree.
+ *
+ * Arguments, layouts, results, validation and error codes are those of
+ * qsa_index_scores; the caller still passes every input and output.  The kernel's
+ * scratch (its work-scheduler counters) lives in one fixed 256-byte static device
+ * array that every GPU loading this library holds until the process exits; this
+ * entry point never calls cudaMalloc, cudaFree or any allocating routine.
+ *  - Every call on a device shares that array, which keeps the last call's
+ *    contents.  Each call zeroes the counters on `stream` before its kernel, so
+ *    calls that overlap on the GPU (for example on two streams) race on them and
+ *    produce undefined logits: serialise them.
+ *  - The first call on a device does a one-time set-up (looks up the array's
+ *    device address and sets the kernel's shared-memory attribute) with that
+ *    device current; make that first call before any stream capture begins.
+ *  - Limit: the work-unit count, ceilDiv of the chunk's token tiles (64 tokens)
+ *    times ceilDiv(numBlocks, 1024), must not exceed 2^31 - 65537; larger
+ *    problems return QSA_E_SHAPE with a message.
+ */
+int qsa_index_scores_no_alloc(qsa_dtype_t dtype, float* logits, const void* qNormed,
+                              const void* kbar, const int32_t* contextLengths, int32_t batchSize,
+                              int32_t seqLen, int32_t numBlocks, int32_t rowStart, int32_t numRows,
+                              qsa_stream_t stream);
 
 /*
  * Device-side fault flags.  Kernels that wait on their own asynchronous copies

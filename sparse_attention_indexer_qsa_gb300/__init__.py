@@ -18,7 +18,8 @@ from .build import LIB_PATH
 
 __all__ = [
     "QsaError", "QSA_BF16", "QSA_F16", "load", "lib", "qsa_abi_version", "qsa_last_error",
-    "qsa_index_q_prep", "qsa_index_k_compress", "qsa_index_scores", "qsa_device_fault_flags",
+    "qsa_index_q_prep", "qsa_index_k_compress", "qsa_index_scores", "qsa_index_scores_no_alloc",
+    "qsa_device_fault_flags",
     "qsa_testing_index_scores_cuda_core", "LIB_PATH",
 ]
 
@@ -27,7 +28,8 @@ QSA_F16 = 1
 STATUS_NAMES = {0: "QSA_OK", -1: "QSA_E_NULL", -2: "QSA_E_SHAPE", -3: "QSA_E_RANGE",
                 -4: "QSA_E_DTYPE", -5: "QSA_E_ALIGN", -6: "QSA_E_CUDA", -7: "QSA_E_DEVICE"}
 EXPORTED = ["qsa_abi_version", "qsa_last_error", "qsa_index_q_prep", "qsa_index_k_compress",
-            "qsa_index_scores", "qsa_device_fault_flags", "qsa_testing_index_scores_cuda_core"]
+            "qsa_index_scores", "qsa_index_scores_no_alloc", "qsa_device_fault_flags",
+            "qsa_testing_index_scores_cuda_core"]
 
 
 class QsaError(RuntimeError):
@@ -62,6 +64,8 @@ def load():
     L.qsa_index_k_compress.restype = ctypes.c_int
     L.qsa_index_scores.argtypes = [ctypes.c_int, p, p, p, p, i32, i32, i32, i32, i32, p]
     L.qsa_index_scores.restype = ctypes.c_int
+    L.qsa_index_scores_no_alloc.argtypes = list(L.qsa_index_scores.argtypes)
+    L.qsa_index_scores_no_alloc.restype = ctypes.c_int
     L.qsa_testing_index_scores_cuda_core.argtypes = list(L.qsa_index_scores.argtypes)
     L.qsa_testing_index_scores_cuda_core.restype = ctypes.c_int
     L.qsa_device_fault_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, p]
@@ -144,6 +148,15 @@ def qsa_index_scores(logits, qNormed, kbar, contextLengths, batchSize, seqLen, n
     _check(load().qsa_index_scores(_dtype(dtype, qNormed, kbar), _addr(logits), _addr(qNormed),
                                 _addr(kbar), _addr(contextLengths), int(batchSize), int(seqLen),
                                 int(numBlocks), int(rowStart), int(numRows), _stream(stream)))
+
+
+def qsa_index_scores_no_alloc(logits, qNormed, kbar, contextLengths, batchSize, seqLen, numBlocks,
+                              rowStart, numRows, stream=None, dtype=None):
+    """K2 with its scratch in one static device array: for callers that cannot allocate
+    (see include/qsa_indexer.h; overlapping calls race)."""
+    _check(load().qsa_index_scores_no_alloc(_dtype(dtype, qNormed, kbar), _addr(logits), _addr(qNormed),
+                                         _addr(kbar), _addr(contextLengths), int(batchSize), int(seqLen),
+                                         int(numBlocks), int(rowStart), int(numRows), _stream(stream)))
 
 
 def qsa_testing_index_scores_cuda_core(logits, qNormed, kbar, contextLengths, batchSize, seqLen,

@@ -637,6 +637,96 @@ cudaError_t launch_scores_tc(const LaunchScores& a) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// No-allocation variant (qsa_index_scores_no_alloc).  Same kernel and numerics as
+// launch_scores_tc; the only difference is where the kernel's scratch lives: one
+// fixed 256-byte static array shared by every call on a device, instead of the
+// rotating per-launch slot table.  Its first two words are the scheduler's
+// {next unit, CTAs finished} counter pair; each call zeroes them on its stream
+// before the kernel runs, so calls that overlap on the GPU race on them.
+constexpr int kNoAllocScratchWords = 64;  // 256 bytes
+static __device__ __align__(256) uint32_t g_k2_noalloc_scratch[kNoAllocScratchWords];
+
+namespace {
+std::mutex g_noalloc_mu;
+bool g_noalloc_ready[64] = {};
+uint32_t* g_noalloc_ptr[64] = {};
+}  // namespace
+
+// Largest number of work units the 32-bit counter can hand out: every CTA
+// overshoots it by one when the work runs out, so keep a CTA-count margin.
+int64_t scores_no_alloc_max_units() { return static_cast<int64_t>(INT32_MAX) - 65536; }
+
+int64_t scores_work_units(int32_t batch, int32_t seq_len, int32_t num_blocks, int32_t row_start,
+                          int32_t num_rows) {
+  using namespace k2;
+  const int64_t tpb = (seq_len + kTokTile - 1) / kTokTile;
+  const int64_t first = row_start;
+  const int64_t last = static_cast<int64_t>(row_start) + num_rows - 1;
+  const int64_t b_first = first / seq_len, b_last = last / seq_len;
+  const int64_t tile_lo = b_first * tpb + (first - b_first * seq_len) / kTokTile;
+  const int64_t tile_hi = b_last * tpb + (last - b_last * seq_len) / kTokTile + 1;
+  const int64_t n_gtiles = (num_blocks + kGTile - 1) / kGTile;
+  (void)batch;
+  return (tile_hi - tile_lo) * ((n_gtiles + kGTilesPerUnit - 1) / kGTilesPerUnit);
+}
+
+cudaError_t launch_scores_tc_no_alloc(const LaunchScores& a) {
+  using namespace k2;
+  cudaError_t e;
+  auto encode = get_encode_fn(&e);
+  if (e != cudaSuccess) return e;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  uint32_t* scratch = nullptr;
+  {
+    // one-time set-up per device, with that device current: kernel attribute and the
+    // device address of the static scratch array (its name is a host-side stand-in)
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!g_noalloc_ready[dev]) {
+      e = cudaFuncSetAttribute(k2_scores_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmemBytes));
+      if (e != cudaSuccess) return e;
+      void* ptr = nullptr;
+      if ((e = cudaGetSymbolAddress(&ptr, g_k2_noalloc_scratch)) != cudaSuccess) return e;
+      g_noalloc_ptr[dev] = static_cast<uint32_t*>(ptr);
+      g_noalloc_ready[dev] = true;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  // the counter pair must start at zero: clear it in stream order (no allocation)
+  if ((e = cudaMemsetAsync(scratch, 0, 2 * sizeof(uint32_t), a.stream)) != cudaSuccess) return e;
+
+  CUtensorMap tq, tk;
+  if ((e = encode_rows(encode, &tq, a.q_normed, 4ull * a.seq_len, a.batch, kN)) != cudaSuccess) return e;
+  if ((e = encode_rows(encode, &tk, a.kbar, a.num_blocks, a.batch, kGTile)) != cudaSuccess) return e;
+  Params p{};
+  p.sched = scratch;
+  p.logits = a.logits;
+  p.ctx = a.context_lengths;
+  p.batch = a.batch;
+  p.seq_len = a.seq_len;
+  p.num_blocks = a.num_blocks;
+  p.row_start = a.row_start;
+  p.num_rows = a.num_rows;
+  p.tiles_per_batch = (a.seq_len + kTokTile - 1) / kTokTile;
+  const int64_t first = a.row_start;
+  const int64_t b_first = first / a.seq_len;
+  p.tile_lo = static_cast<int32_t>(b_first * p.tiles_per_batch + (first - b_first * a.seq_len) / kTokTile);
+  p.n_gtiles = (a.num_blocks + kGTile - 1) / kGTile;
+  p.n_groups = (p.n_gtiles + kGTilesPerUnit - 1) / kGTilesPerUnit;
+  const int64_t units = scores_work_units(a.batch, a.seq_len, a.num_blocks, a.row_start, a.num_rows);
+  if (units > scores_no_alloc_max_units()) return cudaErrorInvalidValue;
+  p.units = static_cast<int32_t>(units);
+  p.idesc = ptx::idesc_f16(a.bf16, kGTile, kN);
+  p.scale = a.scale;
+  p.vec_fill = (a.num_blocks % 4 == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0) ? 1 : 0;
+  const int grid = static_cast<int>(units < a.num_sms ? units : a.num_sms);
+  k2_scores_tc_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, p);
+  return cudaGetLastError();
+}
+
 cudaError_t read_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream) {
   cudaError_t e = cudaMemcpyFromSymbolAsync(flags, g_fault_flags, sizeof(uint32_t), 0,
                                             cudaMemcpyDeviceToHost, stream);

@@ -171,6 +171,30 @@ QSA_API int qsa_index_scores(qsa_dtype_t dtype, float* logits, const void* qNorm
   return launched(fn, qsa::launch_scores_tc(a));
 }
 
+QSA_API int qsa_index_scores_no_alloc(qsa_dtype_t dtype, float* logits, const void* qNormed, const void* kbar,
+                                      const int32_t* contextLengths, int32_t batchSize, int32_t seqLen,
+                                      int32_t numBlocks, int32_t rowStart, int32_t numRows,
+                                      qsa_stream_t stream) {
+  static const char* fn = "qsa_index_scores_no_alloc";
+  int st = validate_scores(fn, dtype, logits, qNormed, kbar, contextLengths, batchSize, seqLen, numBlocks,
+                           rowStart, numRows);
+  if (st != QSA_OK) return st;
+  if (numRows == 0) {
+    g_last_error[0] = '\0';
+    return QSA_OK;
+  }
+  const int64_t units = qsa::scores_work_units(batchSize, seqLen, numBlocks, rowStart, numRows);
+  if (units > qsa::scores_no_alloc_max_units())
+    return fail(QSA_E_SHAPE, "%s: %lld work units exceed the static scratch counter's maximum of %lld", fn,
+                static_cast<long long>(units), static_cast<long long>(qsa::scores_no_alloc_max_units()));
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  qsa::LaunchScores a{dtype == QSA_BF16, logits, qNormed, kbar, contextLengths, batchSize, seqLen,
+                      numBlocks, rowStart, numRows, score_scale(), d.num_sms,
+                      reinterpret_cast<cudaStream_t>(stream)};
+  return launched(fn, qsa::launch_scores_tc_no_alloc(a));
+}
+
 QSA_API int qsa_testing_index_scores_cuda_core(qsa_dtype_t dtype, float* logits, const void* qNormed,
                                                const void* kbar, const int32_t* contextLengths,
                                                int32_t batchSize, int32_t seqLen, int32_t numBlocks,

@@ -49,6 +49,11 @@ cudaError_t launch_q_prep(const LaunchQPrep& a);
 cudaError_t launch_k_compress(const LaunchKCompress& a);
 cudaError_t launch_scores_tc(const LaunchScores& a);
 cudaError_t launch_scores_cc(const LaunchScores& a);  // CUDA-core cross-check (testing only)
+// K2 with its scheduler scratch in one fixed static array (qsa_index_scores_no_alloc)
+cudaError_t launch_scores_tc_no_alloc(const LaunchScores& a);
+int64_t scores_work_units(int32_t batch, int32_t seq_len, int32_t num_blocks, int32_t row_start,
+                          int32_t num_rows);
+int64_t scores_no_alloc_max_units();
 
 // Device fault flags (k2_scores_tc.cu): bits set by bounded waits that ran out.
 cudaError_t read_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
