@@ -140,6 +140,25 @@ def smi_device_id(local: int) -> str:
     return ids[local] if local < len(ids) else str(local)
 
 
+def k2_profiled_traffic(batch: int):
+    """DRAM bytes per K2 launch from the committed ncu summary, scaled to `batch`
+    sequences; None if the kernel source changed since the capture."""
+    import hashlib
+    import re
+    prof = os.path.join(ROOT, "profiles", "k2_scores_tc_B4_S16384.md")
+    src = os.path.join(ROOT, "sparse_attention_indexer_qsa_gb300", "csrc", "k2_scores_tc.cu")
+    try:
+        text = open(prof).read()
+        want = re.search(r"source_sha256_prefix: ([0-9a-f]+)", text).group(1)
+        have = hashlib.sha256(open(src, "rb").read()).hexdigest()[:len(want)]
+        if want != have:
+            return None
+        per_b8 = int(re.search(r"traffic_bytes_per_launch_B8: (\d+)", text).group(1))
+        return per_b8 * batch / 8
+    except Exception:
+        return None
+
+
 # ------------------------------------------------------------------ oracle leg
 
 def oracle_sample(wl, budget_s: float = 12.0, seed: int = 0) -> dict:
@@ -363,15 +382,7 @@ def run_ours(args, rank: int, world: int) -> None:
     kernels["k2"]["causal_tflops"] = ab["k2_causal_flops"] / (per_kernel["k2"] * 1e-3) / 1e12
     kernels["k2"]["frac_of_measured_bf16_peak"] = kernels["k2"]["causal_tflops"] / tf_peak
 
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "k2_traffic.json")
-    if os.path.exists(tpath):
-        try:
-            with open(tpath) as f:
-                traffic = json.load(f).get("dram_bytes_per_launch")
-        except Exception:
-            traffic = None
-
+    traffic = k2_profiled_traffic(B)
     k2_gbs = kernels["k2"]["gbs"]
     line = {
         "metric": METRIC,
