@@ -152,6 +152,27 @@ int qsa_index_scores(qsa_dtype_t dtype, float* logits, const void* qNormed, cons
                      qsa_stream_t stream);
 
 /*
+ * qsa_index_qk_prep: qsa_index_q_prep and the prefill qsa_index_k_compress
+ * (blockBegin = 0, blockEnd = ceilDiv(seqLen, 4), pastLen = 0) in one pass over
+ * indexQk ("Qsa Indexer Kernels": launchQsaIndexQPrep and launchQsaIndexKCompress
+ * as the prefill pipeline calls them).  Outputs are bit-identical to the two
+ * separate calls; each 1280-byte indexQk row is read once instead of in two
+ * slices.
+ *
+ *  qNormed  [out] T [batchSize, seqLen, 4, 128]
+ *  kbar     [out] T [batchSize, numBlocks, 128]; rows [0, ceilDiv(seqLen, 4)) written,
+ *                 numBlocks >= ceilDiv(seqLen, 4) is the row stride
+ *  other arguments as qsa_index_q_prep / qsa_index_k_compress; contextLengths[b]
+ *  is the length of sequence b (0 <= ctx <= seqLen).
+ *
+ * Errors: QSA_E_NULL, QSA_E_DTYPE, QSA_E_SHAPE, QSA_E_ALIGN, QSA_E_CUDA.
+ */
+int qsa_index_qk_prep(qsa_dtype_t dtype, void* qNormed, void* kbar, const void* indexQk,
+                      const float* cosSin, const int32_t* contextLengths, const void* wQ,
+                      const void* wK, float rmsEps, int32_t batchSize, int32_t seqLen,
+                      int32_t numBlocks, qsa_stream_t stream);
+
+/*
  * qsa_index_scores_no_alloc: the K2 scores of qsa_index_scores, for callers that
  * must not allocate device memory.  (No counterpart on the "Qsa Indexer Kernels"
  * page; an addition of this library.)
@@ -185,7 +206,8 @@ int qsa_index_scores_no_alloc(qsa_dtype_t dtype, float* logits, const void* qNor
 
 /*
  * Device-side fault flags.  Kernels that wait on their own asynchronous copies
- * bound every wait (about a second); a wait that runs out sets a bit here
+ * bound every wait (about two seconds); a wait that runs out sets a bit here
+ * (bits 0-3: scoring kernel, bits 8-11: staged q-prep kernels)
  * instead of hanging, the kernel drains and returns, and the outputs of that
  * launch are undefined.  This call synchronises `stream`, copies the flags of
  * the current device into *flags (0 = no fault since the last clear) and clears

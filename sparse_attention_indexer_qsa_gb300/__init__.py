@@ -18,7 +18,8 @@ from .build import LIB_PATH
 
 __all__ = [
     "QsaError", "QSA_BF16", "QSA_F16", "load", "lib", "qsa_abi_version", "qsa_last_error",
-    "qsa_index_q_prep", "qsa_index_k_compress", "qsa_index_scores", "qsa_index_scores_no_alloc",
+    "qsa_index_q_prep", "qsa_index_k_compress", "qsa_index_qk_prep", "qsa_index_scores",
+    "qsa_index_scores_no_alloc",
     "qsa_device_fault_flags",
     "qsa_testing_index_scores_cuda_core", "LIB_PATH",
 ]
@@ -28,6 +29,7 @@ QSA_F16 = 1
 STATUS_NAMES = {0: "QSA_OK", -1: "QSA_E_NULL", -2: "QSA_E_SHAPE", -3: "QSA_E_RANGE",
                 -4: "QSA_E_DTYPE", -5: "QSA_E_ALIGN", -6: "QSA_E_CUDA", -7: "QSA_E_DEVICE"}
 EXPORTED = ["qsa_abi_version", "qsa_last_error", "qsa_index_q_prep", "qsa_index_k_compress",
+            "qsa_index_qk_prep",
             "qsa_index_scores", "qsa_index_scores_no_alloc", "qsa_device_fault_flags",
             "qsa_testing_index_scores_cuda_core"]
 
@@ -62,6 +64,8 @@ def load():
     L.qsa_index_k_compress.argtypes = [ctypes.c_int, p, p, p, p, p, f32, i32, i32, i32,
                                        i32, i32, i32, p]
     L.qsa_index_k_compress.restype = ctypes.c_int
+    L.qsa_index_qk_prep.argtypes = [ctypes.c_int, p, p, p, p, p, p, p, f32, i32, i32, i32, p]
+    L.qsa_index_qk_prep.restype = ctypes.c_int
     L.qsa_index_scores.argtypes = [ctypes.c_int, p, p, p, p, i32, i32, i32, i32, i32, p]
     L.qsa_index_scores.restype = ctypes.c_int
     L.qsa_index_scores_no_alloc.argtypes = list(L.qsa_index_scores.argtypes)
@@ -140,6 +144,15 @@ def qsa_index_k_compress(kbar, indexQk, cosSin, contextLengths, wK, rmsEps, batc
                                     _addr(cosSin), _addr(contextLengths), _addr(wK), float(rmsEps),
                                     int(batchSize), int(seqLen), int(numBlocks), int(blockBegin),
                                     int(blockEnd), int(pastLen), _stream(stream)))
+
+
+def qsa_index_qk_prep(qNormed, kbar, indexQk, cosSin, contextLengths, wQ, wK, rmsEps, batchSize,
+                      seqLen, numBlocks, stream=None, dtype=None):
+    """K1a + prefill K1b in one pass over indexQk (see include/qsa_indexer.h)."""
+    _check(load().qsa_index_qk_prep(_dtype(dtype, indexQk, qNormed, kbar), _addr(qNormed), _addr(kbar),
+                                 _addr(indexQk), _addr(cosSin), _addr(contextLengths), _addr(wQ),
+                                 _addr(wK), float(rmsEps), int(batchSize), int(seqLen), int(numBlocks),
+                                 _stream(stream)))
 
 
 def qsa_index_scores(logits, qNormed, kbar, contextLengths, batchSize, seqLen, numBlocks,

@@ -24,7 +24,8 @@ LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["qsa_abi.cpp", "k1a_qprep.cu", "k1b_compress.cu", "k2_scores_tc.cu", "k2_scores_cc.cu"]
+SOURCES = ["qsa_abi.cpp", "k1a_qprep.cu", "k1b_compress.cu", "k1_stream.cu", "k2_scores_tc.cu",
+           "k2_scores_cc.cu"]
 
 
 def nvcc() -> str:

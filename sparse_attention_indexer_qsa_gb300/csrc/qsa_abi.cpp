@@ -120,6 +120,31 @@ QSA_API int qsa_index_q_prep(qsa_dtype_t dtype, void* qNormed, const void* index
   return launched(fn, qsa::launch_q_prep(a));
 }
 
+QSA_API int qsa_index_qk_prep(qsa_dtype_t dtype, void* qNormed, void* kbar, const void* indexQk,
+                              const float* cosSin, const int32_t* contextLengths, const void* wQ,
+                              const void* wK, float rmsEps, int32_t batchSize, int32_t seqLen,
+                              int32_t numBlocks, qsa_stream_t stream) {
+  static const char* fn = "qsa_index_qk_prep";
+  int st;
+  if ((st = check_dtype(fn, dtype)) != QSA_OK) return st;
+  if (!qNormed || !kbar || !indexQk || !cosSin || !contextLengths || !wQ || !wK)
+    return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  if (batchSize < 1 || seqLen < 1)
+    return fail(QSA_E_SHAPE, "%s: batchSize=%d seqLen=%d must be >= 1", fn, batchSize, seqLen);
+  if (static_cast<int64_t>(batchSize) * seqLen > INT32_MAX)
+    return fail(QSA_E_SHAPE, "%s: batchSize*seqLen exceeds INT32_MAX", fn);
+  if (numBlocks < (seqLen + 3) / 4)
+    return fail(QSA_E_SHAPE, "%s: numBlocks=%d < ceilDiv(seqLen=%d, 4)", fn, numBlocks, seqLen);
+  if (!aligned(qNormed, 16) || !aligned(kbar, 16) || !aligned(indexQk, 16) || !aligned(cosSin, 16) ||
+      !aligned(wQ, 16) || !aligned(wK, 16) || !aligned(contextLengths, 4))
+    return fail(QSA_E_ALIGN, "%s: T and FP32 arrays must be 16-byte aligned, contextLengths 4-byte", fn);
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  qsa::LaunchQKPrep a{dtype == QSA_BF16, qNormed, kbar, indexQk, cosSin, contextLengths, wQ, wK, rmsEps,
+                      batchSize, seqLen, numBlocks, d.num_sms, reinterpret_cast<cudaStream_t>(stream)};
+  return launched(fn, qsa::launch_qk_prep(a));
+}
+
 QSA_API int qsa_index_k_compress(qsa_dtype_t dtype, void* kbar, const void* indexQk, const float* cosSin,
                                  const int32_t* contextLengths, const void* wK, float rmsEps,
                                  int32_t batchSize, int32_t seqLen, int32_t numBlocks, int32_t blockBegin,
@@ -222,8 +247,11 @@ QSA_API int qsa_device_fault_flags(uint32_t* flags, int clear, qsa_stream_t stre
   DeviceInfo d;
   int st = current_device(fn, &d);
   if (st != QSA_OK) return st;
-  cudaError_t e = qsa::read_fault_flags(flags, clear != 0, reinterpret_cast<cudaStream_t>(stream));
+  uint32_t k2 = 0, k1 = 0;
+  cudaError_t e = qsa::read_fault_flags(&k2, clear != 0, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = qsa::read_k1_fault_flags(&k1, clear != 0, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(QSA_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  *flags = k2 | (k1 << 8);
   g_last_error[0] = '\0';
   return QSA_OK;
 }

@@ -33,6 +33,21 @@ struct LaunchKCompress {
   cudaStream_t stream;
 };
 
+struct LaunchQKPrep {
+  bool bf16;
+  void* q_normed;
+  void* kbar;
+  const void* index_qk;
+  const float* cos_sin;
+  const int32_t* context_lengths;
+  const void* w_q;
+  const void* w_k;
+  float eps;
+  int32_t batch, seq_len, num_blocks;
+  int num_sms;
+  cudaStream_t stream;
+};
+
 struct LaunchScores {
   bool bf16;
   float* logits;
@@ -45,7 +60,8 @@ struct LaunchScores {
   cudaStream_t stream;
 };
 
-cudaError_t launch_q_prep(const LaunchQPrep& a);
+cudaError_t launch_q_prep(const LaunchQPrep& a);         // K1a (k1a_qprep.cu)
+cudaError_t launch_qk_prep(const LaunchQKPrep& a);       // fused K1a + prefill K1b (k1_stream.cu)
 cudaError_t launch_k_compress(const LaunchKCompress& a);
 cudaError_t launch_scores_tc(const LaunchScores& a);
 cudaError_t launch_scores_cc(const LaunchScores& a);  // CUDA-core cross-check (testing only)
@@ -55,8 +71,9 @@ int64_t scores_work_units(int32_t batch, int32_t seq_len, int32_t num_blocks, in
                           int32_t num_rows);
 int64_t scores_no_alloc_max_units();
 
-// Device fault flags (k2_scores_tc.cu): bits set by bounded waits that ran out.
+// Device fault flags: bits set by bounded waits that ran out (k2_scores_tc.cu, k1_stream.cu).
 cudaError_t read_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
+cudaError_t read_k1_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
 
 // Cached cudaOccupancyMaxActiveBlocksPerMultiprocessor for (kernel, device).
 cudaError_t occupancy_blocks_per_sm(const void* kernel, int threads, size_t smem, int* out);

@@ -175,3 +175,30 @@ def test_host_validation_enqueues_nothing():
     assert e.value.status == -3
     torch.cuda.synchronize()
     assert not out.view(torch.int16).any()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("B,S,ctx", [(1, 64, [50]), (3, 129, [129, 1, 0]), (2, 1000, [1000, 377]),
+                                     (1, 33, [32]), (4, 2048, None), (1, 5, [5])])
+def test_fused_qk_prep_bit_identical_to_separate_calls(dtype, B, S, ctx):
+    """qsa_index_qk_prep == qsa_index_q_prep + qsa_index_k_compress(0, ceilDiv(S,4), 0)."""
+    import sparse_attention_indexer_qsa_gb300 as qsa
+    g_ = _gpu()
+    if ctx is None:
+        wl = workloads.batched(dtype)
+    else:
+        wl = workloads.custom(B, S, ctx, dtype=dtype, seed=B * 7 + S, nan_padding=True, outlier_frac=0.01)
+    d = g_.DevWorkload(wl)
+    NB = wl.num_blocks + 3                      # a wider row stride: extra rows untouched
+    q_sep = g_.q_prep(d)
+    k_sep = g_.k_compress(d, NB, 0, wl.num_blocks, 0)
+    qo = g_.Guarded(wl.B * wl.S * 512 * 2)
+    ko = g_.Guarded(wl.B * NB * 128 * 2, init=np.full((wl.B, NB, 128), SENT, np.uint16))
+    qsa.qsa_index_qk_prep(qo.ptr, ko.ptr, d.index_qk, d.cos_sin, d.ctx, d.w_q, d.w_k, wl.eps, wl.B, wl.S,
+                          NB, dtype=dtype)
+    q_f = qo.numpy(np.uint16, q_sep.shape)
+    k_f = ko.numpy(np.uint16, k_sep.shape)
+    assert np.array_equal(q_f, q_sep)
+    assert np.array_equal(k_f, k_sep)
+    assert np.all(k_f[:, wl.num_blocks:] == SENT)
+    g_.assert_no_device_faults()
