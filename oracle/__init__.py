@@ -82,6 +82,16 @@ def _load():
         lib.qsa_oracle_scores_row.restype = None
         lib.qsa_oracle_scores.argtypes = [ctypes.c_int, p, p, p, p, i32, i32, i32, i32, i32]
         lib.qsa_oracle_scores.restype = ctypes.c_int
+        lib.qsa_oracle_orderable.argtypes = [f32]
+        lib.qsa_oracle_orderable.restype = ctypes.c_uint32
+        lib.qsa_oracle_ids_fill.argtypes = [p, i32, i32]
+        lib.qsa_oracle_ids_fill.restype = None
+        lib.qsa_oracle_expand_row.argtypes = [p, p, i32, i32]
+        lib.qsa_oracle_expand_row.restype = None
+        lib.qsa_oracle_select_expand_row.argtypes = [p, p, i32, i32, i32, p]
+        lib.qsa_oracle_select_expand_row.restype = None
+        lib.qsa_oracle_select_expand.argtypes = [p, p, p, i32, i32, i32, i32, i32, p]
+        lib.qsa_oracle_select_expand.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -225,4 +235,59 @@ def scores_row(dtype: str, q_row, kbar_b, t: int, ctx: int) -> np.ndarray:
     NB = kb.shape[0]
     out = np.empty(NB, np.float32)
     lib.qsa_oracle_scores_row(DTYPES[dtype], _ptr(out), _ptr(q), _ptr(kb), int(t), int(ctx), NB)
+    return out
+
+
+# ------------------------------------------------------------ prefill selection
+
+INDEX_WIDTH = 2051   # 512 blocks x 4 tokens + 3 tail tokens
+TOPK_BLOCKS = 512
+
+
+def orderable(values) -> np.ndarray:
+    """Order-preserving uint32 map of binary32 values (bits >= 0 ? bits | 2^31 : ~bits)."""
+    lib = _load()
+    return np.array([lib.qsa_oracle_orderable(float(v)) for v in np.asarray(values, np.float32).ravel()],
+                    np.uint32)
+
+
+def ids_fill(num_rows: int, num_blocks: int) -> np.ndarray:
+    lib = _load()
+    out = np.empty((num_rows, num_blocks), np.int32)
+    lib.qsa_oracle_ids_fill(_ptr(out), num_rows, num_blocks)
+    return out
+
+
+def expand_row(sorted_ids, t: int, ctx: int) -> np.ndarray:
+    lib = _load()
+    ids = _i32(sorted_ids)
+    out = np.empty(INDEX_WIDTH, np.int32)
+    lib.qsa_oracle_expand_row(_ptr(out), _ptr(ids), int(t), int(ctx))
+    return out
+
+
+def select_expand_row(logits_row, t: int, ctx: int) -> np.ndarray:
+    """Prefill selection of one row: stable descending sort + expand -> [2051] int32."""
+    lib = _load()
+    row = _f32(logits_row)
+    n = row.shape[0]
+    scratch = np.empty(4 * max(n, 1), np.uint32)
+    out = np.empty(INDEX_WIDTH, np.int32)
+    lib.qsa_oracle_select_expand_row(_ptr(out), _ptr(row), n, int(t), int(ctx), _ptr(scratch))
+    return out
+
+
+def select_expand(logits, context_lengths, B: int, S: int, row_start: int = 0,
+                  out_idx=None) -> np.ndarray:
+    """Rows [row_start, row_start + len(logits)) of outIdx [B*S, 2051]; other rows keep
+    out_idx's contents (zeros if None)."""
+    lib = _load()
+    lg = _f32(logits)
+    num_rows, nb = lg.shape
+    ctx = _i32(context_lengths)
+    out = np.zeros((B * S, INDEX_WIDTH), np.int32) if out_idx is None else np.array(out_idx, np.int32, copy=True)
+    scratch = np.empty(4 * max(nb, 1), np.uint32)
+    rc = lib.qsa_oracle_select_expand(_ptr(out), _ptr(lg), _ptr(ctx), B, S, nb, row_start, num_rows,
+                                      _ptr(scratch))
+    assert rc == 0
     return out

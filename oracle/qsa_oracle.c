@@ -320,3 +320,97 @@ int qsa_oracle_scores(int dtype, float* logits, const uint16_t* qNormed, const u
   }
   return 0;
 }
+
+/* --------------------------------------------------------- prefill selection */
+
+#define QSA_TOPK_BLOCKS 512
+#define QSA_INDEX_WIDTH (QSA_TOPK_BLOCKS * QSA_COMPRESS_RATIO + QSA_COMPRESS_RATIO - 1) /* 2051 */
+
+/* Order-preserving map of binary32 bit patterns to unsigned integers
+ * (launchQsaTopKExpandDecode): u = bits >= 0 ? bits | 0x80000000 : ~bits. */
+uint32_t qsa_oracle_orderable(float f) {
+  uint32_t b = f32_bits(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+/* launchQsaIndexIdsFill: ids[r * numBlocks + c] = c. */
+void qsa_oracle_ids_fill(int32_t* ids, int32_t numRows, int32_t numBlocks) {
+  for (int64_t r = 0; r < numRows; ++r)
+    for (int32_t c = 0; c < numBlocks; ++c) ids[r * numBlocks + c] = c;
+}
+
+/* Stable merge sort of ids by key, descending (equal keys keep their input order). */
+static void stable_sort_desc(uint32_t* key, int32_t* id, uint32_t* tk, int32_t* ti, int32_t n) {
+  for (int32_t width = 1; width < n; width *= 2) {
+    for (int32_t lo = 0; lo < n; lo += 2 * width) {
+      int32_t mid = lo + width < n ? lo + width : n;
+      int32_t hi = lo + 2 * width < n ? lo + 2 * width : n;
+      int32_t a = lo, b = mid, o = lo;
+      while (a < mid && b < hi) {
+        if (key[b] > key[a]) { tk[o] = key[b]; ti[o++] = id[b++]; }   /* only strictly larger jumps ahead */
+        else { tk[o] = key[a]; ti[o++] = id[a++]; }
+      }
+      while (a < mid) { tk[o] = key[a]; ti[o++] = id[a++]; }
+      while (b < hi) { tk[o] = key[b]; ti[o++] = id[b++]; }
+    }
+    memcpy(key, tk, sizeof(uint32_t) * (size_t)n);
+    memcpy(id, ti, sizeof(int32_t) * (size_t)n);
+  }
+}
+
+/*
+ * launchQsaIndexExpand for one row: top kSel = min(512, nVis) block ids (given in
+ * sortedIds order) -> token ids 4*id + j, then the causal tail 4*nVis + j for
+ * j < (t+1) % 4, then -1 to width 2051.  nVis = (t+1)/4.  Padded rows (ctx <= 0 or
+ * t >= ctx) are all -1 and sortedIds is not read.
+ */
+void qsa_oracle_expand_row(int32_t* out, const int32_t* sortedIds, int32_t t, int32_t ctx) {
+  for (int32_t i = 0; i < QSA_INDEX_WIDTH; ++i) out[i] = -1;
+  if (ctx <= 0 || t >= ctx) return;
+  int32_t nVis = (t + 1) / QSA_COMPRESS_RATIO;
+  int32_t kSel = nVis < QSA_TOPK_BLOCKS ? nVis : QSA_TOPK_BLOCKS;
+  int32_t tail = (t + 1) % QSA_COMPRESS_RATIO;
+  for (int32_t i = 0; i < kSel; ++i)
+    for (int32_t j = 0; j < QSA_COMPRESS_RATIO; ++j) out[QSA_COMPRESS_RATIO * i + j] = sortedIds[i] * QSA_COMPRESS_RATIO + j;
+  for (int32_t j = 0; j < tail; ++j) out[QSA_COMPRESS_RATIO * kSel + j] = QSA_COMPRESS_RATIO * nVis + j;
+}
+
+/*
+ * The prefill selection for one row, as the page's pipeline computes it: ids
+ * 0..numBlocks-1, a stable descending sort of the row's FP32 logits (compared by
+ * the order-preserving map, so ties keep ascending ids), then the expand.  Only
+ * the first nVis keys can be selected; the rest are the masked -FLT_MAX cells,
+ * which sort last, so sorting the visible prefix gives the same first kSel ids.
+ * scratch: 4 * numBlocks 32-bit words.
+ */
+void qsa_oracle_select_expand_row(int32_t* out, const float* logits_row, int32_t numBlocks,
+                                  int32_t t, int32_t ctx, uint32_t* scratch) {
+  if (ctx <= 0 || t >= ctx) {
+    for (int32_t i = 0; i < QSA_INDEX_WIDTH; ++i) out[i] = -1;
+    return;
+  }
+  int32_t n = numBlocks;
+  uint32_t* key = scratch;
+  int32_t* id = (int32_t*)(scratch + n);
+  uint32_t* tk = scratch + 2 * (int64_t)n;
+  int32_t* ti = (int32_t*)(scratch + 3 * (int64_t)n);
+  for (int32_t g = 0; g < n; ++g) { key[g] = qsa_oracle_orderable(logits_row[g]); id[g] = g; }
+  stable_sort_desc(key, id, tk, ti, n);
+  qsa_oracle_expand_row(out, id, t, ctx);
+}
+
+/* Rows [rowStart, rowStart + numRows): logits chunk-local [numRows, numBlocks];
+ * outIdx global [B*S, 2051] (rows of the chunk written). */
+int qsa_oracle_select_expand(int32_t* outIdx, const float* logits, const int32_t* contextLengths,
+                             int32_t B, int32_t S, int32_t numBlocks, int32_t rowStart,
+                             int32_t numRows, uint32_t* scratch) {
+  if (rowStart < 0 || numRows < 0 || (int64_t)rowStart + numRows > (int64_t)B * S) return -3;
+  for (int32_t i = 0; i < numRows; ++i) {
+    int64_t r = (int64_t)rowStart + i;
+    int32_t b = (int32_t)(r / S);
+    int32_t t = (int32_t)(r - (int64_t)b * S);
+    qsa_oracle_select_expand_row(outIdx + r * QSA_INDEX_WIDTH, logits + (int64_t)i * numBlocks,
+                                 numBlocks, t, contextLengths[b], scratch);
+  }
+  return 0;
+}

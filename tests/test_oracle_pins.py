@@ -471,3 +471,98 @@ def test_scores_homogeneous_chunked_and_nan_safe(dtype):
         nvis = min(NB, (t + 1) // 4) if t < ctx[b] else 0
         assert int(np.sum(full[r] != NEG_MAX)) == nvis
         assert np.all(full[r, nvis:].view(np.uint32) == np.uint32(0xFF7FFFFF))
+
+
+# ----------------------------------------------------------- prefill selection
+
+def test_orderable_map_is_monotone_and_splits_signed_zero():
+    vals = np.array([0.0, -0.0, 1.0, -1.0], np.float32)
+    assert oracle.orderable(vals).tolist() == [0x80000000, 0x7FFFFFFF, 0xBF800000, 0x407FFFFF]
+    rng = np.random.default_rng(141)
+    x = np.sort(np.concatenate([rng.standard_normal(5000).astype(np.float32) * 1e3,
+                                np.array([np.finfo(np.float32).max, -np.finfo(np.float32).max,
+                                          np.finfo(np.float32).tiny, -np.finfo(np.float32).tiny], np.float32)]))
+    u = oracle.orderable(x).astype(np.int64)
+    assert np.all(np.diff(u) >= 0)
+    assert np.all((np.diff(u) > 0) == (np.diff(x) > 0))
+
+
+def test_ids_fill_closed_form():
+    ids = oracle.ids_fill(3, 7)
+    assert np.array_equal(ids, np.tile(np.arange(7, dtype=np.int32), (3, 1)))
+
+
+def test_expand_row_hand_cases():
+    with open(os.path.join(GOLDEN, "expand_rows.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        out = oracle.expand_row(np.array(c["sorted_ids"], np.int32), c["t"], c["ctx"])
+        prefix = np.array(c["prefix"], np.int32)
+        assert np.array_equal(out[:len(prefix)], prefix), c
+        assert np.all(out[len(prefix):] == -1), c
+
+
+def _check_selection_row(out, logits_row, t, ctx):
+    """Properties any correct prefill selection has (independent of how it sorts)."""
+    if ctx <= 0 or t >= ctx:
+        assert np.all(out == -1)
+        return
+    nvis = (t + 1) // 4
+    ksel = min(512, nvis)
+    tail = (t + 1) % 4
+    used = out[out >= 0]
+    assert used.size == 4 * ksel + tail and np.all(out[used.size:] == -1)
+    assert len(set(used.tolist())) == used.size and used.min() >= 0 and used.max() <= t
+    blocks = out[:4 * ksel:4] // 4
+    assert np.array_equal(out[:4 * ksel].reshape(-1, 4), blocks[:, None] * 4 + np.arange(4))
+    assert np.array_equal(out[4 * ksel:4 * ksel + tail], 4 * nvis + np.arange(tail))
+    u = oracle.orderable(logits_row[:nvis]).astype(np.int64)
+    sel = u[blocks]
+    # emitted in descending key order, equal keys by ascending block id
+    for a, b, ua, ub in zip(blocks[:-1], blocks[1:], sel[:-1], sel[1:]):
+        assert ua > ub or (ua == ub and a < b)
+    # every selected key >= every unselected key; at the threshold, the lowest ids win
+    rest = np.setdiff1d(np.arange(nvis), blocks)
+    if rest.size:
+        thr = sel.min()
+        assert u[rest].max() <= thr
+        tied_rest = rest[u[rest] == thr]
+        tied_sel = blocks[sel == thr]
+        if tied_rest.size:
+            assert tied_sel.max() < tied_rest.min()
+
+
+def test_select_expand_closed_forms_and_properties():
+    NB = 700
+    t = 4 * NB - 1                                   # nVis = 700 > 512
+    dec = np.linspace(10.0, 1.0, NB, dtype=np.float32)
+    out = oracle.select_expand_row(dec, t, t + 1)
+    assert np.array_equal(out[:2048:4] // 4, np.arange(512))
+    inc = dec[::-1].copy()
+    out = oracle.select_expand_row(inc, t, t + 1)
+    assert np.array_equal(out[:2048:4] // 4, np.arange(NB - 1, NB - 513, -1))
+    flat = np.full(NB, 2.5, np.float32)
+    out = oracle.select_expand_row(flat, t, t + 1)
+    assert np.array_equal(out[:2048:4] // 4, np.arange(512))   # stable: ascending ids
+    rng = np.random.default_rng(151)
+    neg = np.float32(-np.finfo(np.float32).max)
+    for trial in range(60):
+        NB = int(rng.integers(1, 900))
+        S = 4 * NB
+        t = int(rng.integers(0, S))
+        ctx = int(rng.integers(0, S + 1))
+        vals = rng.choice([0.0, 0.25, 1.0, 3.0], NB) if trial % 2 else rng.random(NB) * 4
+        row = vals.astype(np.float32)
+        row[(t + 1) // 4:] = neg
+        out = oracle.select_expand_row(row, t, ctx)
+        _check_selection_row(out, row, t, ctx)
+
+
+def test_select_expand_rows_and_golden():
+    with open(os.path.join(GOLDEN, "select_rows.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        out = oracle.select_expand_row(np.array(c["logits"], np.float32), c["t"], c["ctx"])
+        prefix = np.array(c["prefix"], np.int32)
+        assert np.array_equal(out[:len(prefix)], prefix), c
+        assert np.all(out[len(prefix):] == -1), c
