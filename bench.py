@@ -49,12 +49,18 @@ def algorithmic_bytes(ctx: np.ndarray, B: int, S: int, NB: int) -> dict:
     k1b = valid_blocks * (1024 + 256) + (B * NB - valid_blocks) * 256 + int(min(NB, ctx.max() // 4)) * 256
     vis_blocks = int(np.minimum(ctx // 4, NB).sum())
     k2 = valid_rows * 1024 + vis_blocks * 256 + B * S * NB * 4
+    # selection reads each valid row's visible logits and writes 2051 int32 per row
+    vis_logits = 0
+    for c in ctx:
+        t = np.arange(int(min(c, S)))
+        vis_logits += int(np.minimum((t + 1) // 4, NB).sum())
+    select = vis_logits * 4 + B * S * 2051 * 4
     # causal MMA work: row t of a sequence scores floor((t+1)/4) blocks x 4 heads x 128 dims
     flops = 0
     for c in ctx:
         t = np.arange(int(min(c, S)))
         flops += int(((t + 1) // 4).sum()) * 4 * 128 * 2
-    return {"k1a": k1a, "k1b": k1b, "k2": k2, "k2_causal_flops": flops}
+    return {"k1a": k1a, "k1b": k1b, "k2": k2, "select": select, "k2_causal_flops": flops}
 
 
 def load_peaks():
@@ -411,6 +417,15 @@ def run_ours(args, rank: int, world: int) -> None:
     # the separate K1a and K1b entry points, each back to back over the same workload
     ms_k1a = loop_ms(k1a_only, max(K, 20))
     ms_k1b = loop_ms(k1b_only, max(K, 20))
+    # prefill selection on the step's logits (top-512 blocks per row -> 2051 token ids)
+    out_idx = torch.empty((rows, 2051), dtype=torch.int32, device="cuda")
+
+    def select_only():
+        if lib.qsa_index_topk_expand(out_idx.data_ptr(), logits.data_ptr(), ctx.data_ptr(), B, S, NB, 0, rows,
+                                     sp) != 0:
+            raise RuntimeError(qsa.qsa_last_error())
+
+    ms_sel = loop_ms(select_only, max(10, K // 10))
     torch.cuda.synchronize()
     faults = qsa.qsa_device_fault_flags()
 
@@ -420,6 +435,7 @@ def run_ours(args, rank: int, world: int) -> None:
                   for j, n in enumerate(("k1_fused", "k2"))}
     per_kernel["k1a"] = ms_k1a
     per_kernel["k1b"] = ms_k1b
+    per_kernel["select"] = ms_sel
     if rank != 0:
         return
 
@@ -427,14 +443,15 @@ def run_ours(args, rank: int, world: int) -> None:
     ab = algorithmic_bytes(wl.context_lengths, B, S, NB)
     ab["k1_fused"] = ab["k1a"] + ab["k1b"]
     kernels = {}
-    for n in ("k1_fused", "k2", "k1a", "k1b"):
+    for n in ("k1_fused", "k2", "k1a", "k1b", "select"):
         gbs = ab[n] / (per_kernel[n] * 1e-3) / 1e9
         kernels[n] = {"ms": per_kernel[n], "alg_bytes": ab[n], "gbs": gbs,
                       "frac_of_measured_hbm": gbs / hbm_peak, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS}
     kernels["k1_fused"]["rows_per_s"] = rows / (per_kernel["k1_fused"] * 1e-3)
     kernels["k1_fused"]["timed"] = "inside the step (CUDA events around the launch)"
-    for n in ("k1a", "k1b"):
+    for n in ("k1a", "k1b", "select"):
         kernels[n]["timed"] = "separate entry point, back-to-back launches after the step loop"
+    kernels["select"]["rows_per_s"] = rows / (per_kernel["select"] * 1e-3)
     kernels["k1a"]["rows_per_s"] = rows / (per_kernel["k1a"] * 1e-3)
     kernels["k1b"]["blocks_per_s"] = B * NB / (per_kernel["k1b"] * 1e-3)
     kernels["k1b"]["token_rows_per_s"] = 4 * B * NB / (per_kernel["k1b"] * 1e-3)

@@ -172,6 +172,54 @@ int qsa_index_qk_prep(qsa_dtype_t dtype, void* qNormed, void* kbar, const void* 
                       const void* wK, float rmsEps, int32_t batchSize, int32_t seqLen,
                       int32_t numBlocks, qsa_stream_t stream);
 
+#define QSA_TOPK_BLOCKS 512
+#define QSA_INDEX_WIDTH 2051 /* QSA_TOPK_BLOCKS * 4 + 3 */
+
+/*
+ * K3, launchQsaIndexIdsFill: ids[r * numBlocks + c] = c for r < numRows, the value
+ * array of a segmented sort.  ids: [out] INT32 [numRows, numBlocks].
+ * Errors: QSA_E_NULL, QSA_E_SHAPE, QSA_E_ALIGN, QSA_E_CUDA.
+ */
+int qsa_index_ids_fill(int32_t* ids, int32_t numRows, int32_t numBlocks, qsa_stream_t stream);
+
+/*
+ * K4, launchQsaIndexExpand: for global rows r = b*seqLen + t in [rowStart,
+ * rowStart + numRows), with nVis = (t+1)/4, kSel = min(512, nVis),
+ * tail = (t+1) % 4:
+ *   outIdx[r][4i + j]    = sortedIds[r - rowStart][i] * 4 + j   for i < kSel, j < 4
+ *   outIdx[r][4kSel + j] = 4*nVis + j                           for j < tail
+ *   outIdx[r][k]         = -1                                   elsewhere (width 2051)
+ * Padded rows (t >= contextLengths[b] or contextLengths[b] <= 0) are all -1 and
+ * sortedIds is not read for them.
+ *  outIdx    [out] INT32 [batchSize*seqLen, 2051]; only the chunk's rows are written
+ *  sortedIds [in]  INT32 [numRows, numBlocks], chunk-local, block ids by descending logit
+ * Errors: QSA_E_NULL, QSA_E_SHAPE, QSA_E_RANGE, QSA_E_ALIGN, QSA_E_CUDA.
+ */
+int qsa_index_expand(int32_t* outIdx, const int32_t* sortedIds, const int32_t* contextLengths,
+                     int32_t batchSize, int32_t seqLen, int32_t numBlocks, int32_t rowStart,
+                     int32_t numRows, qsa_stream_t stream);
+
+/*
+ * The prefill selection of the page (qsa_index_ids_fill, a stable descending
+ * segmented sort of the chunk's logits with the ids as values, qsa_index_expand)
+ * in one kernel, with no sort and no workspace.  Per row: the FP32 logits of the
+ * visible blocks g < nVis are mapped to order-preserving u32 keys
+ * (bits >= 0 ? bits | 0x80000000 : ~bits); an MSB-first 8-bit radix select finds
+ * the kSel-th largest key; keys above it are selected, and keys equal to it in
+ * ascending block order until kSel are selected.  That is exactly the set of
+ * blocks the three-step pipeline puts first (and the rule of the page's decode
+ * top-k).  The selected blocks are emitted in ascending block order, as the
+ * decode path emits them (the page's token ids are "unsorted"), then expanded:
+ * out[4i + j] = sel[i]*4 + j, the causal tail, -1 to width 2051.
+ *  outIdx [out] INT32 [batchSize*seqLen, 2051] (chunk rows written)
+ *  logits [in]  FP32 [numRows, numBlocks], chunk-local (qsa_index_scores' output)
+ * Limit: numBlocks <= 51200 (a row's keys are staged in shared memory).
+ * Errors: QSA_E_NULL, QSA_E_SHAPE, QSA_E_RANGE, QSA_E_ALIGN, QSA_E_CUDA.
+ */
+int qsa_index_topk_expand(int32_t* outIdx, const float* logits, const int32_t* contextLengths,
+                          int32_t batchSize, int32_t seqLen, int32_t numBlocks, int32_t rowStart,
+                          int32_t numRows, qsa_stream_t stream);
+
 /*
  * qsa_index_scores_no_alloc: the K2 scores of qsa_index_scores, for callers that
  * must not allocate device memory.  (No counterpart on the "Qsa Indexer Kernels"

@@ -19,7 +19,7 @@ from .build import LIB_PATH
 __all__ = [
     "QsaError", "QSA_BF16", "QSA_F16", "load", "lib", "qsa_abi_version", "qsa_last_error",
     "qsa_index_q_prep", "qsa_index_k_compress", "qsa_index_qk_prep", "qsa_index_scores",
-    "qsa_index_scores_no_alloc",
+    "qsa_index_scores_no_alloc", "qsa_index_ids_fill", "qsa_index_expand", "qsa_index_topk_expand",
     "qsa_device_fault_flags",
     "qsa_testing_index_scores_cuda_core", "LIB_PATH",
 ]
@@ -29,7 +29,7 @@ QSA_F16 = 1
 STATUS_NAMES = {0: "QSA_OK", -1: "QSA_E_NULL", -2: "QSA_E_SHAPE", -3: "QSA_E_RANGE",
                 -4: "QSA_E_DTYPE", -5: "QSA_E_ALIGN", -6: "QSA_E_CUDA", -7: "QSA_E_DEVICE"}
 EXPORTED = ["qsa_abi_version", "qsa_last_error", "qsa_index_q_prep", "qsa_index_k_compress",
-            "qsa_index_qk_prep",
+            "qsa_index_qk_prep", "qsa_index_ids_fill", "qsa_index_expand", "qsa_index_topk_expand",
             "qsa_index_scores", "qsa_index_scores_no_alloc", "qsa_device_fault_flags",
             "qsa_testing_index_scores_cuda_core"]
 
@@ -66,6 +66,12 @@ def load():
     L.qsa_index_k_compress.restype = ctypes.c_int
     L.qsa_index_qk_prep.argtypes = [ctypes.c_int, p, p, p, p, p, p, p, f32, i32, i32, i32, p]
     L.qsa_index_qk_prep.restype = ctypes.c_int
+    L.qsa_index_ids_fill.argtypes = [p, i32, i32, p]
+    L.qsa_index_ids_fill.restype = ctypes.c_int
+    L.qsa_index_expand.argtypes = [p, p, p, i32, i32, i32, i32, i32, p]
+    L.qsa_index_expand.restype = ctypes.c_int
+    L.qsa_index_topk_expand.argtypes = [p, p, p, i32, i32, i32, i32, i32, p]
+    L.qsa_index_topk_expand.restype = ctypes.c_int
     L.qsa_index_scores.argtypes = [ctypes.c_int, p, p, p, p, i32, i32, i32, i32, i32, p]
     L.qsa_index_scores.restype = ctypes.c_int
     L.qsa_index_scores_no_alloc.argtypes = list(L.qsa_index_scores.argtypes)
@@ -161,6 +167,25 @@ def qsa_index_scores(logits, qNormed, kbar, contextLengths, batchSize, seqLen, n
     _check(load().qsa_index_scores(_dtype(dtype, qNormed, kbar), _addr(logits), _addr(qNormed),
                                 _addr(kbar), _addr(contextLengths), int(batchSize), int(seqLen),
                                 int(numBlocks), int(rowStart), int(numRows), _stream(stream)))
+
+
+def qsa_index_ids_fill(ids, numRows, numBlocks, stream=None):
+    """K3: ids[r, c] = c (see include/qsa_indexer.h)."""
+    _check(load().qsa_index_ids_fill(_addr(ids), int(numRows), int(numBlocks), _stream(stream)))
+
+
+def qsa_index_expand(outIdx, sortedIds, contextLengths, batchSize, seqLen, numBlocks, rowStart, numRows,
+                     stream=None):
+    """K4: sorted block ids -> 2051 token ids per row (see include/qsa_indexer.h)."""
+    _check(load().qsa_index_expand(_addr(outIdx), _addr(sortedIds), _addr(contextLengths), int(batchSize),
+                                int(seqLen), int(numBlocks), int(rowStart), int(numRows), _stream(stream)))
+
+
+def qsa_index_topk_expand(outIdx, logits, contextLengths, batchSize, seqLen, numBlocks, rowStart, numRows,
+                          stream=None):
+    """Prefill selection in one kernel: radix top-512 + order + expand (see include/qsa_indexer.h)."""
+    _check(load().qsa_index_topk_expand(_addr(outIdx), _addr(logits), _addr(contextLengths), int(batchSize),
+                                     int(seqLen), int(numBlocks), int(rowStart), int(numRows), _stream(stream)))
 
 
 def qsa_index_scores_no_alloc(logits, qNormed, kbar, contextLengths, batchSize, seqLen, numBlocks,

@@ -220,6 +220,71 @@ QSA_API int qsa_index_scores_no_alloc(qsa_dtype_t dtype, float* logits, const vo
   return launched(fn, qsa::launch_scores_tc_no_alloc(a));
 }
 
+QSA_API int qsa_index_ids_fill(int32_t* ids, int32_t numRows, int32_t numBlocks, qsa_stream_t stream) {
+  static const char* fn = "qsa_index_ids_fill";
+  if (!ids) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  if (numRows < 0 || numBlocks < 1) return fail(QSA_E_SHAPE, "%s: numRows=%d >= 0, numBlocks=%d >= 1 required", fn, numRows, numBlocks);
+  if (!aligned(ids, 4)) return fail(QSA_E_ALIGN, "%s: ids must be 4-byte aligned", fn);
+  if (numRows == 0) {
+    g_last_error[0] = '\0';
+    return QSA_OK;
+  }
+  DeviceInfo d;
+  int st = current_device(fn, &d);
+  if (st != QSA_OK) return st;
+  return launched(fn, qsa::launch_ids_fill(ids, numRows, numBlocks, d.num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+int validate_selection(const char* fn, const void* outIdx, const void* in, const int32_t* ctx, int32_t B,
+                       int32_t S, int32_t NB, int32_t rowStart, int32_t numRows) {
+  if (!outIdx || !in || !ctx) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  if (B < 1 || S < 1) return fail(QSA_E_SHAPE, "%s: batchSize=%d seqLen=%d must be >= 1", fn, B, S);
+  if (static_cast<int64_t>(B) * S > INT32_MAX) return fail(QSA_E_SHAPE, "%s: batchSize*seqLen exceeds INT32_MAX", fn);
+  if (NB < (S + 3) / 4) return fail(QSA_E_SHAPE, "%s: numBlocks=%d < ceilDiv(seqLen=%d, 4)", fn, NB, S);
+  if (rowStart < 0 || numRows < 0 || static_cast<int64_t>(rowStart) + numRows > static_cast<int64_t>(B) * S)
+    return fail(QSA_E_RANGE, "%s: rows [%d, %d + %d) outside [0, %lld)", fn, rowStart, rowStart, numRows,
+                static_cast<long long>(B) * S);
+  if (!aligned(outIdx, 4) || !aligned(in, 4) || !aligned(ctx, 4))
+    return fail(QSA_E_ALIGN, "%s: arrays must be 4-byte aligned", fn);
+  return QSA_OK;
+}
+}  // namespace
+
+QSA_API int qsa_index_expand(int32_t* outIdx, const int32_t* sortedIds, const int32_t* contextLengths,
+                             int32_t batchSize, int32_t seqLen, int32_t numBlocks, int32_t rowStart,
+                             int32_t numRows, qsa_stream_t stream) {
+  static const char* fn = "qsa_index_expand";
+  int st = validate_selection(fn, outIdx, sortedIds, contextLengths, batchSize, seqLen, numBlocks, rowStart, numRows);
+  if (st != QSA_OK) return st;
+  if (numRows == 0) {
+    g_last_error[0] = '\0';
+    return QSA_OK;
+  }
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  return launched(fn, qsa::launch_expand(outIdx, sortedIds, contextLengths, seqLen, numBlocks, rowStart, numRows,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QSA_API int qsa_index_topk_expand(int32_t* outIdx, const float* logits, const int32_t* contextLengths,
+                                  int32_t batchSize, int32_t seqLen, int32_t numBlocks, int32_t rowStart,
+                                  int32_t numRows, qsa_stream_t stream) {
+  static const char* fn = "qsa_index_topk_expand";
+  int st = validate_selection(fn, outIdx, logits, contextLengths, batchSize, seqLen, numBlocks, rowStart, numRows);
+  if (st != QSA_OK) return st;
+  if (qsa::topk_smem_bytes(numBlocks) > 200 * 1024)
+    return fail(QSA_E_SHAPE, "%s: numBlocks=%d too large for a row's keys in shared memory", fn, numBlocks);
+  if (numRows == 0) {
+    g_last_error[0] = '\0';
+    return QSA_OK;
+  }
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  return launched(fn, qsa::launch_topk_expand(outIdx, logits, contextLengths, seqLen, numBlocks, rowStart, numRows,
+                                              d.num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 QSA_API int qsa_testing_index_scores_cuda_core(qsa_dtype_t dtype, float* logits, const void* qNormed,
                                                const void* kbar, const int32_t* contextLengths,
                                                int32_t batchSize, int32_t seqLen, int32_t numBlocks,

@@ -71,6 +71,15 @@ int64_t scores_work_units(int32_t batch, int32_t seq_len, int32_t num_blocks, in
                           int32_t num_rows);
 int64_t scores_no_alloc_max_units();
 
+// Prefill selection (k34_select.cu)
+cudaError_t launch_ids_fill(int32_t* ids, int32_t num_rows, int32_t num_blocks, int num_sms, cudaStream_t stream);
+cudaError_t launch_expand(int32_t* out_idx, const int32_t* sorted_ids, const int32_t* ctx, int32_t seq_len,
+                          int32_t num_blocks, int32_t row_start, int32_t num_rows, cudaStream_t stream);
+cudaError_t launch_topk_expand(int32_t* out_idx, const float* logits, const int32_t* ctx, int32_t seq_len,
+                               int32_t num_blocks, int32_t row_start, int32_t num_rows, int num_sms,
+                               cudaStream_t stream);
+size_t topk_smem_bytes(int32_t num_blocks);
+
 // Device fault flags: bits set by bounded waits that ran out (k2_scores_tc.cu, k1_stream.cu).
 cudaError_t read_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
 cudaError_t read_k1_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
