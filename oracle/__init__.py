@@ -92,8 +92,46 @@ def _load():
         lib.qsa_oracle_select_expand_row.restype = None
         lib.qsa_oracle_select_expand.argtypes = [p, p, p, i32, i32, i32, i32, i32, p]
         lib.qsa_oracle_select_expand.restype = ctypes.c_int
+        pp = ctypes.POINTER(PoolState)
+        lib.qsa_oracle_k_compress_paged.argtypes = [ctypes.c_int, p, p, p, p, p, f32, pp,
+                                                    i32, i32, i32, i32, i32, i32]
+        lib.qsa_oracle_k_compress_paged.restype = ctypes.c_int
+        lib.qsa_oracle_raw_k_tail_write_prefill.argtypes = [p, p, pp, i32, i32]
+        lib.qsa_oracle_raw_k_tail_write_prefill.restype = ctypes.c_int
+        lib.qsa_oracle_pre_decode.argtypes = [ctypes.c_int, p, p, p, p, p, p, f32, pp, i32]
+        lib.qsa_oracle_pre_decode.restype = ctypes.c_int
+        lib.qsa_oracle_scores_decode.argtypes = [ctypes.c_int, p, p, p, pp, i32, i32]
+        lib.qsa_oracle_scores_decode.restype = ctypes.c_int
+        lib.qsa_oracle_topk_expand_decode.argtypes = [p, p, p, p, i32, i32, i32, p]
+        lib.qsa_oracle_topk_expand_decode.restype = ctypes.c_int
         _lib = lib
         return lib
+
+
+class PoolState(ctypes.Structure):
+    """Mirror of the oracle's pool descriptor (pool, pageTable, sizes)."""
+    _fields_ = [("pool", ctypes.c_void_p), ("pageTable", ctypes.c_void_p),
+                ("maxPagesPerSeq", ctypes.c_int32), ("numPages", ctypes.c_int32),
+                ("numKVHeads", ctypes.c_int32), ("poolHeadDim", ctypes.c_int32),
+                ("headSize", ctypes.c_int32)]
+
+
+class Pool:
+    """A host copy of a paged indexer pool: pool [2*numPages, 128, numKVHeads,
+    poolHeadDim] uint16 and pageTable [B, 2, maxPagesPerSeq] int32 (V ids already
+    offset by +numPages, -1 = unused)."""
+
+    def __init__(self, pool, page_table, num_pages, num_kv_heads=2, pool_head_dim=384, head_size=256):
+        self.pool = np.ascontiguousarray(pool, dtype=np.uint16)
+        self.page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+        self.num_pages = num_pages
+        self.num_kv_heads = num_kv_heads
+        self.pool_head_dim = pool_head_dim
+        self.head_size = head_size
+
+    def state(self):
+        return PoolState(self.pool.ctypes.data, self.page_table.ctypes.data, self.page_table.shape[2],
+                         self.num_pages, self.num_kv_heads, self.pool_head_dim, self.head_size)
 
 
 def _ptr(a: np.ndarray) -> int:
@@ -290,4 +328,70 @@ def select_expand(logits, context_lengths, B: int, S: int, row_start: int = 0,
     rc = lib.qsa_oracle_select_expand(_ptr(out), _ptr(lg), _ptr(ctx), B, S, nb, row_start, num_rows,
                                       _ptr(scratch))
     assert rc == 0
+    return out
+
+
+# ------------------------------------------------------ paged pool, decode path
+
+def k_compress_paged(dtype, index_qk, cos_sin, context_lengths, w_k, eps, pool: Pool, num_blocks,
+                     block_begin, block_end, past_len, kbar_init=None):
+    """K1b-paged: returns kbar; pool.pool is updated in place (V-tails of valid blocks)."""
+    lib = _load()
+    iq = _u16(index_qk)
+    B, S, _ = iq.shape
+    out = (np.zeros((B, num_blocks, 128), np.uint16) if kbar_init is None
+           else np.array(kbar_init, np.uint16, copy=True))
+    st = pool.state()
+    rc = lib.qsa_oracle_k_compress_paged(DTYPES[dtype], _ptr(out), _ptr(iq), _ptr(_f32(cos_sin)),
+                                         _ptr(_i32(context_lengths)), _ptr(_u16(w_k)), float(eps),
+                                         ctypes.byref(st), B, S, num_blocks, block_begin, block_end, past_len)
+    assert rc == 0
+    return out
+
+
+def raw_k_tail_write_prefill(index_qk, context_lengths, pool: Pool):
+    lib = _load()
+    iq = _u16(index_qk)
+    B, S, _ = iq.shape
+    st = pool.state()
+    assert lib.qsa_oracle_raw_k_tail_write_prefill(_ptr(iq), _ptr(_i32(context_lengths)), ctypes.byref(st),
+                                                   B, S) == 0
+
+
+def pre_decode(dtype, index_qk_rows, cos_sin, context_lengths, w_q, w_k, eps, pool: Pool):
+    """B1: index_qk_rows [B, 640] (one new token each) -> qNormed [B, 1, 4, 128]; pool updated."""
+    lib = _load()
+    iq = _u16(index_qk_rows).reshape(-1, 640)
+    B = iq.shape[0]
+    q = np.empty((B, 1, 4, 128), np.uint16)
+    st = pool.state()
+    assert lib.qsa_oracle_pre_decode(DTYPES[dtype], _ptr(q), _ptr(iq), _ptr(_f32(cos_sin)),
+                                     _ptr(_i32(context_lengths)), _ptr(_u16(w_q)), _ptr(_u16(w_k)),
+                                     float(eps), ctypes.byref(st), B) == 0
+    return q
+
+
+def scores_decode(dtype, q_normed, context_lengths, pool: Pool, max_blocks, logits_init=None):
+    """B2: logits [B, max_blocks]; only [0, ctx/4) of each row is written."""
+    lib = _load()
+    q = _u16(q_normed).reshape(-1, 4, 128)
+    B = q.shape[0]
+    out = (np.full((B, max_blocks), np.nan, np.float32) if logits_init is None
+           else np.array(logits_init, np.float32, copy=True))
+    st = pool.state()
+    assert lib.qsa_oracle_scores_decode(DTYPES[dtype], _ptr(out), _ptr(q), _ptr(_i32(context_lengths)),
+                                        ctypes.byref(st), B, max_blocks) == 0
+    return out
+
+
+def topk_expand_decode(logits, context_lengths, split_counters=None, num_kv_heads=2):
+    """B3: outIdx [B, 2051] (and split_counters zeroed in place when given)."""
+    lib = _load()
+    lg = _f32(logits)
+    B, maxb = lg.shape
+    out = np.empty((B, INDEX_WIDTH), np.int32)
+    scratch = np.empty(4 * max(maxb, 1), np.uint32)
+    sc = 0 if split_counters is None else _ptr(split_counters)
+    assert lib.qsa_oracle_topk_expand_decode(_ptr(out), _ptr(lg), _ptr(_i32(context_lengths)), sc,
+                                             num_kv_heads, B, maxb, _ptr(scratch)) == 0
     return out

@@ -414,3 +414,202 @@ int qsa_oracle_select_expand(int32_t* outIdx, const float* logits, const int32_t
   }
   return 0;
 }
+
+/* ------------------------------------------------- paged pool (decode state) */
+
+/*
+ * QsaIndexerPoolState: pool [2*numPages, 128, numKVHeads, poolHeadDim] T; element
+ * (page, row, head, col) at ((page*128 + row)*numKVHeads + head)*poolHeadDim + col.
+ * pageTable [B, 2, maxPagesPerSeq]: plane 0 = K pages, plane 1 = V pages (ids already
+ * offset by +numPages).  Token t's raw index-K tail: K page pageTable[b][0][t >> 7],
+ * row t & 127, head 0, columns [headSize, headSize + 128).  Block g's kbar: V page
+ * pageTable[b][1][(4g) >> 7], row (4g) & 127, head 0, same columns.  Entries equal to
+ * -1 (unused) -- and slots past maxPagesPerSeq or ids outside the pool -- mean
+ * "nothing persistable here" and are never dereferenced.
+ */
+typedef struct {
+  uint16_t* pool;
+  const int32_t* pageTable;
+  int32_t maxPagesPerSeq;
+  int32_t numPages;
+  int32_t numKVHeads;
+  int32_t poolHeadDim;
+  int32_t headSize;
+} qsa_oracle_pool_t;
+
+#define QSA_PAGE_TOKENS 128
+
+static uint16_t* pool_tail(const qsa_oracle_pool_t* ps, int32_t b, int32_t plane, int32_t token) {
+  if (token < 0) return 0;
+  int32_t slot = token / QSA_PAGE_TOKENS;
+  if (slot >= ps->maxPagesPerSeq) return 0;
+  int32_t page = ps->pageTable[((int64_t)b * 2 + plane) * ps->maxPagesPerSeq + slot];
+  if (page < 0 || page >= 2 * ps->numPages) return 0;
+  int64_t row = token % QSA_PAGE_TOKENS;
+  int64_t off = (((int64_t)page * QSA_PAGE_TOKENS + row) * ps->numKVHeads + 0) * ps->poolHeadDim + ps->headSize;
+  return ps->pool + off;
+}
+
+/* launchQsaIndexKCompressPaged: launchQsaIndexKCompress, and each VALID block's kbar
+ * row is also copied to the V-tail of token 4g when that page slot is usable. */
+int qsa_oracle_k_compress_paged(int dtype, uint16_t* kbar, const uint16_t* indexQk, const float* cosSin,
+                                const int32_t* contextLengths, const uint16_t* wK, float eps,
+                                const qsa_oracle_pool_t* ps, int32_t B, int32_t S, int32_t numBlocks,
+                                int32_t blockBegin, int32_t blockEnd, int32_t pastLen) {
+  int rc = qsa_oracle_k_compress(dtype, kbar, indexQk, cosSin, contextLengths, wK, eps, B, S, numBlocks,
+                                 blockBegin, blockEnd, pastLen);
+  if (rc) return rc;
+  for (int32_t b = 0; b < B; ++b)
+    for (int32_t g = blockBegin; g < blockEnd; ++g) {
+      if (!qsa_oracle_block_valid(g, contextLengths[b], S, pastLen)) continue;
+      uint16_t* dst = pool_tail(ps, b, 1, QSA_COMPRESS_RATIO * g);
+      if (dst) memcpy(dst, kbar + ((int64_t)b * numBlocks + g) * QSA_HEAD_DIM, 2 * QSA_HEAD_DIM);
+    }
+  return 0;
+}
+
+/* launchQsaRawKTailWritePrefill: tokens t in [ctx - ctx % 4, ctx) copy their raw
+ * index-K (indexQk columns [512, 640)) bit for bit to their K-tails. */
+int qsa_oracle_raw_k_tail_write_prefill(const uint16_t* indexQk, const int32_t* contextLengths,
+                                        const qsa_oracle_pool_t* ps, int32_t B, int32_t S) {
+  for (int32_t b = 0; b < B; ++b) {
+    int32_t c = contextLengths[b];
+    if (c <= 0) continue;
+    for (int32_t t = c - c % QSA_COMPRESS_RATIO; t < c && t < S; ++t) {
+      uint16_t* dst = pool_tail(ps, b, 0, t);
+      if (dst) memcpy(dst, indexQk + ((int64_t)b * S + t) * QSA_ROW_WIDTH + QSA_K_COL, 2 * QSA_HEAD_DIM);
+    }
+  }
+  return 0;
+}
+
+/*
+ * launchQsaIndexerPreDecode, per sequence b with one new token (indexQk [B, 640]) and
+ * TOTAL length ctx = contextLengths[b], pos = ctx - 1:
+ *   ctx <= 0: qNormed[b] = exact zeros, nothing else.
+ *   q-prep of the new row at rope position pos (launchQsaIndexQPrep numerics).
+ *   ctx % 4 != 0: the row's raw index-K goes bit for bit to the K-tail of pos.
+ *   ctx % 4 == 0: block g = ctx/4 - 1 is complete: tokens 4g..4g+2 come from their
+ *   K-tails, token 4g+3 from the new row; launchQsaIndexKCompress numerics; the kbar
+ *   row goes to the V-tail of 4g.  If a needed page slot is unusable, the block is
+ *   not written.
+ */
+int qsa_oracle_pre_decode(int dtype, uint16_t* qNormed, const uint16_t* indexQk, const float* cosSin,
+                          const int32_t* contextLengths, const uint16_t* wQ, const uint16_t* wK, float eps,
+                          const qsa_oracle_pool_t* ps, int32_t B) {
+  for (int32_t b = 0; b < B; ++b) {
+    int32_t c = contextLengths[b];
+    uint16_t* q = qNormed + (int64_t)b * QSA_NUM_Q_HEADS * QSA_HEAD_DIM;
+    const uint16_t* in = indexQk + (int64_t)b * QSA_ROW_WIDTH;
+    if (c <= 0) {
+      memset(q, 0, sizeof(uint16_t) * QSA_NUM_Q_HEADS * QSA_HEAD_DIM);
+      continue;
+    }
+    int32_t pos = c - 1;
+    for (int h = 0; h < QSA_NUM_Q_HEADS; ++h) {
+      float x[QSA_HEAD_DIM];
+      for (int d = 0; d < QSA_HEAD_DIM; ++d) x[d] = qsa_oracle_t_to_f32(dtype, in[h * QSA_HEAD_DIM + d]);
+      qsa_oracle_norm_rope(dtype, x, wQ, eps, cosSin + (int64_t)pos * 64, q + h * QSA_HEAD_DIM);
+    }
+    if (c % QSA_COMPRESS_RATIO != 0) {
+      uint16_t* dst = pool_tail(ps, b, 0, pos);
+      if (dst) memcpy(dst, in + QSA_K_COL, 2 * QSA_HEAD_DIM);
+      continue;
+    }
+    int32_t g = c / QSA_COMPRESS_RATIO - 1;
+    const uint16_t* k[QSA_COMPRESS_RATIO];
+    int ok = 1;
+    for (int j = 0; j < QSA_COMPRESS_RATIO - 1; ++j) {
+      k[j] = pool_tail(ps, b, 0, QSA_COMPRESS_RATIO * g + j);
+      if (!k[j]) ok = 0;
+    }
+    k[QSA_COMPRESS_RATIO - 1] = in + QSA_K_COL;
+    uint16_t* dst = pool_tail(ps, b, 1, QSA_COMPRESS_RATIO * g);
+    if (!ok || !dst) continue;
+    uint16_t m[QSA_HEAD_DIM];
+    qsa_oracle_block_mean(dtype, k[0], k[1], k[2], k[3], m);
+    float x[QSA_HEAD_DIM];
+    for (int d = 0; d < QSA_HEAD_DIM; ++d) x[d] = qsa_oracle_t_to_f32(dtype, m[d]);
+    qsa_oracle_norm_rope(dtype, x, wK, eps, cosSin + (int64_t)QSA_COMPRESS_RATIO * g * 64, dst);
+  }
+  return 0;
+}
+
+/*
+ * launchQsaIndexScoresDecode: logits[b][g] for g < nVis = ctx/4 only, K2 numerics
+ * with kbar gathered from the V-tail of token 4g; a block whose page slot is
+ * unusable scores -FLT_MAX (reading: "nothing persistable here").  Entries at
+ * g >= nVis are not written.
+ */
+int qsa_oracle_scores_decode(int dtype, float* logits, const uint16_t* qNormed, const int32_t* contextLengths,
+                             const qsa_oracle_pool_t* ps, int32_t B, int32_t maxBlocks) {
+  const float scale = 1.0f / sqrtf(128.0f);
+  for (int32_t b = 0; b < B; ++b) {
+    int32_t c = contextLengths[b];
+    int32_t nVis = c > 0 ? c / QSA_COMPRESS_RATIO : 0;
+    if (nVis > maxBlocks) nVis = maxBlocks;
+    const uint16_t* q = qNormed + (int64_t)b * QSA_NUM_Q_HEADS * QSA_HEAD_DIM;
+    float qf[QSA_NUM_Q_HEADS][QSA_HEAD_DIM];
+    for (int h = 0; h < QSA_NUM_Q_HEADS; ++h)
+      for (int d = 0; d < QSA_HEAD_DIM; ++d) qf[h][d] = qsa_oracle_t_to_f32(dtype, q[h * QSA_HEAD_DIM + d]);
+    for (int32_t g = 0; g < nVis; ++g) {
+      const uint16_t* k = pool_tail(ps, b, 1, QSA_COMPRESS_RATIO * g);
+      float* out = logits + (int64_t)b * maxBlocks + g;
+      if (!k) { *out = -FLT_MAX; continue; }
+      float sum = 0.0f;
+      for (int h = 0; h < QSA_NUM_Q_HEADS; ++h) {
+        float dot = 0.0f;
+        for (int d = 0; d < QSA_HEAD_DIM; ++d) {
+          float p = qf[h][d] * qsa_oracle_t_to_f32(dtype, k[d]);
+          dot = dot + p;
+        }
+        float rel = fmaxf(0.0f, dot);
+        sum = sum + rel;
+      }
+      *out = scale * sum;
+    }
+  }
+  return 0;
+}
+
+/*
+ * launchQsaTopKExpandDecode, per sequence b (ctx = contextLengths[b], nVis = ctx/4,
+ * kSel = min(512, nVis), tail = ctx % 4): splitCounters[b*numKVHeads ..) zeroed if
+ * given; the selected set is the first kSel blocks of the stable descending sort of
+ * logits[b][0..nVis) (keys above the kSel-th largest, ties in ascending id), emitted
+ * in ascending block order; out[b][4i + j] = sel[i]*4 + j, then tokens 4*nVis + j for
+ * j < tail, then -1 to width 2051.  scratch: 4 * maxBlocks words.
+ */
+int qsa_oracle_topk_expand_decode(int32_t* outIdx, const float* logits, const int32_t* contextLengths,
+                                  int32_t* splitCounters, int32_t numKVHeads, int32_t B, int32_t maxBlocks,
+                                  uint32_t* scratch) {
+  for (int32_t b = 0; b < B; ++b) {
+    if (splitCounters)
+      for (int32_t h = 0; h < numKVHeads; ++h) splitCounters[(int64_t)b * numKVHeads + h] = 0;
+    int32_t* out = outIdx + (int64_t)b * QSA_INDEX_WIDTH;
+    for (int32_t i = 0; i < QSA_INDEX_WIDTH; ++i) out[i] = -1;
+    int32_t c = contextLengths[b];
+    if (c <= 0) continue;
+    int32_t nVis = c / QSA_COMPRESS_RATIO;
+    if (nVis > maxBlocks) nVis = maxBlocks;
+    if (nVis < 0) nVis = 0;
+    int32_t kSel = nVis < QSA_TOPK_BLOCKS ? nVis : QSA_TOPK_BLOCKS;
+    int32_t tail = c % QSA_COMPRESS_RATIO;
+    uint32_t* key = scratch;
+    int32_t* id = (int32_t*)(scratch + maxBlocks);
+    uint32_t* tk = scratch + 2 * (int64_t)maxBlocks;
+    int32_t* ti = (int32_t*)(scratch + 3 * (int64_t)maxBlocks);
+    for (int32_t g = 0; g < nVis; ++g) { key[g] = qsa_oracle_orderable(logits[(int64_t)b * maxBlocks + g]); id[g] = g; }
+    stable_sort_desc(key, id, tk, ti, nVis);
+    /* ascending block order of the selected set: mark, then scan */
+    uint8_t* mark = (uint8_t*)tk;
+    memset(mark, 0, (size_t)nVis);
+    for (int32_t i = 0; i < kSel; ++i) mark[id[i]] = 1;
+    int32_t n = 0;
+    for (int32_t g = 0; g < nVis; ++g)
+      if (mark[g])
+        for (int32_t j = 0; j < QSA_COMPRESS_RATIO; ++j) out[n++] = g * QSA_COMPRESS_RATIO + j;
+    for (int32_t j = 0; j < tail; ++j) out[n++] = QSA_COMPRESS_RATIO * nVis + j;
+  }
+  return 0;
+}

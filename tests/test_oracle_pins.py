@@ -566,3 +566,98 @@ def test_select_expand_rows_and_golden():
         prefix = np.array(c["prefix"], np.int32)
         assert np.array_equal(out[:len(prefix)], prefix), c
         assert np.all(out[len(prefix):] == -1), c
+
+
+# ------------------------------------------------------------- decode path
+
+def _decode_sequence(dtype, total, prefill, seed, unused=()):
+    """Prefill `prefill` tokens (paged K1b + raw-K tail write), then decode one token at
+    a time up to `total`; returns the pool, per-step qNormed and the full workload."""
+    import pool_util
+    wl = workloads.custom(2, total, [total, total - 3], dtype=dtype, seed=seed, nan_padding=False,
+                          max_positions=total)
+    pool = pool_util.make_pool(2, total, seed, unused_slots=unused)
+    pctx = np.minimum(wl.context_lengths, prefill).astype(np.int32)
+    nbp = (prefill + 3) // 4
+    iq_pre = np.ascontiguousarray(wl.index_qk[:, :prefill])
+    oracle.k_compress_paged(dtype, iq_pre, wl.cos_sin, pctx, wl.w_k, wl.eps, pool, nbp, 0, nbp, 0)
+    oracle.raw_k_tail_write_prefill(iq_pre, pctx, pool)
+    qs = {}
+    for pos in range(prefill, total):
+        ctx = np.array([min(pos + 1, c) for c in wl.context_lengths], np.int32)
+        active = np.array([pos < c for c in wl.context_lengths])
+        ctx = np.where(active, ctx, 0).astype(np.int32)
+        rows = np.ascontiguousarray(wl.index_qk[:, pos])
+        qs[pos] = (ctx, oracle.pre_decode(dtype, rows, wl.cos_sin, ctx, wl.w_q, wl.w_k, wl.eps, pool))
+    return wl, pool, qs
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_decode_compress_bit_identical_to_prefill_and_addressing(dtype):
+    import pool_util
+    total, prefill = 300, 133
+    wl, pool, qs = _decode_sequence(dtype, total, prefill, seed=7)
+    NB = total // 4
+    full_k = oracle.k_compress(dtype, wl.index_qk, wl.cos_sin, wl.context_lengths, wl.w_k, wl.eps,
+                               (total + 3) // 4, 0, (total + 3) // 4, 0)
+    full_q = oracle.q_prep(dtype, wl.index_qk, wl.cos_sin, wl.context_lengths, wl.w_q, wl.eps)
+    for b in range(2):
+        c = int(wl.context_lengths[b])
+        for g in range(c // 4):           # every completed block, prefill or decode made
+            assert np.array_equal(pool_util.v_tail(pool, b, g), full_k[b, g]), (b, g)
+        for g in range(c // 4, NB):        # never completed: the V-tail row is untouched
+            assert np.all(pool_util.v_tail(pool, b, g) == 0x5A5A)
+        for t in range(c - c % 4, c):      # raw keys of the open block, bit for bit
+            assert np.array_equal(pool_util.k_tail(pool, b, t), wl.index_qk[b, t, 512:])
+        for pos in range(prefill, c):
+            assert np.array_equal(qs[pos][1][b, 0], full_q[b, pos]), (b, pos)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_decode_scores_and_selection_match_prefill(dtype):
+    import pool_util
+    total, prefill = 2300, 2100
+    wl, pool, qs = _decode_sequence(dtype, total, prefill, seed=9)
+    full_q = oracle.q_prep(dtype, wl.index_qk, wl.cos_sin, wl.context_lengths, wl.w_q, wl.eps)
+    NB = (total + 3) // 4
+    full_k = oracle.k_compress(dtype, wl.index_qk, wl.cos_sin, wl.context_lengths, wl.w_k, wl.eps, NB, 0, NB, 0)
+    maxb = NB + 5
+    for pos in (prefill, prefill + 1, prefill + 3, total - 1):
+        ctx, q = qs[pos]
+        lg = oracle.scores_decode(dtype, q, ctx, pool, maxb)
+        sc = np.full((2, 2), 9, np.int32)
+        sel = oracle.topk_expand_decode(lg, ctx, sc)
+        assert not sc.any()
+        for b in range(2):
+            if ctx[b] <= 0:
+                assert np.all(sel[b] == -1)
+                continue
+            t = int(ctx[b]) - 1
+            nvis = int(ctx[b]) // 4
+            ref = oracle.scores_row(dtype, full_q[b, t], full_k[b], t, int(ctx[b]))
+            assert np.array_equal(lg[b, :nvis].view(np.uint32), ref[:nvis].view(np.uint32))
+            assert np.all(np.isnan(lg[b, nvis:]))                       # only the prefix written
+            pre = oracle.select_expand_row(ref, t, int(ctx[b]))
+            n = int((pre >= 0).sum())
+            assert int((sel[b] >= 0).sum()) == n and np.all(sel[b][n:] == -1)
+            k = 4 * min(512, nvis)
+            assert np.array_equal(np.sort(sel[b][:k]), np.sort(pre[:k]))  # identical block sets
+            assert np.all(np.diff(sel[b][:k:4]) > 0)                    # ascending block order
+            assert np.array_equal(sel[b][k:n], pre[k:n])                # the open block's tokens
+
+
+def test_unused_page_entries_are_never_dereferenced():
+    import pool_util
+    dtype = "bf16"
+    total, prefill = 520, 300
+    # sequence 0: its K page slot 1 and V page slot 2 are unused
+    wl, pool, qs = _decode_sequence(dtype, total, prefill, seed=13, unused=((0, 0, 1), (0, 1, 2)))
+    table = pool.page_table
+    used = set(table[table >= 0].ravel().tolist())
+    unused_pages = [p for p in range(2 * pool.num_pages) if p not in used]
+    assert np.all(pool.pool[unused_pages] == 0x5A5A)                   # nothing landed elsewhere
+    # blocks whose V slot is unused score -FLT_MAX in decode
+    ctx, q = qs[total - 1]
+    lg = oracle.scores_decode(dtype, q, ctx, pool, total // 4 + 2)
+    g_unused = [g for g in range(ctx[0] // 4) if (4 * g) // 128 == 2]
+    assert g_unused and np.all(lg[0, g_unused] == NEG_MAX)
