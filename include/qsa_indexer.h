@@ -221,6 +221,100 @@ int qsa_index_topk_expand(int32_t* outIdx, const float* logits, const int32_t* c
                           int32_t numRows, qsa_stream_t stream);
 
 /*
+ * QsaIndexerPoolState ("Qsa Indexer Kernels"): where the decode state lives.
+ *  poolPtr      [2*numPages, 128, numKVHeads, poolHeadDim] T, element (page, row, head,
+ *               col) at ((page*128 + row)*numKVHeads + head)*poolHeadDim + col
+ *  pageTable    INT32 [B, 2, maxPagesPerSeq]: plane 0 = K pages, plane 1 = V pages
+ *               (ids already offset by +numPages); -1 = unused
+ * Token t's raw index-K tail: K page pageTable[b][0][t >> 7], row t & 127, head 0,
+ * columns [headSize, headSize + 128).  Block g's kbar: V page pageTable[b][1][(4g) >> 7],
+ * row (4g) & 127, head 0, same columns.  A slot past maxPagesPerSeq, an entry of -1 or
+ * an id outside [0, 2*numPages) is never dereferenced: writes there are skipped.
+ * Requirements: headSize + 128 <= poolHeadDim, headSize and poolHeadDim multiples of
+ * 8, poolPtr 16-byte aligned.  The struct is a host object; its pointers are device
+ * pointers.
+ */
+typedef struct {
+  void* poolPtr;
+  const int32_t* pageTable;
+  int32_t maxPagesPerSeq;
+  int32_t numPages;   /* K-plane page count */
+  int32_t numKVHeads;
+  int32_t poolHeadDim;
+  int32_t headSize;   /* tail column offset */
+} qsa_pool_state_t;
+
+/*
+ * launchQsaIndexKCompressPaged: qsa_index_k_compress, and every VALID block's kbar
+ * row is also written to the V-tail of token 4g.  The dense kbar output is
+ * bit-identical to qsa_index_k_compress; invalid blocks write dense zeros and never
+ * touch the pool; unusable page slots skip the pool write only.
+ * Errors: those of qsa_index_k_compress, plus QSA_E_NULL / QSA_E_SHAPE / QSA_E_ALIGN
+ * for the pool state.
+ */
+int qsa_index_k_compress_paged(qsa_dtype_t dtype, void* kbar, const void* indexQk,
+                               const float* cosSin, const int32_t* contextLengths, const void* wK,
+                               float rmsEps, const qsa_pool_state_t* pool, int32_t batchSize,
+                               int32_t seqLen, int32_t numBlocks, int32_t blockBegin,
+                               int32_t blockEnd, int32_t pastLen, qsa_stream_t stream);
+
+/*
+ * launchQsaRawKTailWritePrefill: for each sequence, tokens t in
+ * [ctx - ctx % 4, ctx) (the trailing incomplete block) copy indexQk row (b, t)
+ * columns [512, 640) BIT-UNMODIFIED to their K-tails.  Nothing else in the pool is
+ * touched.  0 <= contextLengths[b] <= seqLen.
+ */
+int qsa_raw_k_tail_write_prefill(qsa_dtype_t dtype, const void* indexQk, const int32_t* contextLengths,
+                                 const qsa_pool_state_t* pool, int32_t batchSize, int32_t seqLen,
+                                 qsa_stream_t stream);
+
+/*
+ * launchQsaIndexerPreDecode: one new token per sequence; contextLengths[b] is the
+ * TOTAL length including it, pos = ctx - 1.
+ *  qNormed  [out] T [batchSize, 1, 4, 128]: qsa_index_q_prep numerics at rope
+ *           position pos; exact zeros when ctx <= 0 (and nothing else is done).
+ *  indexQk  [in]  T [batchSize, 1, 640]
+ *  ctx % 4 != 0: the row's raw index-K goes bit for bit to the K-tail of pos.
+ *  ctx % 4 == 0: block g = ctx/4 - 1 is complete: the raw keys of 4g..4g+2 are read
+ *           from their K-tails, 4g+3 is the new row; qsa_index_k_compress numerics
+ *           (bit-identical to prefill); the kbar row goes to the V-tail of 4g.  If
+ *           any of those page slots is unusable the block is not written.
+ *  cosSin   FP32 [maxPositions, 64], maxPositions >= max ctx.
+ */
+int qsa_indexer_pre_decode(qsa_dtype_t dtype, void* qNormed, const void* indexQk, const float* cosSin,
+                           const int32_t* contextLengths, const void* wQ, const void* wK, float rmsEps,
+                           const qsa_pool_state_t* pool, int32_t batchSize, qsa_stream_t stream);
+
+/*
+ * launchQsaIndexScoresDecode: logits[b][g] = (1/sqrtf(128)) * sum_h relu(q[b][h] .
+ * kbar[b][g]) (FP32, ascending h, scale after the sum) for g < nVis = ctx/4, with
+ * kbar read from the V-tail of token 4g.  ONLY [0, nVis) of each row is written.  A
+ * block whose V page slot is unusable scores -FLT_MAX.
+ *  logits   [out] FP32 [batchSize, maxBlocks]; maxBlocks >= ceilDiv(max ctx, 4)
+ *  qNormed  [in]  T [batchSize, 1, 4, 128] (qsa_indexer_pre_decode's output)
+ */
+int qsa_index_scores_decode(qsa_dtype_t dtype, float* logits, const void* qNormed,
+                            const int32_t* contextLengths, const qsa_pool_state_t* pool,
+                            int32_t batchSize, int32_t maxBlocks, qsa_stream_t stream);
+
+/*
+ * launchQsaTopKExpandDecode, per sequence b (ctx = contextLengths[b], nVis = ctx/4,
+ * kSel = min(512, nVis), tail = ctx % 4):
+ *  splitCounters[b*numKVHeads .. +numKVHeads) are zeroed when splitCounters != NULL;
+ *  nVis <= 512 selects every block (logits not read); otherwise keys above the
+ *  kSel-th largest logit (order-preserving u32 map) and keys equal to it in
+ *  ascending block order until kSel are selected (the set the prefill selection
+ *  picks for identical logits); outIdx[b][4i + j] = sel[i]*4 + j with sel in
+ *  ascending order, then tokens 4*nVis + j for j < tail, then -1 to width 2051.
+ *  Deterministic: identical inputs give identical bits.
+ *  outIdx  [out] INT32 [batchSize, 1, 2051];  logits [in] FP32 [batchSize, maxBlocks]
+ *  (only [0, nVis) read).
+ */
+int qsa_topk_expand_decode(int32_t* outIdx, const float* logits, const int32_t* contextLengths,
+                           int32_t* splitCounters, int32_t numKVHeads, int32_t batchSize, int32_t maxBlocks,
+                           qsa_stream_t stream);
+
+/*
  * qsa_index_scores_no_alloc: the K2 scores of qsa_index_scores, for callers that
  * must not allocate device memory.  (No counterpart on the "Qsa Indexer Kernels"
  * page; an addition of this library.)

@@ -20,6 +20,8 @@ __all__ = [
     "QsaError", "QSA_BF16", "QSA_F16", "load", "lib", "qsa_abi_version", "qsa_last_error",
     "qsa_index_q_prep", "qsa_index_k_compress", "qsa_index_qk_prep", "qsa_index_scores",
     "qsa_index_scores_no_alloc", "qsa_index_ids_fill", "qsa_index_expand", "qsa_index_topk_expand",
+    "PoolState", "pool_state", "qsa_index_k_compress_paged", "qsa_raw_k_tail_write_prefill",
+    "qsa_indexer_pre_decode", "qsa_index_scores_decode", "qsa_topk_expand_decode",
     "qsa_device_fault_flags",
     "qsa_testing_index_scores_cuda_core", "LIB_PATH",
 ]
@@ -30,6 +32,8 @@ STATUS_NAMES = {0: "QSA_OK", -1: "QSA_E_NULL", -2: "QSA_E_SHAPE", -3: "QSA_E_RAN
                 -4: "QSA_E_DTYPE", -5: "QSA_E_ALIGN", -6: "QSA_E_CUDA", -7: "QSA_E_DEVICE"}
 EXPORTED = ["qsa_abi_version", "qsa_last_error", "qsa_index_q_prep", "qsa_index_k_compress",
             "qsa_index_qk_prep", "qsa_index_ids_fill", "qsa_index_expand", "qsa_index_topk_expand",
+            "qsa_index_k_compress_paged", "qsa_raw_k_tail_write_prefill", "qsa_indexer_pre_decode",
+            "qsa_index_scores_decode", "qsa_topk_expand_decode",
             "qsa_index_scores", "qsa_index_scores_no_alloc", "qsa_device_fault_flags",
             "qsa_testing_index_scores_cuda_core"]
 
@@ -38,6 +42,22 @@ class QsaError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
         self.status = status
+
+
+class PoolState(ctypes.Structure):
+    """qsa_pool_state_t: the paged indexer pool (device pointers, host struct)."""
+    _fields_ = [("poolPtr", ctypes.c_void_p), ("pageTable", ctypes.c_void_p),
+                ("maxPagesPerSeq", ctypes.c_int32), ("numPages", ctypes.c_int32),
+                ("numKVHeads", ctypes.c_int32), ("poolHeadDim", ctypes.c_int32),
+                ("headSize", ctypes.c_int32)]
+
+
+def pool_state(pool, pageTable, numPages, numKVHeads=2, poolHeadDim=384, headSize=256) -> PoolState:
+    """Describe a device pool [2*numPages, 128, numKVHeads, poolHeadDim] and its page table
+    [B, 2, maxPagesPerSeq] (V ids offset by +numPages, -1 = unused)."""
+    max_pages = pageTable.shape[-1] if hasattr(pageTable, "shape") else int(pageTable[1])
+    return PoolState(_addr(pool), _addr(pageTable), int(max_pages), int(numPages), int(numKVHeads),
+                     int(poolHeadDim), int(headSize))
 
 
 _lib = None
@@ -72,6 +92,17 @@ def load():
     L.qsa_index_expand.restype = ctypes.c_int
     L.qsa_index_topk_expand.argtypes = [p, p, p, i32, i32, i32, i32, i32, p]
     L.qsa_index_topk_expand.restype = ctypes.c_int
+    pp = ctypes.POINTER(PoolState)
+    L.qsa_index_k_compress_paged.argtypes = [ctypes.c_int, p, p, p, p, p, f32, pp, i32, i32, i32, i32, i32, i32, p]
+    L.qsa_index_k_compress_paged.restype = ctypes.c_int
+    L.qsa_raw_k_tail_write_prefill.argtypes = [ctypes.c_int, p, p, pp, i32, i32, p]
+    L.qsa_raw_k_tail_write_prefill.restype = ctypes.c_int
+    L.qsa_indexer_pre_decode.argtypes = [ctypes.c_int, p, p, p, p, p, p, f32, pp, i32, p]
+    L.qsa_indexer_pre_decode.restype = ctypes.c_int
+    L.qsa_index_scores_decode.argtypes = [ctypes.c_int, p, p, p, pp, i32, i32, p]
+    L.qsa_index_scores_decode.restype = ctypes.c_int
+    L.qsa_topk_expand_decode.argtypes = [p, p, p, p, i32, i32, i32, p]
+    L.qsa_topk_expand_decode.restype = ctypes.c_int
     L.qsa_index_scores.argtypes = [ctypes.c_int, p, p, p, p, i32, i32, i32, i32, i32, p]
     L.qsa_index_scores.restype = ctypes.c_int
     L.qsa_index_scores_no_alloc.argtypes = list(L.qsa_index_scores.argtypes)
@@ -186,6 +217,45 @@ def qsa_index_topk_expand(outIdx, logits, contextLengths, batchSize, seqLen, num
     """Prefill selection in one kernel: radix top-512 + order + expand (see include/qsa_indexer.h)."""
     _check(load().qsa_index_topk_expand(_addr(outIdx), _addr(logits), _addr(contextLengths), int(batchSize),
                                      int(seqLen), int(numBlocks), int(rowStart), int(numRows), _stream(stream)))
+
+
+def qsa_index_k_compress_paged(kbar, indexQk, cosSin, contextLengths, wK, rmsEps, pool: PoolState, batchSize,
+                               seqLen, numBlocks, blockBegin, blockEnd, pastLen, stream=None, dtype=None):
+    """K1b that also persists valid kbar rows to the pool V-tails (see include/qsa_indexer.h)."""
+    _check(load().qsa_index_k_compress_paged(_dtype(dtype, indexQk, kbar), _addr(kbar), _addr(indexQk),
+                                          _addr(cosSin), _addr(contextLengths), _addr(wK), float(rmsEps),
+                                          ctypes.byref(pool), int(batchSize), int(seqLen), int(numBlocks),
+                                          int(blockBegin), int(blockEnd), int(pastLen), _stream(stream)))
+
+
+def qsa_raw_k_tail_write_prefill(indexQk, contextLengths, pool: PoolState, batchSize, seqLen, stream=None,
+                                 dtype=None):
+    """Raw index-K of each sequence's trailing incomplete block -> pool K-tails."""
+    _check(load().qsa_raw_k_tail_write_prefill(_dtype(dtype, indexQk), _addr(indexQk), _addr(contextLengths),
+                                            ctypes.byref(pool), int(batchSize), int(seqLen), _stream(stream)))
+
+
+def qsa_indexer_pre_decode(qNormed, indexQk, cosSin, contextLengths, wQ, wK, rmsEps, pool: PoolState, batchSize,
+                           stream=None, dtype=None):
+    """Decode pre-pass: q-prep of the new token + K-tail write or block compress."""
+    _check(load().qsa_indexer_pre_decode(_dtype(dtype, indexQk, qNormed), _addr(qNormed), _addr(indexQk),
+                                      _addr(cosSin), _addr(contextLengths), _addr(wQ), _addr(wK), float(rmsEps),
+                                      ctypes.byref(pool), int(batchSize), _stream(stream)))
+
+
+def qsa_index_scores_decode(logits, qNormed, contextLengths, pool: PoolState, batchSize, maxBlocks, stream=None,
+                            dtype=None):
+    """Decode block logits from the pool V-tails (valid prefix [0, ctx/4) only)."""
+    _check(load().qsa_index_scores_decode(_dtype(dtype, qNormed), _addr(logits), _addr(qNormed),
+                                       _addr(contextLengths), ctypes.byref(pool), int(batchSize), int(maxBlocks),
+                                       _stream(stream)))
+
+
+def qsa_topk_expand_decode(outIdx, logits, contextLengths, splitCounters, numKVHeads, batchSize, maxBlocks,
+                           stream=None):
+    """Decode top-512 + expand (+ split-counter zeroing)."""
+    _check(load().qsa_topk_expand_decode(_addr(outIdx), _addr(logits), _addr(contextLengths), _addr(splitCounters),
+                                      int(numKVHeads), int(batchSize), int(maxBlocks), _stream(stream)))
 
 
 def qsa_index_scores_no_alloc(logits, qNormed, kbar, contextLengths, batchSize, seqLen, numBlocks,

@@ -18,12 +18,16 @@ namespace qsa {
 #define QSA_K1B_MINB 3
 #endif
 
-template <class T>
+// PAGED (launchQsaIndexKCompressPaged): additionally copy every VALID block's kbar
+// row to the pool V-tail of token 4g when that page slot is usable; the dense
+// output is the same code path, so it is bit-identical to the unpaged kernel.
+template <class T, bool PAGED>
 __global__ void __launch_bounds__(256, QSA_K1B_MINB)
 k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ index_qk,
                     const float* __restrict__ cos_sin, const int32_t* __restrict__ context_lengths,
                     const uint16_t* __restrict__ w_k, float eps, int32_t batch, int32_t seq_len,
-                    int32_t num_blocks, int32_t block_begin, int32_t block_end, int32_t past_len) {
+                    int32_t num_blocks, int32_t block_begin, int32_t block_end, int32_t past_len,
+                    const PoolDev pool) {
   const int lane = threadIdx.x & 31;
   const int j = lane & 7;
   const int ca = chunk_a(j);
@@ -87,6 +91,13 @@ k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ in
       uint16_t* dst = kbar + (static_cast<int64_t>(b) * num_blocks + g) * kHeadDim;
       st_v4(dst + ca, oa);
       st_v4(dst + cb, ob);
+      if (PAGED && valid) {
+        uint16_t* tail = pool_tail(pool, b, 1, kRatio * g);
+        if (tail != nullptr) {
+          st_v4(tail + ca, oa);
+          st_v4(tail + cb, ob);
+        }
+      }
     }
   }
 }
@@ -94,9 +105,9 @@ k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ in
 namespace {
 constexpr int kK1bThreads = 256;
 
-template <class T>
-cudaError_t launch_t(const LaunchKCompress& a) {
-  auto kern = k1b_compress_kernel<T>;
+template <class T, bool PAGED>
+cudaError_t launch_t(const LaunchKCompress& a, const PoolDev& pool) {
+  auto kern = k1b_compress_kernel<T, PAGED>;
   const int64_t units = static_cast<int64_t>(a.batch) * (a.block_end - a.block_begin);
   const int64_t blocks_needed = (units * 8 + kK1bThreads - 1) / kK1bThreads;
   int per_sm = 0;
@@ -107,13 +118,18 @@ cudaError_t launch_t(const LaunchKCompress& a) {
   kern<<<grid, kK1bThreads, 0, a.stream>>>(
       static_cast<uint16_t*>(a.kbar), static_cast<const uint16_t*>(a.index_qk), a.cos_sin,
       a.context_lengths, static_cast<const uint16_t*>(a.w_k), a.eps, a.batch, a.seq_len,
-      a.num_blocks, a.block_begin, a.block_end, a.past_len);
+      a.num_blocks, a.block_begin, a.block_end, a.past_len, pool);
   return cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_k_compress(const LaunchKCompress& a) {
-  return a.bf16 ? launch_t<Bf16>(a) : launch_t<F16>(a);
+  const PoolDev none{};
+  return a.bf16 ? launch_t<Bf16, false>(a, none) : launch_t<F16, false>(a, none);
+}
+
+cudaError_t launch_k_compress_paged(const LaunchKCompressPaged& a) {
+  return a.base.bf16 ? launch_t<Bf16, true>(a.base, a.pool) : launch_t<F16, true>(a.base, a.pool);
 }
 
 }  // namespace qsa

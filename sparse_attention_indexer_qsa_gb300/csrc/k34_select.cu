@@ -93,10 +93,14 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
   return base + incl - v;
 }
 
+// DECODE (launchQsaTopKExpandDecode): row b is sequence b's one new token at
+// t = ctx_b - 1, logits [B, num_blocks = maxBlocks], outIdx [B, 2051], and the
+// decode attention's split-K counters of b are zeroed first when given.
+template <bool DECODE>
 __global__ void __launch_bounds__(kSelThreads)
 topk_expand_kernel(int32_t* __restrict__ out_idx, const float* __restrict__ logits,
                    const int32_t* __restrict__ ctx, int32_t seq_len, int32_t num_blocks,
-                   int32_t row_start) {
+                   int32_t row_start, int32_t* __restrict__ split_counters, int32_t num_kv_heads) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ uint32_t hist[kSelWarps][256];
   __shared__ uint32_t warp_tot[kSelWarps];
@@ -107,10 +111,21 @@ topk_expand_kernel(int32_t* __restrict__ out_idx, const float* __restrict__ logi
   const uint32_t lt = lanemask_lt();
 
   const int32_t i = blockIdx.x;
-  const int64_t r = static_cast<int64_t>(row_start) + i;
-  const int32_t b = static_cast<int32_t>(r / seq_len);
-  const int32_t t = static_cast<int32_t>(r - static_cast<int64_t>(b) * seq_len);
-  const int32_t c = __ldg(ctx + b);
+  int64_t r;
+  int32_t b, t, c;
+  if (DECODE) {
+    r = i;
+    b = i;
+    c = __ldg(ctx + b);
+    t = c - 1;
+    if (split_counters != nullptr)
+      for (int k = tid; k < num_kv_heads; k += kSelThreads) split_counters[static_cast<int64_t>(b) * num_kv_heads + k] = 0;
+  } else {
+    r = static_cast<int64_t>(row_start) + i;
+    b = static_cast<int32_t>(r / seq_len);
+    t = static_cast<int32_t>(r - static_cast<int64_t>(b) * seq_len);
+    c = __ldg(ctx + b);
+  }
   int32_t* out = out_idx + r * kWidth;
   if (c <= 0 || t >= c) {  // padded row: all -1, logits not read
     for (int k = tid; k < kWidth; k += kSelThreads) out[k] = -1;
@@ -237,12 +252,26 @@ cudaError_t launch_topk_expand(int32_t* out_idx, const float* logits, const int3
   (void)num_sms;
   const size_t smem = topk_smem_bytes(num_blocks);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(sel::topk_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(sel::topk_expand_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  sel::topk_expand_kernel<<<num_rows, sel::kSelThreads, smem, stream>>>(out_idx, logits, ctx, seq_len, num_blocks,
-                                                                        row_start);
+  sel::topk_expand_kernel<false><<<num_rows, sel::kSelThreads, smem, stream>>>(out_idx, logits, ctx, seq_len,
+                                                                               num_blocks, row_start, nullptr, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_expand_decode(int32_t* out_idx, const float* logits, const int32_t* ctx,
+                                      int32_t* split_counters, int32_t num_kv_heads, int32_t batch,
+                                      int32_t max_blocks, cudaStream_t stream) {
+  const size_t smem = topk_smem_bytes(max_blocks);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(sel::topk_expand_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  sel::topk_expand_kernel<true><<<batch, sel::kSelThreads, smem, stream>>>(out_idx, logits, ctx, 1, max_blocks, 0,
+                                                                          split_counters, num_kv_heads);
   return cudaGetLastError();
 }
 

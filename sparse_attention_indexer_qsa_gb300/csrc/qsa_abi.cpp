@@ -285,6 +285,132 @@ QSA_API int qsa_index_topk_expand(int32_t* outIdx, const float* logits, const in
                                               d.num_sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+int validate_pool(const char* fn, const qsa_pool_state_t* ps, qsa::PoolDev* out) {
+  if (!ps || !ps->poolPtr || !ps->pageTable) return fail(QSA_E_NULL, "%s: null pool state or pool pointer", fn);
+  if (ps->maxPagesPerSeq < 1 || ps->numPages < 1 || ps->numKVHeads < 1 || ps->headSize < 0 ||
+      ps->headSize + 128 > ps->poolHeadDim)
+    return fail(QSA_E_SHAPE, "%s: pool needs maxPagesPerSeq, numPages, numKVHeads >= 1 and headSize + 128 <= poolHeadDim", fn);
+  if (ps->headSize % 8 != 0 || ps->poolHeadDim % 8 != 0 || !aligned(ps->poolPtr, 16) || !aligned(ps->pageTable, 4))
+    return fail(QSA_E_ALIGN, "%s: pool tails must be 16-byte aligned (headSize, poolHeadDim multiples of 8)", fn);
+  *out = qsa::PoolDev{static_cast<uint16_t*>(ps->poolPtr), ps->pageTable, ps->maxPagesPerSeq, ps->numPages,
+                      ps->numKVHeads, ps->poolHeadDim, ps->headSize};
+  return QSA_OK;
+}
+}  // namespace
+
+QSA_API int qsa_index_k_compress_paged(qsa_dtype_t dtype, void* kbar, const void* indexQk, const float* cosSin,
+                                       const int32_t* contextLengths, const void* wK, float rmsEps,
+                                       const qsa_pool_state_t* pool, int32_t batchSize, int32_t seqLen,
+                                       int32_t numBlocks, int32_t blockBegin, int32_t blockEnd, int32_t pastLen,
+                                       qsa_stream_t stream) {
+  static const char* fn = "qsa_index_k_compress_paged";
+  int st;
+  if ((st = check_dtype(fn, dtype)) != QSA_OK) return st;
+  if (!kbar || !indexQk || !cosSin || !contextLengths || !wK) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  qsa::PoolDev pd;
+  if ((st = validate_pool(fn, pool, &pd)) != QSA_OK) return st;
+  if (batchSize < 1 || seqLen < 1 || numBlocks < 1)
+    return fail(QSA_E_SHAPE, "%s: batchSize=%d seqLen=%d numBlocks=%d must be >= 1", fn, batchSize, seqLen, numBlocks);
+  if (static_cast<int64_t>(batchSize) * seqLen > INT32_MAX)
+    return fail(QSA_E_SHAPE, "%s: batchSize*seqLen exceeds INT32_MAX", fn);
+  if (blockBegin < 0 || blockBegin > blockEnd || blockEnd > numBlocks || pastLen < 0)
+    return fail(QSA_E_RANGE, "%s: need 0 <= blockBegin=%d <= blockEnd=%d <= numBlocks=%d and pastLen=%d >= 0", fn,
+                blockBegin, blockEnd, numBlocks, pastLen);
+  if (!aligned(kbar, 16) || !aligned(indexQk, 16) || !aligned(cosSin, 16) || !aligned(wK, 16) ||
+      !aligned(contextLengths, 4))
+    return fail(QSA_E_ALIGN, "%s: T and FP32 arrays must be 16-byte aligned, contextLengths 4-byte", fn);
+  if (blockBegin == blockEnd) {
+    g_last_error[0] = '\0';
+    return QSA_OK;
+  }
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  qsa::LaunchKCompressPaged a{{dtype == QSA_BF16, kbar, indexQk, cosSin, contextLengths, wK, rmsEps, batchSize, seqLen,
+                               numBlocks, blockBegin, blockEnd, pastLen, d.num_sms,
+                               reinterpret_cast<cudaStream_t>(stream)},
+                              pd};
+  return launched(fn, qsa::launch_k_compress_paged(a));
+}
+
+QSA_API int qsa_raw_k_tail_write_prefill(qsa_dtype_t dtype, const void* indexQk, const int32_t* contextLengths,
+                                         const qsa_pool_state_t* pool, int32_t batchSize, int32_t seqLen,
+                                         qsa_stream_t stream) {
+  static const char* fn = "qsa_raw_k_tail_write_prefill";
+  int st;
+  if ((st = check_dtype(fn, dtype)) != QSA_OK) return st;
+  if (!indexQk || !contextLengths) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  qsa::PoolDev pd;
+  if ((st = validate_pool(fn, pool, &pd)) != QSA_OK) return st;
+  if (batchSize < 1 || seqLen < 1) return fail(QSA_E_SHAPE, "%s: batchSize=%d seqLen=%d must be >= 1", fn, batchSize, seqLen);
+  if (static_cast<int64_t>(batchSize) * seqLen > INT32_MAX)
+    return fail(QSA_E_SHAPE, "%s: batchSize*seqLen exceeds INT32_MAX", fn);
+  if (!aligned(indexQk, 16) || !aligned(contextLengths, 4))
+    return fail(QSA_E_ALIGN, "%s: indexQk must be 16-byte aligned, contextLengths 4-byte", fn);
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  return launched(fn, qsa::launch_raw_k_tail_write_prefill(dtype == QSA_BF16, indexQk, contextLengths, pd, batchSize,
+                                                           seqLen, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QSA_API int qsa_indexer_pre_decode(qsa_dtype_t dtype, void* qNormed, const void* indexQk, const float* cosSin,
+                                   const int32_t* contextLengths, const void* wQ, const void* wK, float rmsEps,
+                                   const qsa_pool_state_t* pool, int32_t batchSize, qsa_stream_t stream) {
+  static const char* fn = "qsa_indexer_pre_decode";
+  int st;
+  if ((st = check_dtype(fn, dtype)) != QSA_OK) return st;
+  if (!qNormed || !indexQk || !cosSin || !contextLengths || !wQ || !wK)
+    return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  qsa::PoolDev pd;
+  if ((st = validate_pool(fn, pool, &pd)) != QSA_OK) return st;
+  if (batchSize < 1) return fail(QSA_E_SHAPE, "%s: batchSize=%d must be >= 1", fn, batchSize);
+  if (!aligned(qNormed, 16) || !aligned(indexQk, 16) || !aligned(cosSin, 16) || !aligned(wQ, 16) ||
+      !aligned(wK, 16) || !aligned(contextLengths, 4))
+    return fail(QSA_E_ALIGN, "%s: T and FP32 arrays must be 16-byte aligned, contextLengths 4-byte", fn);
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  return launched(fn, qsa::launch_pre_decode(dtype == QSA_BF16, qNormed, indexQk, cosSin, contextLengths, wQ, wK,
+                                             rmsEps, pd, batchSize, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QSA_API int qsa_index_scores_decode(qsa_dtype_t dtype, float* logits, const void* qNormed,
+                                    const int32_t* contextLengths, const qsa_pool_state_t* pool, int32_t batchSize,
+                                    int32_t maxBlocks, qsa_stream_t stream) {
+  static const char* fn = "qsa_index_scores_decode";
+  int st;
+  if ((st = check_dtype(fn, dtype)) != QSA_OK) return st;
+  if (!logits || !qNormed || !contextLengths) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  qsa::PoolDev pd;
+  if ((st = validate_pool(fn, pool, &pd)) != QSA_OK) return st;
+  if (batchSize < 1 || maxBlocks < 1 || maxBlocks > 65535 * 256)
+    return fail(QSA_E_SHAPE, "%s: batchSize=%d >= 1 and 1 <= maxBlocks=%d <= 16776960 required", fn, batchSize, maxBlocks);
+  if (!aligned(qNormed, 16) || !aligned(logits, 4) || !aligned(contextLengths, 4))
+    return fail(QSA_E_ALIGN, "%s: qNormed must be 16-byte aligned, logits/contextLengths 4-byte", fn);
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  return launched(fn, qsa::launch_scores_decode(dtype == QSA_BF16, logits, qNormed, contextLengths, pd, batchSize,
+                                                maxBlocks, score_scale(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+QSA_API int qsa_topk_expand_decode(int32_t* outIdx, const float* logits, const int32_t* contextLengths,
+                                   int32_t* splitCounters, int32_t numKVHeads, int32_t batchSize, int32_t maxBlocks,
+                                   qsa_stream_t stream) {
+  static const char* fn = "qsa_topk_expand_decode";
+  if (!outIdx || !logits || !contextLengths) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  if (batchSize < 1 || maxBlocks < 1) return fail(QSA_E_SHAPE, "%s: batchSize=%d maxBlocks=%d must be >= 1", fn, batchSize, maxBlocks);
+  if (splitCounters && numKVHeads < 0) return fail(QSA_E_SHAPE, "%s: numKVHeads=%d must be >= 0", fn, numKVHeads);
+  if (qsa::topk_smem_bytes(maxBlocks) > 200 * 1024)
+    return fail(QSA_E_SHAPE, "%s: maxBlocks=%d too large for a row's keys in shared memory", fn, maxBlocks);
+  if (!aligned(outIdx, 4) || !aligned(logits, 4) || !aligned(contextLengths, 4) || !aligned(splitCounters, 4))
+    return fail(QSA_E_ALIGN, "%s: arrays must be 4-byte aligned", fn);
+  DeviceInfo d;
+  int st = current_device(fn, &d);
+  if (st != QSA_OK) return st;
+  return launched(fn, qsa::launch_topk_expand_decode(outIdx, logits, contextLengths, splitCounters,
+                                                     splitCounters ? numKVHeads : 0, batchSize, maxBlocks,
+                                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 QSA_API int qsa_testing_index_scores_cuda_core(qsa_dtype_t dtype, float* logits, const void* qNormed,
                                                const void* kbar, const int32_t* contextLengths,
                                                int32_t batchSize, int32_t seqLen, int32_t numBlocks,

@@ -7,6 +7,32 @@
 
 namespace qsa {
 
+// Paged indexer state ("Qsa Indexer Kernels", QsaIndexerPoolState): pool
+// [2*numPages, 128, numKVHeads, poolHeadDim] T; page table [B, 2, maxPagesPerSeq]
+// (plane 0: K pages, plane 1: V pages with ids already offset by +numPages; -1 =
+// unused).  Token t's raw index-K tail: K page table[b][0][t >> 7], row t & 127,
+// head 0, columns [headSize, headSize + 128); block g's kbar: V page
+// table[b][1][(4g) >> 7], row (4g) & 127, head 0, same columns.
+struct PoolDev {
+  uint16_t* pool;
+  const int32_t* table;
+  int32_t max_pages, num_pages, num_kv_heads, pool_head_dim, head_size;
+};
+
+#ifdef __CUDACC__
+// The tail of `token` in `plane` (0 = K, 1 = V), or nullptr when the page slot is past
+// maxPagesPerSeq, unused (-1) or outside the pool: such entries are never dereferenced.
+__device__ __forceinline__ uint16_t* pool_tail(const PoolDev& p, int32_t b, int plane, int32_t token) {
+  if (token < 0) return nullptr;
+  const int32_t slot = token >> 7;
+  if (slot >= p.max_pages) return nullptr;
+  const int32_t page = __ldg(p.table + (static_cast<int64_t>(b) * 2 + plane) * p.max_pages + slot);
+  if (page < 0 || page >= 2 * p.num_pages) return nullptr;
+  const int64_t row = token & 127;
+  return p.pool + ((static_cast<int64_t>(page) * 128 + row) * p.num_kv_heads) * p.pool_head_dim + p.head_size;
+}
+#endif
+
 struct LaunchQPrep {
   bool bf16;
   void* q_normed;
@@ -31,6 +57,11 @@ struct LaunchKCompress {
   int32_t batch, seq_len, num_blocks, block_begin, block_end, past_len;
   int num_sms;
   cudaStream_t stream;
+};
+
+struct LaunchKCompressPaged {
+  LaunchKCompress base;
+  PoolDev pool;
 };
 
 struct LaunchQKPrep {
@@ -71,6 +102,18 @@ int64_t scores_work_units(int32_t batch, int32_t seq_len, int32_t num_blocks, in
                           int32_t num_rows);
 int64_t scores_no_alloc_max_units();
 
+cudaError_t launch_k_compress_paged(const LaunchKCompressPaged& a);
+
+// Decode path and prefill tail persistence (k_decode.cu)
+cudaError_t launch_raw_k_tail_write_prefill(bool bf16, const void* index_qk, const int32_t* ctx, const PoolDev& pool,
+                                            int32_t batch, int32_t seq_len, cudaStream_t stream);
+cudaError_t launch_pre_decode(bool bf16, void* q_normed, const void* index_qk, const float* cos_sin,
+                              const int32_t* ctx, const void* w_q, const void* w_k, float eps, const PoolDev& pool,
+                              int32_t batch, cudaStream_t stream);
+cudaError_t launch_scores_decode(bool bf16, float* logits, const void* q_normed, const int32_t* ctx,
+                                 const PoolDev& pool, int32_t batch, int32_t max_blocks, float scale,
+                                 cudaStream_t stream);
+
 // Prefill selection (k34_select.cu)
 cudaError_t launch_ids_fill(int32_t* ids, int32_t num_rows, int32_t num_blocks, int num_sms, cudaStream_t stream);
 cudaError_t launch_expand(int32_t* out_idx, const int32_t* sorted_ids, const int32_t* ctx, int32_t seq_len,
@@ -79,6 +122,9 @@ cudaError_t launch_topk_expand(int32_t* out_idx, const float* logits, const int3
                                int32_t num_blocks, int32_t row_start, int32_t num_rows, int num_sms,
                                cudaStream_t stream);
 size_t topk_smem_bytes(int32_t num_blocks);
+cudaError_t launch_topk_expand_decode(int32_t* out_idx, const float* logits, const int32_t* ctx,
+                                      int32_t* split_counters, int32_t num_kv_heads, int32_t batch,
+                                      int32_t max_blocks, cudaStream_t stream);
 
 // Device fault flags: bits set by bounded waits that ran out (k2_scores_tc.cu, k1_stream.cu).
 cudaError_t read_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);

@@ -1,0 +1,192 @@
+"""GPU parity of the paged persistence and decode path ("Qsa Indexer Kernels":
+QsaIndexerPoolState, launchQsaIndexKCompressPaged, launchQsaRawKTailWritePrefill,
+launchQsaIndexerPreDecode, launchQsaIndexScoresDecode, launchQsaTopKExpandDecode).
+
+Bit-exact where the page demands it: the paged K1b's dense output equals the plain
+K1b, pool writes land exactly where the addressing contract puts them, raw K tails
+are bit copies, the decode block compression equals prefill K1b, decode q equals
+prefill q at the same position, and the decode top-k equals the oracle on the same
+logits.  Decode scores are compared with the oracle within the logits tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pool_util
+import workloads
+from tolerance import check_logits, logits_floor
+
+pytestmark = pytest.mark.gpu
+NEG_MAX = np.float32(-np.finfo(np.float32).max)
+
+
+def _qsa():
+    import sparse_attention_indexer_qsa_gb300 as qsa
+    return qsa
+
+
+def _gu():
+    import gpu_util
+    return gpu_util
+
+
+class DevPool:
+    def __init__(self, host_pool):
+        g_ = _gu()
+        self.host = host_pool
+        self.pool = g_.dev(host_pool.pool)
+        self.table = g_.dev(host_pool.page_table)
+        self.state = _qsa().pool_state(self.pool, self.table, host_pool.num_pages, host_pool.num_kv_heads,
+                                       host_pool.pool_head_dim, host_pool.head_size)
+
+    def numpy(self):
+        torch.cuda.synchronize()
+        return self.pool.cpu().numpy().view(np.uint16)
+
+
+def _expected_v_tails(pool0, kbar, ctx, past_len, S, blocks):
+    """Pool after a paged K1b: V-tails of valid blocks with usable slots hold kbar rows."""
+    exp = oracle.Pool(pool0.pool.copy(), pool0.page_table, pool0.num_pages, pool0.num_kv_heads,
+                      pool0.pool_head_dim, pool0.head_size)
+    for b in range(kbar.shape[0]):
+        for g in blocks:
+            if oracle.block_valid(g, int(ctx[b]), S, past_len):
+                tail = pool_util.v_tail(exp, b, g)
+                if tail is not None:
+                    tail[:] = kbar[b, g]
+    return exp.pool
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_paged_compress_and_raw_tails(dtype):
+    qsa, g_ = _qsa(), _gu()
+    B, S = 3, 700
+    wl = workloads.custom(B, S, [700, 513, 3], dtype=dtype, seed=21, nan_padding=True)
+    d = g_.DevWorkload(wl)
+    NB = wl.num_blocks
+    host_pool = pool_util.make_pool(B, S, seed=5, unused_slots=((0, 1, 2), (1, 0, 1), (1, 1, 3)))
+    dp = DevPool(host_pool)
+    plain = g_.k_compress(d, NB, 0, NB, 0)
+    kb = g_.Guarded(B * NB * 128 * 2, init=np.full((B, NB, 128), 0x1234, np.uint16))
+    qsa.qsa_index_k_compress_paged(kb.ptr, d.index_qk, d.cos_sin, d.ctx, d.w_k, wl.eps, dp.state, B, S, NB, 0, NB,
+                                   0, dtype=dtype)
+    dense = kb.numpy(np.uint16, (B, NB, 128))
+    assert np.array_equal(dense, plain), "paged dense output differs from K1b"
+    assert np.array_equal(dp.numpy(), _expected_v_tails(host_pool, plain, wl.context_lengths, 0, S, range(NB)))
+    # raw K tails of the trailing incomplete blocks: a bit copy, nowhere else
+    before = dp.numpy().copy()
+    qsa.qsa_raw_k_tail_write_prefill(d.index_qk, d.ctx, dp.state, B, S, dtype=dtype)
+    ref = oracle.Pool(before.copy(), host_pool.page_table, host_pool.num_pages)
+    oracle.raw_k_tail_write_prefill(wl.index_qk, wl.context_lengths, ref)
+    assert np.array_equal(dp.numpy(), ref.pool)
+    assert not np.array_equal(ref.pool, before)                        # something was written
+    # a sub-range recompress with pastLen writes the same V-tails
+    dp2 = DevPool(pool_util.make_pool(B, S, seed=5, unused_slots=((0, 1, 2), (1, 0, 1), (1, 1, 3))))
+    P = 128
+    sub = d.index_qk[:, P:].contiguous()
+    kb2 = torch.zeros((B, NB, 128), dtype=torch.int16, device="cuda")
+    for bB, bE in workloads.subrange_tiles(9, P, NB):
+        qsa.qsa_index_k_compress_paged(kb2, sub, d.cos_sin, d.ctx, d.w_k, wl.eps, dp2.state, B, S - P, NB, bB, bE,
+                                       P, dtype=dtype)
+    blocks = [g for g in range(NB) if 4 * g >= P]
+    exp = _expected_v_tails(dp2.host, plain, wl.context_lengths, P, S - P, blocks)
+    assert np.array_equal(dp2.numpy(), exp)
+
+
+def test_decode_loop_matches_oracle_and_prefill():
+    """Prefill, then one token per step across nVis = 512 and a 128-token page edge."""
+    qsa, g_ = _qsa(), _gu()
+    dtype = "bf16"
+    B = 3
+    total = [2100, 2060, 300]
+    prefill = [2040, 2046, 250]
+    S = max(total)
+    wl = workloads.custom(B, S, total, dtype=dtype, seed=31, nan_padding=True, max_positions=S)
+    d = g_.DevWorkload(wl)
+    NB = (S + 3) // 4
+    maxb = NB + 3
+    host_pool = pool_util.make_pool(B, S, seed=8)
+    dp = DevPool(host_pool)
+    # prefill: paged K1b + raw tails of each sequence's first `prefill` tokens
+    pctx = g_.dev(np.array(prefill, np.int32))
+    kb = torch.empty((B, NB, 128), dtype=torch.int16, device="cuda")
+    qsa.qsa_index_k_compress_paged(kb, d.index_qk, d.cos_sin, pctx, d.w_k, wl.eps, dp.state, B, S, NB, 0, NB, 0,
+                                   dtype=dtype)
+    qsa.qsa_raw_k_tail_write_prefill(d.index_qk, pctx, dp.state, B, S, dtype=dtype)
+    # reference: the whole sequences through prefill K1a / K1b on the GPU
+    full_q = g_.q_prep(d)
+    full_k = g_.k_compress(d, NB, 0, NB, 0)
+    q = torch.empty((B, 1, 4, 128), dtype=torch.int16, device="cuda")
+    logits = torch.full((B, maxb), float("nan"), dtype=torch.float32, device="cuda")
+    out = torch.empty((B, 2051), dtype=torch.int32, device="cuda")
+    split = torch.full((B, 2), 7, dtype=torch.int32, device="cuda")
+    for step in range(max(t - p for t, p in zip(total, prefill))):
+        pos = [p + step for p in prefill]
+        ctx = np.array([ps + 1 if ps < t else 0 for ps, t in zip(pos, total)], np.int32)
+        rows = np.stack([wl.index_qk[b, min(pos[b], S - 1)] for b in range(B)])
+        d_rows, d_ctx = g_.dev(rows), g_.dev(ctx)
+        qsa.qsa_indexer_pre_decode(q, d_rows, d.cos_sin, d_ctx, d.w_q, d.w_k, wl.eps, dp.state, B, dtype=dtype)
+        logits.fill_(float("nan"))
+        qsa.qsa_index_scores_decode(logits, q, d_ctx, dp.state, B, maxb, dtype=dtype)
+        qsa.qsa_topk_expand_decode(out, logits, d_ctx, split, 2, B, maxb)
+        torch.cuda.synchronize()
+        qh = q.cpu().numpy().view(np.uint16)
+        lg = logits.cpu().numpy()
+        oh = out.cpu().numpy()
+        assert not split.any()
+        split.fill_(7)
+        pool_now = dp.numpy()
+        ref_pool = oracle.Pool(pool_now, host_pool.page_table, host_pool.num_pages)
+        for b in range(B):
+            if ctx[b] <= 0:
+                assert not qh[b].any() and np.all(oh[b] == -1)
+                continue
+            assert np.array_equal(qh[b, 0], full_q[b, pos[b]]), (step, b)   # decode q == prefill q
+        # scores against the oracle on the GPU's q and pool
+        ref = oracle.scores_decode(dtype, qh, ctx, ref_pool, maxb)
+        for b in range(B):
+            nv = int(ctx[b]) // 4
+            assert np.all(np.isnan(lg[b, nv:])), (step, b)                 # only the valid prefix
+            if nv:
+                kb_b = np.stack([pool_util.v_tail(ref_pool, b, g) for g in range(nv)])
+                fl = logits_floor(qh[b, 0][None], kb_b, dtype)
+                ok, st = check_logits(lg[b, :nv][None], ref[b, :nv][None], dtype, fl)
+                assert ok, (step, b, st)
+        # top-k: bit-exact against the oracle on the same logits
+        assert np.array_equal(oh, oracle.topk_expand_decode(lg, ctx)), step
+        # and the prefill selection kernel picks the same blocks for the same logits
+        for b in range(B):
+            if ctx[b] <= 0:
+                continue
+            t = int(ctx[b]) - 1
+            one = torch.full((S * 1, 2051), -5, dtype=torch.int32, device="cuda")
+            row = torch.from_numpy(lg[b:b + 1, :NB].copy()).cuda()
+            row[:, int(ctx[b]) // 4:] = float(NEG_MAX)
+            qsa.qsa_index_topk_expand(one, row, g_.dev(np.array([S], np.int32)), 1, S, NB, t, 1)
+            assert np.array_equal(one[t].cpu().numpy(), oh[b]), (step, b)
+    # every block completed by prefill or decode holds the prefill K1b bits
+    pool_end = oracle.Pool(dp.numpy(), host_pool.page_table, host_pool.num_pages)
+    for b in range(B):
+        for g in range(total[b] // 4):
+            assert np.array_equal(pool_util.v_tail(pool_end, b, g), full_k[b, g]), (b, g)
+        for t in range(total[b] - total[b] % 4, total[b]):
+            assert np.array_equal(pool_util.k_tail(pool_end, b, t), wl.index_qk[b, t, 512:])
+    assert qsa.qsa_device_fault_flags() == 0
+
+
+def test_decode_validation_rejects_bad_pools():
+    qsa = _qsa()
+    P = 0x1000
+    bad = qsa.PoolState(P, P, 4, 8, 2, 384, 300)           # headSize + 128 > poolHeadDim
+    with pytest.raises(qsa.QsaError) as e:
+        qsa.qsa_index_scores_decode(P, P, P, bad, 2, 16, stream=0, dtype="bf16")
+    assert e.value.status == -2
+    odd = qsa.PoolState(P, P, 4, 8, 2, 384, 250)            # tails not 16-byte aligned
+    with pytest.raises(qsa.QsaError) as e:
+        qsa.qsa_indexer_pre_decode(P, P, P, P, P, P, 1e-6, odd, 2, stream=0, dtype="bf16")
+    assert e.value.status == -5
+    null = qsa.PoolState(0, P, 4, 8, 2, 384, 256)
+    with pytest.raises(qsa.QsaError) as e:
+        qsa.qsa_raw_k_tail_write_prefill(P, P, null, 2, 8, stream=0, dtype="bf16")
+    assert e.value.status == -1
