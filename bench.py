@@ -218,6 +218,77 @@ def oracle_sample(wl, budget_s: float = 12.0, seed: int = 0) -> dict:
 
 # ------------------------------------------------------------------ main legs
 
+def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
+    """One decode step for B sequences of length ctx_len over a paged pool
+    (pre-decode, paged scores, top-k + expand), timed with CUDA events per kernel.
+    The pool's V-tails hold N(0,1) bf16 values; every sequence completes a block this
+    step (ctx % 4 == 0), so the pre-decode compresses a block from three K-tails."""
+    import torch
+    sp = stream.cuda_stream
+    pages = (ctx_len + 127) // 128
+    num_pages = B * pages
+    pool = torch.randn((2 * num_pages, 128, 2, 384), device="cuda").to(torch.bfloat16)
+    table = torch.empty((B, 2, pages), dtype=torch.int32, device="cuda")
+    ids = torch.arange(num_pages, dtype=torch.int32, device="cuda").view(B, pages)
+    table[:, 0] = ids
+    table[:, 1] = ids + num_pages
+    state = qsa.pool_state(pool, table, num_pages)
+    rows = torch.randn((B, 1, 640), device="cuda").to(torch.bfloat16)
+    cs = torch.randn((ctx_len, 64), device="cuda")
+    ctx = torch.full((B,), ctx_len, dtype=torch.int32, device="cuda")
+    wq = (torch.randn(128, device="cuda") * 0.1).to(torch.bfloat16)
+    wk = (torch.randn(128, device="cuda") * 0.1).to(torch.bfloat16)
+    q = torch.empty((B, 1, 4, 128), dtype=torch.bfloat16, device="cuda")
+    maxb = (ctx_len + 3) // 4
+    logits = torch.empty((B, maxb), dtype=torch.float32, device="cuda")
+    out = torch.empty((B, 2051), dtype=torch.int32, device="cuda")
+    split = torch.zeros((B, 2), dtype=torch.int32, device="cuda")
+    import ctypes
+    st_ref = ctypes.byref(state)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        rc = lib.qsa_indexer_pre_decode(qsa.QSA_BF16, q.data_ptr(), rows.data_ptr(), cs.data_ptr(), ctx.data_ptr(),
+                                        wq.data_ptr(), wk.data_ptr(), 1e-6, st_ref, B, sp)
+        if ev is not None:
+            ev[1].record(stream)
+        rc |= lib.qsa_index_scores_decode(qsa.QSA_BF16, logits.data_ptr(), q.data_ptr(), ctx.data_ptr(), st_ref, B,
+                                          maxb, sp)
+        if ev is not None:
+            ev[2].record(stream)
+        rc |= lib.qsa_topk_expand_decode(out.data_ptr(), logits.data_ptr(), ctx.data_ptr(), split.data_ptr(), 2, B,
+                                         maxb, sp)
+        if ev is not None:
+            ev[3].record(stream)
+        if rc != 0:
+            raise RuntimeError(qsa.qsa_last_error())
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    n = max(20, K)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    for i in range(n):
+        step(evs[i])
+    torch.cuda.synchronize()
+    ms = {name: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
+          for j, name in enumerate(("pre_decode", "scores_decode", "topk_expand_decode"))}
+    step_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][3]) for i in range(n))
+    nvis = ctx_len // 4
+    alg = {"pre_decode": B * (1280 + 1024 + 3 * 256 + 256 + 2 * 256),
+           "scores_decode": B * (nvis * 256 + 1024 + nvis * 4),
+           "topk_expand_decode": B * (nvis * 4 + 2051 * 4)}
+    hbm_peak, _, _ = load_peaks()
+    kernels = {k: {"ms": ms[k], "alg_bytes": alg[k], "gbs": alg[k] / (ms[k] * 1e-3) / 1e9,
+                   "frac_of_measured_hbm": alg[k] / (ms[k] * 1e-3) / 1e9 / hbm_peak} for k in ms}
+    del pool
+    torch.cuda.empty_cache()
+    return {"workload": f"decode step, B={B} sequences at ctx={ctx_len}, paged pool (128-token pages), bf16",
+            "ms_per_step": step_ms, "tokens_per_s": B / (step_ms * 1e-3), "kernels": kernels,
+            "timed": "CUDA events per kernel over back-to-back steps"}
+
+
 def run_reference(args, rank: int) -> None:
     if rank != 0:
         return
@@ -426,6 +497,7 @@ def run_ours(args, rank: int, world: int) -> None:
             raise RuntimeError(qsa.qsa_last_error())
 
     ms_sel = loop_ms(select_only, max(10, K // 10))
+    decode = None if args.no_decode else decode_leg(qsa, lib, stream, K)
     torch.cuda.synchronize()
     faults = qsa.qsa_device_fault_flags()
 
@@ -490,6 +562,8 @@ def run_ours(args, rank: int, world: int) -> None:
         "clocks": clk.summary(),
         "device_fault_flags": faults,
     }
+    if decode is not None:
+        line["decode"] = decode
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(wl)
     print(json.dumps(line), flush=True)
@@ -503,6 +577,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-decode", action="store_true", help="skip the paged decode-step leg")
     ap.add_argument("--batch", type=int, default=8,
                     help="sequences per step (8 is the scoring workload; smaller for profiler captures)")
     args = ap.parse_args()
