@@ -213,7 +213,7 @@ int qsa_index_expand(int32_t* outIdx, const int32_t* sortedIds, const int32_t* c
  * out[4i + j] = sel[i]*4 + j, the causal tail, -1 to width 2051.
  *  outIdx [out] INT32 [batchSize*seqLen, 2051] (chunk rows written)
  *  logits [in]  FP32 [numRows, numBlocks], chunk-local (qsa_index_scores' output)
- * Limit: numBlocks <= 51200 (a row's keys are staged in shared memory).
+ * Limit: numBlocks <= 65536.
  * Errors: QSA_E_NULL, QSA_E_SHAPE, QSA_E_RANGE, QSA_E_ALIGN, QSA_E_CUDA.
  */
 int qsa_index_topk_expand(int32_t* outIdx, const float* logits, const int32_t* contextLengths,

@@ -273,8 +273,8 @@ QSA_API int qsa_index_topk_expand(int32_t* outIdx, const float* logits, const in
   static const char* fn = "qsa_index_topk_expand";
   int st = validate_selection(fn, outIdx, logits, contextLengths, batchSize, seqLen, numBlocks, rowStart, numRows);
   if (st != QSA_OK) return st;
-  if (qsa::topk_smem_bytes(numBlocks) > 200 * 1024)
-    return fail(QSA_E_SHAPE, "%s: numBlocks=%d too large for a row's keys in shared memory", fn, numBlocks);
+  if (numBlocks > qsa::topk_max_blocks())
+    return fail(QSA_E_SHAPE, "%s: numBlocks=%d above %d", fn, numBlocks, qsa::topk_max_blocks());
   if (numRows == 0) {
     g_last_error[0] = '\0';
     return QSA_OK;
@@ -399,8 +399,8 @@ QSA_API int qsa_topk_expand_decode(int32_t* outIdx, const float* logits, const i
   if (!outIdx || !logits || !contextLengths) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
   if (batchSize < 1 || maxBlocks < 1) return fail(QSA_E_SHAPE, "%s: batchSize=%d maxBlocks=%d must be >= 1", fn, batchSize, maxBlocks);
   if (splitCounters && numKVHeads < 0) return fail(QSA_E_SHAPE, "%s: numKVHeads=%d must be >= 0", fn, numKVHeads);
-  if (qsa::topk_smem_bytes(maxBlocks) > 200 * 1024)
-    return fail(QSA_E_SHAPE, "%s: maxBlocks=%d too large for a row's keys in shared memory", fn, maxBlocks);
+  if (maxBlocks > qsa::topk_max_blocks())
+    return fail(QSA_E_SHAPE, "%s: maxBlocks=%d above %d", fn, maxBlocks, qsa::topk_max_blocks());
   if (!aligned(outIdx, 4) || !aligned(logits, 4) || !aligned(contextLengths, 4) || !aligned(splitCounters, 4))
     return fail(QSA_E_ALIGN, "%s: arrays must be 4-byte aligned", fn);
   DeviceInfo d;

@@ -121,7 +121,7 @@ cudaError_t launch_expand(int32_t* out_idx, const int32_t* sorted_ids, const int
 cudaError_t launch_topk_expand(int32_t* out_idx, const float* logits, const int32_t* ctx, int32_t seq_len,
                                int32_t num_blocks, int32_t row_start, int32_t num_rows, int num_sms,
                                cudaStream_t stream);
-size_t topk_smem_bytes(int32_t num_blocks);
+int32_t topk_max_blocks();  // longest row the selection kernels take
 cudaError_t launch_topk_expand_decode(int32_t* out_idx, const float* logits, const int32_t* ctx,
                                       int32_t* split_counters, int32_t num_kv_heads, int32_t batch,
                                       int32_t max_blocks, cudaStream_t stream);

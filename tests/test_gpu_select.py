@@ -176,3 +176,57 @@ def test_topk_expand_on_scoring_workload():
     assert torch.equal(out >= 0, pos < want[:, None])
     assert bool((out.max(1).values <= t).all())
     assert qsa.qsa_device_fault_flags() == 0
+
+
+def _rows_of(kind, n, NB, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "normal":                       # both signs: no common leading key bits
+        v = rng.standard_normal((n, NB)).astype(np.float32)
+        v[:, ::97] = -0.0
+        v[:, 1::89] = 0.0
+    elif kind == "equal":                      # every key identical
+        v = np.full((n, NB), 1.5, np.float32)
+    elif kind == "narrow":                     # keys sharing most leading bits
+        v = (1.0 + rng.integers(0, 64, (n, NB)) * np.float32(2.0 ** -20)).astype(np.float32)
+    else:
+        v = rng.gamma(2.0, 1.0, (n, NB)).astype(np.float32)
+    return v
+
+
+@pytest.mark.parametrize("NB", [3001, 4096, 6000, 8192, 12007, 16384, 20000, 65536])
+@pytest.mark.parametrize("kind", ["gamma", "normal", "equal", "narrow"])
+def test_topk_expand_long_rows(NB, kind):
+    """Rows up to the 65536-block limit: every mask width (4096 blocks per 32-bit word a
+    thread), rows not 16-byte aligned, ragged nVis, keys of both signs, all-equal and
+    narrow ranges (the threshold bin holding more candidates than its list)."""
+    qsa, g_ = _qsa(), _gu()
+    S = 4 * NB
+    out = torch.full((S, W), SENT, dtype=torch.int32, device="cuda")
+    d_ctx = g_.dev(np.array([S], np.int32))
+    ts = sorted({min(x, S - 3) for x in (4 * 513 - 1, 4 * 4096 - 2, 4 * min(NB, 8192) + 1, 4 * NB - 1, S - 3,
+                                         4 * (NB // 3) + 2)})
+    for j, start in enumerate(ts):
+        n = 3
+        lg = _rows_of(kind, n, NB, seed=NB + j)
+        for i in range(n):                                         # the K2 mask beyond nVis
+            lg[i, min(NB, (start + i + 1) // 4):] = NEG_MAX
+        qsa.qsa_index_topk_expand(out, g_.dev(lg), d_ctx, 1, S, NB, start, n)
+        got = out[start:start + n].cpu().numpy()
+        ref = np.stack([oracle.select_expand_row(lg[i], start + i, S) for i in range(n)])
+        assert_same_selection(got, ref)
+    assert qsa.qsa_device_fault_flags() == 0
+
+
+@pytest.mark.parametrize("maxb", [700, 4100, 9000, 17000])
+def test_topk_expand_decode_long_rows(maxb):
+    """Decode top-k over long rows is bit-exact against the oracle (ascending emission)."""
+    qsa, g_ = _qsa(), _gu()
+    B = 5
+    ctx = np.array([4 * maxb, 4 * maxb - 1, 2051, 0, 4 * (maxb // 2) + 3], np.int32)
+    lg = _rows_of("normal", B, maxb, seed=maxb)
+    lg[1, ::3] = lg[1, 5]                                           # heavy ties in one row
+    out = g_.Guarded(B * W * 4, init=np.full((B, W), SENT, np.int32))
+    split = torch.full((B, 3), 9, dtype=torch.int32, device="cuda")
+    qsa.qsa_topk_expand_decode(out.ptr, g_.dev(lg), g_.dev(ctx), split, 3, B, maxb)
+    assert np.array_equal(out.numpy(np.int32, (B, W)), oracle.topk_expand_decode(lg, ctx))
+    assert not split.any()
