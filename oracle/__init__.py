@@ -55,7 +55,10 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        # QSA_ORACLE_LIBRARY: a build of a deliberately altered qsa_oracle.c, loaded
+        # instead of the real one by tests/test_oracle_mutants.py to show that the pins
+        # catch each alteration
+        lib = ctypes.CDLL(os.environ.get("QSA_ORACLE_LIBRARY") or build())
         p = ctypes.c_void_p
         i32 = ctypes.c_int32
         f32 = ctypes.c_float

@@ -355,6 +355,28 @@ def test_k_compress_reads_rows_4g_plus_j_minus_pastlen(P):
         assert np.array_equal(to_f64(kb[0, g], dtype), to_f64(exp, dtype)), g
 
 
+def test_k_compress_sums_rows_4g_to_4g_plus_3_in_that_order():
+    # dim 0 of the block's four rows holds an order-sensitive golden case, every other
+    # dim is 1.0 in all rows (mean exactly 1); eps = 0, w = 0, position 0 (rope is the
+    # identity there).  The output must equal the norm of [golden mean, 1, 1, ...]: a K
+    # compress that read the rows in another order, or summed them in another order,
+    # would normalise a different first element.
+    with open(os.path.join(GOLDEN, "block_mean_order.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        dtype = c["dtype"]
+        iq = np.zeros((1, 4, 640), np.uint16)
+        iq[0, :, 512:] = t_bits([1.0], dtype)[0]
+        iq[0, :, 512] = t_bits(c["k"], dtype)
+        cs = workloads.cos_sin_table(4)
+        kb = oracle.k_compress(dtype, iq, cs, [4], np.zeros(128, np.uint16), 0.0, 1, 0, 1, 0)
+        x = np.ones(128)
+        x[0] = c["mean"]
+        assert np.array_equal(kb[0, 0], oracle.norm_rope(dtype, x, np.zeros(128, np.uint16), 0.0, cs[0])), c
+        ok, st = check_t(kb[0, 0], ref_norm_rope64(x, np.zeros(128, np.uint16), 0.0, cs[0], dtype), dtype)
+        assert ok, (c, st)
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_k_compress_subrange_equals_full(dtype):
     wl = workloads.custom(3, 96, [96, 50, 7], dtype=dtype, seed=9)
