@@ -289,6 +289,31 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
             "timed": "CUDA events per kernel over back-to-back steps"}
 
 
+# ----------------------------------------------------------------- ranks (N > 1)
+
+def rank_barrier(world: int) -> None:
+    """All ranks meet (gloo; no data-path collective exists: rows are independent)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks_of(x: float, world: int) -> float:
+    """The slowest rank's time: whole-job time of N replicas run side by side."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rows_per_s(rows_per_rank: int, ms_max: float, world: int) -> float:
+    """Weak scaling: every rank processed its own rows_per_rank in at most ms_max."""
+    return world * rows_per_rank / (ms_max * 1e-3)
+
+
 def run_reference(args, rank: int) -> None:
     if rank != 0:
         return
@@ -382,17 +407,10 @@ def run_ours(args, rank: int, world: int) -> None:
         return e0.elapsed_time(e1) / n
 
     def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
+        rank_barrier(world)
 
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks_of(x, world)
 
     for _ in range(args.warmup):
         step()
@@ -535,7 +553,7 @@ def run_ours(args, rank: int, world: int) -> None:
     k2_gbs = kernels["k2"]["gbs"]
     line = {
         "metric": METRIC,
-        "value": world * rows / (ms_step * 1e-3),
+        "value": whole_job_rows_per_s(rows, ms_step, world),
         "unit": UNIT,
         "n_gpus": world,
         "steps": K,
@@ -554,7 +572,7 @@ def run_ours(args, rank: int, world: int) -> None:
                      "unit": "GB/s", "frac": k2_gbs / hbm_peak, "traffic": traffic,
                      "peak_source": f"{peak_src} hbm_gbs"},
         "kernels": kernels,
-        "e2e": {"value": world * rows / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_rows_per_s(rows, ms_e2e, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": K_e2e,
                 "how": "Python API, pinned host buffers; copies overlap compute across streams; "
                        "K2 in per-sequence row chunks"},

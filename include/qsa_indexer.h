@@ -142,6 +142,12 @@ int qsa_index_k_compress(qsa_dtype_t dtype, void* kbar, const void* indexQk,
  *   for g < (t+1)/4 (block fully before or at t), else -FLT_MAX.
  * Padded rows are -FLT_MAX everywhere and their q rows are ignored.
  *
+ * Work is handed out by a device-side counter pair; calls take turns through 64
+ * such pairs per device and each launch resets its pair when it ends, so at most
+ * 64 launches may be in flight on one device at a time.  A CUDA graph that
+ * captured a launch keeps that launch's pair on every replay (replays of one
+ * graph must not overlap each other).
+ *
  * Errors: QSA_E_NULL, QSA_E_DTYPE, QSA_E_SHAPE (batchSize < 1, seqLen < 1,
  *         numBlocks < ceilDiv(seqLen, 4)), QSA_E_RANGE (row range), QSA_E_ALIGN,
  *         QSA_E_CUDA, QSA_E_DEVICE.
