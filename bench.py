@@ -168,50 +168,77 @@ def k2_profiled_traffic(batch: int):
 
 # ------------------------------------------------------------------ oracle leg
 
-def oracle_sample(wl, budget_s: float = 12.0, seed: int = 0) -> dict:
-    """Time the CPU oracle (single thread, as it stands) on a bounded sample of the
+def oracle_sample(wl, budget_s: float = 12.0, seed: int = 0, threads: int | None = None) -> dict:
+    """Time the CPU oracle (as it stands; its calls release the GIL, so `threads`
+    host threads run it side by side on disjoint rows) on a bounded sample of the
     workload and extrapolate to one full step: K1a on whole rows, K1b on whole
     blocks, K2 on rows spread evenly over every position t (its cost grows with t)."""
+    import concurrent.futures as cf
     import oracle
     B, S, NB = wl.B, wl.S, wl.num_blocks
     dtype = wl.dtype
-    # K1a: a contiguous slab of rows
-    n1 = min(S, 4096)
+    if threads is None:
+        threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    threads = max(1, int(threads))
+    pool = cf.ThreadPoolExecutor(max_workers=threads)
+    # K1a: a slab of rows of sequence 0, one contiguous share a thread
+    n1 = min(S, 512 * threads)
+    cuts = np.linspace(0, n1, threads + 1).astype(int)
+
+    def k1a_part(i):
+        lo, hi = int(cuts[i]), int(cuts[i + 1])
+        ctx = np.array([hi - lo], np.int32)
+        oracle.q_prep(dtype, wl.index_qk[:1, lo:hi], wl.cos_sin[lo:], ctx, wl.w_q, wl.eps)
+
     t0 = time.perf_counter()
-    oracle.q_prep(dtype, wl.index_qk[:1, :n1], wl.cos_sin, np.array([n1], np.int32), wl.w_q, wl.eps)
+    list(pool.map(k1a_part, range(threads)))
     k1a_per_row = (time.perf_counter() - t0) / n1
-    # K1b: the blocks of that slab
-    nb1 = n1 // 4
+    # K1b: the blocks of that slab, one contiguous share a thread
+    bcuts = (cuts // 4) * 4
+
+    def k1b_part(i):
+        lo, hi = int(bcuts[i]), int(bcuts[i + 1])
+        nb = (hi - lo) // 4
+        if nb:
+            oracle.k_compress(dtype, wl.index_qk[:1, lo:hi], wl.cos_sin[lo:], np.array([hi - lo], np.int32),
+                              wl.w_k, wl.eps, nb, 0, nb, 0)
+
     t0 = time.perf_counter()
-    oracle.k_compress(dtype, wl.index_qk[:1, :n1], wl.cos_sin, np.array([n1], np.int32), wl.w_k, wl.eps,
-                      nb1, 0, nb1, 0)
-    k1b_per_block = (time.perf_counter() - t0) / nb1
-    # K2: rows at evenly spaced positions, on oracle-made qNormed/kbar of sequence 0
+    list(pool.map(k1b_part, range(threads)))
+    k1b_per_block = (time.perf_counter() - t0) / max(1, n1 // 4)
+    # K2: rows at random positions of sequence 0 (oracle-made qNormed/kbar), each
+    # thread takes every threads-th position of one permutation until the budget
     q0 = oracle.q_prep(dtype, wl.index_qk[:1], wl.cos_sin, wl.context_lengths[:1], wl.w_q, wl.eps)[0]
     kb0 = oracle.k_compress(dtype, wl.index_qk[:1], wl.cos_sin, wl.context_lengths[:1], wl.w_k, wl.eps,
                             NB, 0, NB, 0)[0]
     ctx0 = int(wl.context_lengths[0])
-    rows_done, k2_time = 0, 0.0
-    stride_order = np.random.default_rng(seed).permutation(S)
+    order = np.random.default_rng(seed).permutation(S)
     t_start = time.perf_counter()
-    for t in stride_order:
-        a = time.perf_counter()
-        oracle.scores_row(dtype, q0[t], kb0, int(t), ctx0)
-        k2_time += time.perf_counter() - a
-        rows_done += 1
-        if time.perf_counter() - t_start > budget_s and rows_done >= 64:
-            break
-    k2_per_row = k2_time / rows_done
+
+    def k2_part(i):
+        done = 0
+        for t in order[i::threads]:
+            oracle.scores_row(dtype, q0[t], kb0, int(t), ctx0)
+            done += 1
+            if time.perf_counter() - t_start > budget_s and done >= 8:
+                break
+        return done
+
+    rows_done = sum(pool.map(k2_part, range(threads)))
+    k2_wall = time.perf_counter() - t_start
+    pool.shutdown()
+    # the sampled positions are uniform over t, so their mean cost is the step's mean row cost
+    k2_per_row = k2_wall / rows_done
     rows = B * S
     step_s = k1a_per_row * rows + k1b_per_block * B * NB + k2_per_row * rows
     return {
         "value": rows / step_s,
         "unit": UNIT,
-        "cores": 1,
+        "cores": threads,
         "kind": "oracle",
-        "sample": (f"K1a on {n1} rows, K1b on {nb1} blocks, K2 on {rows_done} rows at random positions "
-                   f"of sequence 0 (S={S}); per-row/per-block times scaled to one full step of "
-                   f"{rows} rows and {B * NB} blocks"),
+        "sample": (f"{threads} host threads on disjoint rows: K1a on {n1} rows, K1b on {n1 // 4} blocks, K2 on "
+                   f"{rows_done} rows at random positions of sequence 0 (S={S}); wall time per row/block "
+                   f"scaled to one full step of {rows} rows and {B * NB} blocks"),
         "est_step_s": step_s,
     }
 
@@ -289,6 +316,144 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
             "timed": "CUDA events per kernel over back-to-back steps"}
 
 
+def _graph_ms(torch, launches, reps: int = 10) -> float:
+    """Median over `reps` replays of a CUDA graph holding `launches` (callables taking a
+    stream handle), divided by the number of launches: per-launch device time."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for f in launches[:2]:                # first-call set-up outside the capture
+            if f(s.cuda_stream) != 0:
+                raise RuntimeError("launch failed before capture")
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for f in launches:
+                if f(s.cuda_stream) != 0:
+                    raise RuntimeError("launch failed during capture")
+    torch.cuda.current_stream().wait_stream(s)
+    times = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(reps):
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return statistics.median(times) / len(launches)
+
+
+def _k1_launchers(qsa, lib, dt, bufs, ctx, cs, wq, wk, eps, B, S, NB):
+    """(K1a, K1b, fused K1) launchers over buffer set i: (iq, qn, kb) views."""
+    def k1a(i):
+        iq, qn, _ = bufs(i)
+        return lambda st: lib.qsa_index_q_prep(dt, qn, iq, cs, ctx, wq, eps, B, S, st)
+
+    def k1b(i):
+        iq, _, kb = bufs(i)
+        return lambda st: lib.qsa_index_k_compress(dt, kb, iq, cs, ctx, wk, eps, B, S, NB, 0, NB, 0, st)
+
+    def fused(i):
+        iq, qn, kb = bufs(i)
+        return lambda st: lib.qsa_index_qk_prep(dt, qn, kb, iq, cs, ctx, wq, wk, eps, B, S, NB, st)
+    return {"k1a": k1a, "k1b": k1b, "k1_fused": fused}
+
+
+def k1_configs_leg(qsa, lib, hbm_peak: float, names=None, sweep: bool = True) -> dict:
+    """K1a, K1b and the fused K1 on the small configurations (tiny, batched bf16/fp16,
+    long, decode-parity full compress) and a size sweep of B*S from 2^16 to 2^22 rows.
+    Small configs fit in L2, so each timed launch uses its own copy of the inputs and
+    outputs, cycling through enough copies to exceed twice the L2 size; the launches run
+    back to back from a CUDA graph, median of 10 replays."""
+    import torch
+    import workloads
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+
+    def measure(B, S, NB, dtype, ctx_np, make_sets, cs, wq, wk, eps, per_set_bytes):
+        n_sets = max(4, -(-2 * l2 // per_set_bytes))
+        bufs = make_sets(n_sets)
+        ctx = torch.from_numpy(np.ascontiguousarray(ctx_np, np.int32)).cuda()
+        dt = qsa.QSA_BF16 if dtype == "bf16" else qsa.QSA_F16
+        L = _k1_launchers(qsa, lib, dt, bufs, ctx.data_ptr(), cs.data_ptr(), wq.data_ptr(), wk.data_ptr(), eps,
+                          B, S, NB)
+        ab = algorithmic_bytes(ctx_np, B, S, NB)
+        ab["k1_fused"] = ab["k1a"] + ab["k1b"]
+        out = {"sets": n_sets, "bytes_per_set": per_set_bytes}
+        for name, mk in L.items():
+            ms = _graph_ms(torch, [mk(i) for i in range(n_sets)])
+            gbs = ab[name] / (ms * 1e-3) / 1e9
+            out[name] = {"us": ms * 1e3, "alg_bytes": ab[name], "gbs": gbs, "frac_of_measured_hbm": gbs / hbm_peak}
+        return out
+
+    def host_sets(wl):
+        B, S, NB = wl.B, wl.S, wl.num_blocks
+        per = B * S * 1280 + B * S * 1024 + B * NB * 256
+
+        def make(n):
+            iq0 = torch.from_numpy(np.ascontiguousarray(wl.index_qk).view(np.int16)).cuda()
+            iq = iq0.unsqueeze(0).repeat(n, 1, 1, 1).contiguous()
+            qn = torch.empty((n, B, S, 512), dtype=torch.int16, device="cuda")
+            kb = torch.empty((n, B, NB, 128), dtype=torch.int16, device="cuda")
+            return lambda i: (iq[i].data_ptr(), qn[i].data_ptr(), kb[i].data_ptr())
+        return make, per
+
+    res = {"configs": {}, "sweep": []}
+    cfgs = {"tiny": lambda: workloads.tiny(), "batched_bf16": lambda: workloads.batched("bf16"),
+            "batched_fp16": lambda: workloads.batched("fp16"), "long": lambda: workloads.long_prefill(),
+            "decode_parity_full_compress": lambda: workloads.decode_parity()}
+    for name, make_wl in cfgs.items():
+        if names is not None and name not in names:
+            continue
+        wl = make_wl()
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
+                                         else np.ascontiguousarray(a)).cuda()
+        make, per = host_sets(wl)
+        r = measure(wl.B, wl.S, wl.num_blocks, wl.dtype, wl.context_lengths, make, dev(wl.cos_sin),
+                    dev(wl.w_q), dev(wl.w_k), wl.eps, per)
+        r["shape"] = {"B": wl.B, "S": wl.S, "num_blocks": wl.num_blocks, "dtype": wl.dtype}
+        res["configs"][name] = r
+        torch.cuda.empty_cache()
+    if not sweep:
+        return res
+    # sweep: S = 16384, ctx = S, B = 4 .. 256; inputs drawn on the device (seeded), bf16
+    S = 16384
+    NB = S // 4
+    cs = torch.from_numpy(workloads.cos_sin_table(S)).cuda()
+    rng = np.random.default_rng(5)
+    wq = torch.from_numpy(workloads.gamma(rng, "bf16").view(np.int16)).cuda()
+    wk = torch.from_numpy(workloads.gamma(rng, "bf16").view(np.int16)).cuda()
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    for B in (4, 8, 16, 32, 64, 128, 256):
+        per = B * S * (1280 + 1024) + B * NB * 256
+
+        def make(n, B=B):
+            iq = torch.randn((n, B, S, 640), generator=gen, device="cuda").to(torch.bfloat16).view(torch.int16)
+            qn = torch.empty((n, B, S, 512), dtype=torch.int16, device="cuda")
+            kb = torch.empty((n, B, NB, 128), dtype=torch.int16, device="cuda")
+            return lambda i: (iq[i].data_ptr(), qn[i].data_ptr(), kb[i].data_ptr())
+        n_sets = 1 if per > 2 * l2 else 2
+        bufs = make(n_sets)
+        ctx_np = np.full(B, S, np.int32)
+        ctx = torch.from_numpy(ctx_np).cuda()
+        L = _k1_launchers(qsa, lib, qsa.QSA_BF16, bufs, ctx.data_ptr(), cs.data_ptr(), wq.data_ptr(),
+                          wk.data_ptr(), 1e-6, B, S, NB)
+        ab = algorithmic_bytes(ctx_np, B, S, NB)
+        ab["k1_fused"] = ab["k1a"] + ab["k1b"]
+        row = {"rows": B * S, "B": B, "S": S, "sets": n_sets}
+        for name, mk in L.items():
+            ms = _graph_ms(torch, [mk(i) for i in range(n_sets)] * 2)
+            row[name + "_gbs"] = ab[name] / (ms * 1e-3) / 1e9
+            row[name + "_us"] = ms * 1e3
+        res["sweep"].append(row)
+        del bufs, L
+        torch.cuda.empty_cache()
+    res["how"] = ("per-launch device time from a CUDA graph of back-to-back launches (median of 10 replays); "
+                  "small configs cycle through copies of inputs and outputs totalling more than 2x L2; the "
+                  "sweep's inputs are drawn on the device (torch generator, seed 5), S=16384, ctx=S, bf16")
+    res["l2_bytes"] = l2
+    return res
+
+
 # ----------------------------------------------------------------- ranks (N > 1)
 
 def rank_barrier(world: int) -> None:
@@ -336,7 +501,8 @@ def run_reference(args, rank: int) -> None:
         "ms_per_step": 1000.0 * wl.B * wl.S / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD.format(B=wl.B), "B": wl.B, "S": wl.S, "num_blocks": wl.num_blocks},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": res["sample"]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": res["cores"], "kind": "oracle",
+                         "sample": res["sample"]},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -516,6 +682,7 @@ def run_ours(args, rank: int, world: int) -> None:
 
     ms_sel = loop_ms(select_only, max(10, K // 10))
     decode = None if args.no_decode else decode_leg(qsa, lib, stream, K)
+    k1_small = None if args.no_sweep or rank != 0 else k1_configs_leg(qsa, lib, load_peaks()[0])
     torch.cuda.synchronize()
     faults = qsa.qsa_device_fault_flags()
 
@@ -582,6 +749,8 @@ def run_ours(args, rank: int, world: int) -> None:
     }
     if decode is not None:
         line["decode"] = decode
+    if k1_small is not None:
+        line["k1_small_configs"] = k1_small
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(wl)
     print(json.dumps(line), flush=True)
@@ -596,6 +765,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-decode", action="store_true", help="skip the paged decode-step leg")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip K1 on the small configurations and the B*S size sweep")
+    ap.add_argument("--only-k1-configs", nargs="?", const="all", default=None, metavar="NAMES",
+                    help="run only K1 on the small configurations and the size sweep, or on the named "
+                         "configurations (comma-separated) without the sweep; for profiler captures")
     ap.add_argument("--batch", type=int, default=8,
                     help="sequences per step (8 is the scoring workload; smaller for profiler captures)")
     args = ap.parse_args()
@@ -607,6 +781,14 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank)
+        elif args.only_k1_configs:
+            if rank == 0:
+                import torch
+                import sparse_attention_indexer_qsa_gb300 as qsa
+                torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+                names = None if args.only_k1_configs == "all" else args.only_k1_configs.split(",")
+                leg = k1_configs_leg(qsa, qsa.load(), load_peaks()[0], names=names, sweep=names is None)
+                print(json.dumps({"k1_small_configs": leg}), flush=True)
         else:
             run_ours(args, rank, world)
     finally:
