@@ -567,6 +567,9 @@ topk_kernel(int32_t* __restrict__ out_idx, const float* __restrict__ logits, con
 #ifndef QSA_SEL_THREADS
 #define QSA_SEL_THREADS 64
 #endif
+#ifndef QSA_SEL_DECODE_THREADS
+#define QSA_SEL_DECODE_THREADS 128
+#endif
 
 template <int T, bool DECODE>
 cudaError_t launch_plain(int32_t* out_idx, const float* logits, const int32_t* ctx, int32_t seq_len,
@@ -619,8 +622,8 @@ cudaError_t launch_topk_expand(int32_t* out_idx, const float* logits, const int3
 cudaError_t launch_topk_expand_decode(int32_t* out_idx, const float* logits, const int32_t* ctx,
                                       int32_t* split_counters, int32_t num_kv_heads, int32_t batch,
                                       int32_t max_blocks, cudaStream_t stream) {
-  return sel::launch_plain<128, true>(out_idx, logits, ctx, 1, max_blocks, 0, batch, split_counters, num_kv_heads,
-                                     stream);
+  return sel::launch_plain<QSA_SEL_DECODE_THREADS, true>(out_idx, logits, ctx, 1, max_blocks, 0, batch,
+                                                        split_counters, num_kv_heads, stream);
 }
 
 }  // namespace qsa

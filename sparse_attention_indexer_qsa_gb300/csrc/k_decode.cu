@@ -11,8 +11,12 @@
 //                K-tails of 4g..4g+2 plus the new row (K1b numerics: the same device
 //                routines as the prefill kernels, so the kbar is bit-identical to
 //                prefill K1b) and written to the V-tail of 4g.
-//   scores_decode  K2 numerics at S = 1 over the V-tails: logits[b][g] for
+//   scores_decode  K2's scoring at S = 1 over the V-tails: logits[b][g] for
 //                g < ctx/4 only; a block whose page slot is unusable scores -FLT_MAX.
+//                FP32 dot products in another order than K2's (eight-term partial
+//                dots per lane, then a lane tree), so equal to K2 within the logits
+//                tolerance, not bit for bit; relu, the ascending head sum and the
+//                scale as in K2.
 #include <cfloat>
 
 #include "qsa_common.cuh"
@@ -120,50 +124,78 @@ __global__ void __launch_bounds__(64) pre_decode_kernel(uint16_t* __restrict__ q
   }
 }
 
-// grid (B, ceilDiv(maxBlocks, 256)), one thread per block column
+// grid (B, ceilDiv(maxBlocks, kDecBlocksPerCta)), kDecThreads threads.  A 16-lane
+// half-warp scores one block at a time: lane c holds dims [8c, 8c+8) of the 4 q heads
+// in registers, reads the matching 16 bytes of the block's V-tail (the half-warp reads
+// the 256-byte row in one coalesced access), forms 4 partial dots, and the half-warp
+// reduces them (a reduce-scatter over lane bits 3 and 2, then bits 1 and 0), so that
+// lanes 0/4/8/12 hold heads 0/1/2/3; lane 0 sums relu of the heads in ascending order.
+constexpr int kDecThreads = 256;
+constexpr int kDecUnroll = 4;                                       // blocks in flight a half-warp
+constexpr int kDecBlocksPerCta = (kDecThreads / 16) * kDecUnroll * 2;  // two rounds
+
 template <class T>
-__global__ void __launch_bounds__(256) scores_decode_kernel(float* __restrict__ logits,
-                                                            const uint16_t* __restrict__ q_normed,
-                                                            const int32_t* __restrict__ ctx, const PoolDev pool,
-                                                            int32_t max_blocks, float scale) {
-  __shared__ float qs[kNumQHeads * kHeadDim];
+__global__ void __launch_bounds__(kDecThreads) scores_decode_kernel(float* __restrict__ logits,
+                                                                    const uint16_t* __restrict__ q_normed,
+                                                                    const int32_t* __restrict__ ctx,
+                                                                    const PoolDev pool, int32_t max_blocks,
+                                                                    float scale) {
   const int32_t b = blockIdx.x;
   const int32_t c = __ldg(ctx + b);
   const int32_t n_vis = c > 0 ? min(c / kRatio, max_blocks) : 0;
-  const int32_t g0 = blockIdx.y * blockDim.x;
-  if (g0 >= n_vis) return;  // only the valid prefix is written
-  const uint16_t* q = q_normed + static_cast<int64_t>(b) * (kNumQHeads * kHeadDim);
-  for (int i = threadIdx.x; i < kNumQHeads * kHeadDim / 2; i += blockDim.x) {
-    const uint32_t w = reinterpret_cast<const uint32_t*>(q)[i];
-    qs[2 * i] = T::lo(w);
-    qs[2 * i + 1] = T::hi(w);
-  }
-  __syncthreads();
-  const int32_t g = g0 + threadIdx.x;
-  if (g >= n_vis) return;
-  float* out = logits + static_cast<int64_t>(b) * max_blocks + g;
-  const uint16_t* k = pool_tail(pool, b, 1, kRatio * g);
-  if (k == nullptr) {
-    *out = -FLT_MAX;
-    return;
-  }
-  float kf[kHeadDim];
+  const int32_t g_begin = blockIdx.y * kDecBlocksPerCta;
+  if (g_begin >= n_vis) return;  // only the valid prefix is written
+  const int32_t g_end = min(g_begin + kDecBlocksPerCta, n_vis);
+  const int lane = threadIdx.x & 31, ch = lane & 15, hw = threadIdx.x >> 4;
+  const unsigned half = lane & 16;
+  float qf[kNumQHeads][8];
+  const uint16_t* q = q_normed + static_cast<int64_t>(b) * (kNumQHeads * kHeadDim) + 8 * ch;
 #pragma unroll
-  for (int ch = 0; ch < kHeadDim / 8; ++ch) {
-    float f[8];
-    unpack8<T>(ld_cached_v4(k + 8 * ch), f);
+  for (int h = 0; h < kNumQHeads; ++h) unpack8<T>(ld_cached_v4(q + h * kHeadDim), qf[h]);
+  float* out = logits + static_cast<int64_t>(b) * max_blocks;
+  const bool keep_hi = (ch & 8) != 0, keep_odd = (ch & 4) != 0;
+#pragma unroll 1
+  for (int32_t base = g_begin; base < g_end; base += 16 * kDecUnroll) {  // warp-uniform: shuffles below
+    const int32_t g0 = base + hw;
+    uint4 raw[kDecUnroll];
+    bool ok[kDecUnroll];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) kf[8 * ch + e] = f[e];
+    for (int u = 0; u < kDecUnroll; ++u) {
+      const int32_t g = g0 + 16 * u;
+      const uint16_t* k = g < g_end ? pool_tail(pool, b, 1, kRatio * g) : nullptr;
+      ok[u] = k != nullptr;
+      raw[u] = ok[u] ? ld_stream_v4(k + 8 * ch) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kDecUnroll; ++u) {
+      float kf[8];
+      unpack8<T>(raw[u], kf);
+      float d[kNumQHeads];
+#pragma unroll
+      for (int h = 0; h < kNumQHeads; ++h) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
+        d[h] = acc;
+      }
+      // lane bit 3: keep heads {2,3} or {0,1}; send the other pair to the partner
+      const float s0 = keep_hi ? d[0] : d[2], s1 = keep_hi ? d[1] : d[3];
+      const float r0 = __shfl_xor_sync(0xffffffffu, s0, 8), r1 = __shfl_xor_sync(0xffffffffu, s1, 8);
+      const float e0 = (keep_hi ? d[2] : d[0]) + r0, e1 = (keep_hi ? d[3] : d[1]) + r1;
+      // lane bit 2: keep the pair's second or first head
+      const float r2 = __shfl_xor_sync(0xffffffffu, keep_odd ? e0 : e1, 4);
+      float f = (keep_odd ? e1 : e0) + r2;
+      f += __shfl_xor_sync(0xffffffffu, f, 2);
+      f += __shfl_xor_sync(0xffffffffu, f, 1);
+      const float rel = fmaxf(0.0f, f);  // head ((ch >> 3) & 1) * 2 + ((ch >> 2) & 1)
+      const float h1 = __shfl_sync(0xffffffffu, rel, half | 4);
+      const float h2 = __shfl_sync(0xffffffffu, rel, half | 8);
+      const float h3 = __shfl_sync(0xffffffffu, rel, half | 12);
+      const int32_t g = g0 + 16 * u;
+      if (ch == 0 && g < g_end) out[g] = ok[u] ? __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(rel, h1), h2), h3), scale)
+                                              : -FLT_MAX;
+    }
   }
-  float sum = 0.0f;
-#pragma unroll
-  for (int hh = 0; hh < kNumQHeads; ++hh) {
-    float dot = 0.0f;
-#pragma unroll
-    for (int d = 0; d < kHeadDim; ++d) dot = fmaf(qs[hh * kHeadDim + d], kf[d], dot);
-    sum = __fadd_rn(sum, fmaxf(0.0f, dot));
-  }
-  *out = __fmul_rn(sum, scale);
 }
 
 }  // namespace dec
@@ -191,10 +223,13 @@ cudaError_t launch_pre_decode(bool bf16, void* q_normed, const void* index_qk, c
 cudaError_t launch_scores_decode(bool bf16, float* logits, const void* q_normed, const int32_t* ctx,
                                  const PoolDev& pool, int32_t batch, int32_t max_blocks, float scale,
                                  cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>(batch), static_cast<unsigned>((max_blocks + 255) / 256));
+  const dim3 grid(static_cast<unsigned>(batch),
+                  static_cast<unsigned>((max_blocks + dec::kDecBlocksPerCta - 1) / dec::kDecBlocksPerCta));
   auto* q = static_cast<const uint16_t*>(q_normed);
-  if (bf16) dec::scores_decode_kernel<Bf16><<<grid, 256, 0, stream>>>(logits, q, ctx, pool, max_blocks, scale);
-  else dec::scores_decode_kernel<F16><<<grid, 256, 0, stream>>>(logits, q, ctx, pool, max_blocks, scale);
+  if (bf16)
+    dec::scores_decode_kernel<Bf16><<<grid, dec::kDecThreads, 0, stream>>>(logits, q, ctx, pool, max_blocks, scale);
+  else
+    dec::scores_decode_kernel<F16><<<grid, dec::kDecThreads, 0, stream>>>(logits, q, ctx, pool, max_blocks, scale);
   return cudaGetLastError();
 }
 
