@@ -30,10 +30,17 @@ __device__ uint32_t g_k1_fault_flags;
 namespace k1s {
 
 constexpr int kModeQK = 3;  // the one mode built: q heads and compressed k together
-constexpr int kRows = 32;                 // token rows per unit (one CTA)
+#ifndef QSA_K1S_ROWS
+#define QSA_K1S_ROWS 32
+#endif
+#ifndef QSA_K1S_CTAS
+#define QSA_K1S_CTAS 4
+#endif
+constexpr int kRows = QSA_K1S_ROWS;       // token rows per unit (one CTA)
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kCtasPerSm = 4;
+constexpr int kCtasPerSm = QSA_K1S_CTAS;
+static_assert(kRows % (kRatio * 2) == 0 && kRows / kRatio <= 2 * 4, "blocks of a unit: two 8-lane groups a warp");
 constexpr uint32_t kCsBytes = kCsWidth * 4;  // 256-byte cos/sin row
 
 template <int MODE>
@@ -163,10 +170,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k1_stream_kernel(const P
       st_v4(dst + cb, ob);
     }
     if (MODE == kModeQK) {
-      // K1b: the 8-lane group h of warp w owns block jb = 2*w + h (h < 2) of the unit
+      // K1b: the 8-lane group h of warp w owns block jb = 2*w + h (h < 2, jb < kRows/4) of the unit
       const int jb = 2 * warp + (h & 1);
       const int32_t g = t0 / kRatio + jb;
-      const bool mine = h < 2;
+      const bool mine = h < 2 && jb < kRows / kRatio;
       const bool exists = mine && kRatio * g < p.seq_len;        // g < ceilDiv(S, 4)
       const bool valid = exists && kRatio * jb + (kRatio - 1) < nq;  // its four rows were copied
       float a[8], bv[8];
