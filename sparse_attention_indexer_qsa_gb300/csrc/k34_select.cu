@@ -25,9 +25,10 @@ constexpr int kTopK = 512;
 constexpr int kRatio = 4;
 constexpr int kWidth = kTopK * kRatio + kRatio - 1;  // 2051
 
+// bits >= 0 ? bits | 2^31 : ~bits, as b ^ (sign-fill | 2^31): two instructions, no select
 __device__ __forceinline__ uint32_t orderable(float f) {
   const uint32_t b = __float_as_uint(f);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u);
 }
 
 __global__ void ids_fill_kernel(int32_t* __restrict__ ids, int64_t total, int32_t num_blocks) {
