@@ -94,10 +94,10 @@ def test_paged_compress_and_raw_tails(dtype):
     assert np.array_equal(dp2.numpy(), exp)
 
 
-def test_decode_loop_matches_oracle_and_prefill():
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_decode_loop_matches_oracle_and_prefill(dtype):
     """Prefill, then one token per step across nVis = 512 and a 128-token page edge."""
     qsa, g_ = _qsa(), _gu()
-    dtype = "bf16"
     B = 3
     total = [2100, 2060, 300]
     prefill = [2040, 2046, 250]
