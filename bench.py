@@ -694,7 +694,7 @@ def run_ours(args, rank: int, world: int) -> None:
             raise RuntimeError(qsa.qsa_last_error())
 
     ms_sel = loop_ms(select_only, max(10, K // 10))
-    decode = None if args.no_decode else decode_leg(qsa, lib, stream, K)
+    decode = None if args.no_decode else decode_leg(qsa, lib, stream, K, B=args.decode_batch)
     k1_small = None if args.no_sweep or rank != 0 else k1_configs_leg(qsa, lib, load_peaks()[0])
     torch.cuda.synchronize()
     faults = qsa.qsa_device_fault_flags()
@@ -780,6 +780,9 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the paged decode-step leg")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip K1 on the small configurations and the B*S size sweep")
+    ap.add_argument("--decode-batch", type=int, default=64, help="sequences in the decode-step leg")
+    ap.add_argument("--only-decode", action="store_true",
+                    help="run only the decode-step leg (for profiler captures)")
     ap.add_argument("--only-k1-configs", nargs="?", const="all", default=None, metavar="NAMES",
                     help="run only K1 on the small configurations and the size sweep, or on the named "
                          "configurations (comma-separated) without the sweep; for profiler captures")
@@ -794,6 +797,13 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank)
+        elif args.only_decode:
+            if rank == 0:
+                import torch
+                import sparse_attention_indexer_qsa_gb300 as qsa
+                torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+                leg = decode_leg(qsa, qsa.load(), torch.cuda.current_stream(), args.steps, B=args.decode_batch)
+                print(json.dumps({"decode": leg}), flush=True)
         elif args.only_k1_configs:
             if rank == 0:
                 import torch
