@@ -39,7 +39,7 @@ FALLBACK_HBM_GBS = 6800.0
 
 def algorithmic_bytes(ctx: np.ndarray, B: int, S: int, NB: int) -> dict:
     """Bytes each kernel must move (T = 2 bytes), from the layouts on the
-    "Qsa Indexer Kernels" page; see the design doc for the per-unit figures."""
+    "Qsa Indexer Kernels" page: per valid row or block, its reads and writes."""
     ctx = np.clip(ctx.astype(np.int64), 0, None)
     valid_rows = int(np.minimum(ctx, S).sum())
     pad_rows = B * S - valid_rows
@@ -294,9 +294,14 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
     for _ in range(5):
         step()
     torch.cuda.synchronize()
+    # a step touches 67 MB at B=64 (V-tails and logits), which L2 would keep from one
+    # step to the next: every timed step runs after an L2 flush
+    l2_flush = torch.empty(2 * torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size,
+                           dtype=torch.uint8, device="cuda")
     n = max(20, K)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
     for i in range(n):
+        l2_flush.fill_(1)
         step(evs[i])
     torch.cuda.synchronize()
     ms = {name: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
@@ -312,7 +317,26 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
                                          maxb, st)
         return rc
 
-    graph_step_ms = _graph_ms(torch, [step_on] * 10)  # a serving loop replays the step as a graph
+    # a serving loop replays the step as a graph: one step per replay, L2 flushed before each
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gs):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            if step_on(gs.cuda_stream) != 0:
+                raise RuntimeError("decode step failed during capture")
+    torch.cuda.current_stream().wait_stream(gs)
+    gts = []
+    for _ in range(max(20, K // 4)):
+        l2_flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        e1.synchronize()
+        gts.append(e0.elapsed_time(e1))
+    graph_step_ms = statistics.median(gts)
+    del l2_flush
     nvis = ctx_len // 4
     alg = {"pre_decode": B * (1280 + 1024 + 3 * 256 + 256 + 2 * 256),
            "scores_decode": B * (nvis * 256 + 1024 + nvis * 4),
@@ -325,8 +349,8 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
     return {"workload": f"decode step, B={B} sequences at ctx={ctx_len}, paged pool (128-token pages), bf16",
             "ms_per_step": graph_step_ms, "tokens_per_s": B / (graph_step_ms * 1e-3),
             "ms_per_step_eager": step_ms, "kernels": kernels,
-            "timed": ("step: CUDA graph of 10 back-to-back steps, median of 10 replays; kernels: CUDA events "
-                      "per kernel over eagerly launched steps")}
+            "timed": ("step: a CUDA graph of one step, replayed after an L2 flush, median; kernels: CUDA events "
+                      "per kernel over eagerly launched steps, each after an L2 flush")}
 
 
 def _graph_ms(torch, launches, reps: int = 10) -> float:
@@ -372,43 +396,51 @@ def _k1_launchers(qsa, lib, dt, bufs, ctx, cs, wq, wk, eps, B, S, NB):
     return {"k1a": k1a, "k1b": k1b, "k1_fused": fused}
 
 
+def _k1_touched(B: int, S: int, NB: int) -> dict:
+    """Bytes each K1 kernel touches (the cache-line footprint that L2 could keep between
+    launches): K1a the q part of every row and qNormed, K1b the 256-byte K slices and
+    kbar, the fused pass whole rows, qNormed and kbar."""
+    return {"k1a": B * S * 2048 + S * 256, "k1b": B * S * 256 + B * NB * 256 + S * 64,
+            "k1_fused": B * S * 2304 + B * NB * 256 + S * 256}
+
+
+K1_MAX_COPIES = 2048
+
+
 def k1_configs_leg(qsa, lib, hbm_peak: float, names=None, sweep: bool = True) -> dict:
     """K1a, K1b and the fused K1 on the small configurations (tiny, batched bf16/fp16,
     long, decode-parity full compress) and a size sweep of B*S from 2^16 to 2^22 rows.
-    Small configs fit in L2, so each timed launch uses its own copy of the inputs and
-    outputs, cycling through enough copies to exceed twice the L2 size; the launches run
-    back to back from a CUDA graph, median of 10 replays."""
+    Each timed launch of a kernel uses its own copy of the inputs and outputs, cycling
+    through enough copies that the kernel's footprint over a cycle exceeds twice the L2
+    size (at most K1_MAX_COPIES: the tiny configuration stays partly L2-warm); the
+    launches run back to back from a CUDA graph, median of 10 replays."""
     import torch
     import workloads
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
 
-    def measure(B, S, NB, dtype, ctx_np, make_sets, cs, wq, wk, eps, per_set_bytes):
-        n_sets = max(4, -(-2 * l2 // per_set_bytes))
-        bufs = make_sets(n_sets)
+    def copies(touched: int) -> int:
+        return int(min(K1_MAX_COPIES, max(1, -(-2 * l2 // touched))))
+
+    def measure(B, S, NB, dt, ctx_np, make_sets, cs, wq, wk, eps):
+        touched = _k1_touched(B, S, NB)
+        n_sets = {k: copies(v) for k, v in touched.items()}
+        bufs = make_sets(max(n_sets.values()))
         ctx = torch.from_numpy(np.ascontiguousarray(ctx_np, np.int32)).cuda()
-        dt = qsa.QSA_BF16 if dtype == "bf16" else qsa.QSA_F16
         L = _k1_launchers(qsa, lib, dt, bufs, ctx.data_ptr(), cs.data_ptr(), wq.data_ptr(), wk.data_ptr(), eps,
                           B, S, NB)
         ab = algorithmic_bytes(ctx_np, B, S, NB)
         ab["k1_fused"] = ab["k1a"] + ab["k1b"]
-        out = {"sets": n_sets, "bytes_per_set": per_set_bytes}
+        out = {}
         for name, mk in L.items():
-            ms = _graph_ms(torch, [mk(i) for i in range(n_sets)])
+            launches = [mk(i) for i in range(n_sets[name])]
+            if len(launches) == 1:
+                launches = launches * 2  # footprint above 2x L2: the second launch is cold too
+            ms = _graph_ms(torch, launches)
             gbs = ab[name] / (ms * 1e-3) / 1e9
-            out[name] = {"us": ms * 1e3, "alg_bytes": ab[name], "gbs": gbs, "frac_of_measured_hbm": gbs / hbm_peak}
+            out[name] = {"us": ms * 1e3, "alg_bytes": ab[name], "gbs": gbs, "frac_of_measured_hbm": gbs / hbm_peak,
+                         "copies": n_sets[name], "touched_bytes": touched[name]}
+        del bufs
         return out
-
-    def host_sets(wl):
-        B, S, NB = wl.B, wl.S, wl.num_blocks
-        per = B * S * 1280 + B * S * 1024 + B * NB * 256
-
-        def make(n):
-            iq0 = torch.from_numpy(np.ascontiguousarray(wl.index_qk).view(np.int16)).cuda()
-            iq = iq0.unsqueeze(0).repeat(n, 1, 1, 1).contiguous()
-            qn = torch.empty((n, B, S, 512), dtype=torch.int16, device="cuda")
-            kb = torch.empty((n, B, NB, 128), dtype=torch.int16, device="cuda")
-            return lambda i: (iq[i].data_ptr(), qn[i].data_ptr(), kb[i].data_ptr())
-        return make, per
 
     res = {"configs": {}, "sweep": []}
     cfgs = {"tiny": lambda: workloads.tiny(), "batched_bf16": lambda: workloads.batched("bf16"),
@@ -418,12 +450,19 @@ def k1_configs_leg(qsa, lib, hbm_peak: float, names=None, sweep: bool = True) ->
         if names is not None and name not in names:
             continue
         wl = make_wl()
+        B, S, NB = wl.B, wl.S, wl.num_blocks
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
                                          else np.ascontiguousarray(a)).cuda()
-        make, per = host_sets(wl)
-        r = measure(wl.B, wl.S, wl.num_blocks, wl.dtype, wl.context_lengths, make, dev(wl.cos_sin),
-                    dev(wl.w_q), dev(wl.w_k), wl.eps, per)
-        r["shape"] = {"B": wl.B, "S": wl.S, "num_blocks": wl.num_blocks, "dtype": wl.dtype}
+
+        def make(n, wl=wl, B=B, S=S, NB=NB):
+            iq0 = torch.from_numpy(np.ascontiguousarray(wl.index_qk).view(np.int16)).cuda()
+            iq = iq0.unsqueeze(0).repeat(n, 1, 1, 1).contiguous()
+            qn = torch.empty((n, B, S, 512), dtype=torch.int16, device="cuda")
+            kb = torch.empty((n, B, NB, 128), dtype=torch.int16, device="cuda")
+            return lambda i: (iq[i].data_ptr(), qn[i].data_ptr(), kb[i].data_ptr())
+        dt = qsa.QSA_BF16 if wl.dtype == "bf16" else qsa.QSA_F16
+        r = measure(B, S, NB, dt, wl.context_lengths, make, dev(wl.cos_sin), dev(wl.w_q), dev(wl.w_k), wl.eps)
+        r["shape"] = {"B": B, "S": S, "num_blocks": NB, "dtype": wl.dtype}
         res["configs"][name] = r
         torch.cuda.empty_cache()
     if not sweep:
@@ -437,32 +476,26 @@ def k1_configs_leg(qsa, lib, hbm_peak: float, names=None, sweep: bool = True) ->
     wk = torch.from_numpy(workloads.gamma(rng, "bf16").view(np.int16)).cuda()
     gen = torch.Generator(device="cuda").manual_seed(5)
     for B in (4, 8, 16, 32, 64, 128, 256):
-        per = B * S * (1280 + 1024) + B * NB * 256
-
         def make(n, B=B):
-            iq = torch.randn((n, B, S, 640), generator=gen, device="cuda").to(torch.bfloat16).view(torch.int16)
+            iq = torch.empty((n, B, S, 640), dtype=torch.int16, device="cuda")
+            for i in range(n):
+                iq[i].copy_(torch.randn((B, S, 640), generator=gen, device="cuda").to(torch.bfloat16)
+                            .view(torch.int16))
             qn = torch.empty((n, B, S, 512), dtype=torch.int16, device="cuda")
             kb = torch.empty((n, B, NB, 128), dtype=torch.int16, device="cuda")
             return lambda i: (iq[i].data_ptr(), qn[i].data_ptr(), kb[i].data_ptr())
-        n_sets = 1 if per > 2 * l2 else 2
-        bufs = make(n_sets)
-        ctx_np = np.full(B, S, np.int32)
-        ctx = torch.from_numpy(ctx_np).cuda()
-        L = _k1_launchers(qsa, lib, qsa.QSA_BF16, bufs, ctx.data_ptr(), cs.data_ptr(), wq.data_ptr(),
-                          wk.data_ptr(), 1e-6, B, S, NB)
-        ab = algorithmic_bytes(ctx_np, B, S, NB)
-        ab["k1_fused"] = ab["k1a"] + ab["k1b"]
-        row = {"rows": B * S, "B": B, "S": S, "sets": n_sets}
-        for name, mk in L.items():
-            ms = _graph_ms(torch, [mk(i) for i in range(n_sets)] * 2)
-            row[name + "_gbs"] = ab[name] / (ms * 1e-3) / 1e9
-            row[name + "_us"] = ms * 1e3
+        r = measure(B, S, NB, qsa.QSA_BF16, np.full(B, S, np.int32), make, cs, wq, wk, 1e-6)
+        row = {"rows": B * S, "B": B, "S": S}
+        for name in ("k1a", "k1b", "k1_fused"):
+            row[name + "_gbs"] = r[name]["gbs"]
+            row[name + "_us"] = r[name]["us"]
+            row[name + "_copies"] = r[name]["copies"]
         res["sweep"].append(row)
-        del bufs, L
         torch.cuda.empty_cache()
-    res["how"] = ("per-launch device time from a CUDA graph of back-to-back launches (median of 10 replays); "
-                  "small configs cycle through copies of inputs and outputs totalling more than 2x L2; the "
-                  "sweep's inputs are drawn on the device (torch generator, seed 5), S=16384, ctx=S, bf16")
+    res["how"] = ("per-launch device time from a CUDA graph of back-to-back launches (median of 10 replays); each "
+                  "kernel cycles through copies of its inputs and outputs whose footprint exceeds 2x L2 (at most "
+                  f"{K1_MAX_COPIES} copies); the sweep's inputs are drawn on the device (torch generator, seed 5), "
+                  "S=16384, ctx=S, bf16")
     res["l2_bytes"] = l2
     return res
 
@@ -683,8 +716,28 @@ def run_ours(args, rank: int, world: int) -> None:
         ms_e2e = e0.elapsed_time(e1) / K_e2e if K_e2e else float("nan")
     torch.cuda.synchronize()
     # the separate K1a and K1b entry points, each back to back over the same workload
-    ms_k1a = loop_ms(k1a_only, max(K, 20))
-    ms_k1b = loop_ms(k1b_only, max(K, 20))
+    # K1b alone touches 42 MB (the K slices and kbar), which L2 would keep across
+    # back-to-back launches: each standalone launch runs after an L2 flush instead
+    l2_flush = torch.empty(2 * torch.cuda.get_device_properties(local).L2_cache_size, dtype=torch.uint8,
+                           device="cuda")
+
+    def cold_ms(fn, n):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(n):
+            l2_flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    ms_k1a = cold_ms(k1a_only, max(K // 4, 20))
+    ms_k1b = cold_ms(k1b_only, max(K // 4, 20))
     # prefill selection on the step's logits (top-512 blocks per row -> 2051 token ids)
     out_idx = torch.empty((rows, 2051), dtype=torch.int32, device="cuda")
 
@@ -719,8 +772,9 @@ def run_ours(args, rank: int, world: int) -> None:
                       "frac_of_measured_hbm": gbs / hbm_peak, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS}
     kernels["k1_fused"]["rows_per_s"] = rows / (per_kernel["k1_fused"] * 1e-3)
     kernels["k1_fused"]["timed"] = "inside the step (CUDA events around the launch)"
-    for n in ("k1a", "k1b", "select"):
-        kernels[n]["timed"] = "separate entry point, back-to-back launches after the step loop"
+    for n in ("k1a", "k1b"):
+        kernels[n]["timed"] = "separate entry point after the step loop; each launch after an L2 flush, median"
+    kernels["select"]["timed"] = "separate entry point, back-to-back launches after the step loop (1 GB of logits)"
     kernels["select"]["rows_per_s"] = rows / (per_kernel["select"] * 1e-3)
     kernels["k1a"]["rows_per_s"] = rows / (per_kernel["k1a"] * 1e-3)
     kernels["k1b"]["blocks_per_s"] = B * NB / (per_kernel["k1b"] * 1e-3)
