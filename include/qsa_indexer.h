@@ -210,7 +210,7 @@ int qsa_index_expand(int32_t* outIdx, const int32_t* sortedIds, const int32_t* c
  * segmented sort of the chunk's logits with the ids as values, qsa_index_expand)
  * in one kernel, with no sort and no workspace.  Per row: the FP32 logits of the
  * visible blocks g < nVis are mapped to order-preserving u32 keys
- * (bits >= 0 ? bits | 0x80000000 : ~bits); an MSB-first 8-bit radix select finds
+ * (bits >= 0 ? bits | 0x80000000 : ~bits); an MSB-first radix select finds
  * the kSel-th largest key; keys above it are selected, and keys equal to it in
  * ascending block order until kSel are selected.  That is exactly the set of
  * blocks the three-step pipeline puts first (and the rule of the page's decode
