@@ -336,11 +336,44 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
         e1.synchronize()
         gts.append(e0.elapsed_time(e1))
     graph_step_ms = statistics.median(gts)
-    del l2_flush
     nvis = ctx_len // 4
     alg = {"pre_decode": B * (1280 + 1024 + 3 * 256 + 256 + 2 * 256),
            "scores_decode": B * (nvis * 256 + 1024 + nvis * 4),
            "topk_expand_decode": B * (nvis * 4 + 2051 * 4)}
+    # prefill persistence into the same pool: K1b with the V-tail write over every
+    # sequence's ctx-1 tokens (4095 complete blocks each), then the 3 raw K-tails
+    iq_full = torch.randn((B, ctx_len, 640), device="cuda").to(torch.bfloat16)
+    kb_dense = torch.empty((B, maxb, 128), dtype=torch.bfloat16, device="cuda")
+    pctx = torch.full((B,), ctx_len - 1, dtype=torch.int32, device="cuda")
+    cs_full = torch.randn((ctx_len, 64), device="cuda")
+
+    def compress_paged(st):
+        return lib.qsa_index_k_compress_paged(qsa.QSA_BF16, kb_dense.data_ptr(), iq_full.data_ptr(),
+                                              cs_full.data_ptr(), pctx.data_ptr(), wk.data_ptr(), 1e-6, st_ref,
+                                              B, ctx_len, maxb, 0, maxb, 0, st)
+
+    def raw_tails(st):
+        return lib.qsa_raw_k_tail_write_prefill(qsa.QSA_BF16, iq_full.data_ptr(), pctx.data_ptr(), st_ref, B,
+                                                ctx_len, st)
+
+    for name, fn in (("k_compress_paged", compress_paged), ("raw_k_tail_write_prefill", raw_tails)):
+        for _ in range(3):
+            if fn(sp) != 0:
+                raise RuntimeError(qsa.qsa_last_error())
+        pts = []
+        for _ in range(20):
+            l2_flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn(sp)
+            e1.record(stream)
+            e1.synchronize()
+            pts.append(e0.elapsed_time(e1))
+        ms[name] = statistics.median(pts)
+    valid_blocks = B * ((ctx_len - 1) // 4)
+    alg["k_compress_paged"] = valid_blocks * (1024 + 256 + 256) + ((ctx_len - 1) // 4) * 256
+    alg["raw_k_tail_write_prefill"] = B * ((ctx_len - 1) % 4) * 512
+    del iq_full, kb_dense, l2_flush
     hbm_peak, _, _ = load_peaks()
     kernels = {k: {"ms": ms[k], "alg_bytes": alg[k], "gbs": alg[k] / (ms[k] * 1e-3) / 1e9,
                    "frac_of_measured_hbm": alg[k] / (ms[k] * 1e-3) / 1e9 / hbm_peak} for k in ms}
@@ -350,7 +383,9 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
             "ms_per_step": graph_step_ms, "tokens_per_s": B / (graph_step_ms * 1e-3),
             "ms_per_step_eager": step_ms, "kernels": kernels,
             "timed": ("step: a CUDA graph of one step, replayed after an L2 flush, median; kernels: CUDA events "
-                      "per kernel over eagerly launched steps, each after an L2 flush")}
+                      "per kernel over eagerly launched steps, each after an L2 flush; k_compress_paged and "
+                      "raw_k_tail_write_prefill: the prefill persistence of the same B sequences (ctx-1 tokens "
+                      "each) into the pool, one launch after an L2 flush, median")}
 
 
 def _graph_ms(torch, launches, reps: int = 10) -> float:
