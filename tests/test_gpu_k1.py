@@ -202,3 +202,28 @@ def test_fused_qk_prep_bit_identical_to_separate_calls(dtype, B, S, ctx):
     assert np.array_equal(k_f, k_sep)
     assert np.all(k_f[:, wl.num_blocks:] == SENT)
     g_.assert_no_device_faults()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_cos_sin_rows_past_the_last_needed_position_are_never_read(dtype):
+    """cos/sin rows at positions no valid row or block uses (>= max ctx) hold NaN: K1a,
+    K1b and the fused pass give the same bits as with a clean table."""
+    import sparse_attention_indexer_qsa_gb300 as qsa
+    g_ = _gpu()
+    wl = workloads.custom(3, 300, [300, 157, 9], dtype=dtype, seed=61, nan_padding=True, max_positions=600)
+    d = g_.DevWorkload(wl)
+    NB = wl.num_blocks
+    clean_q = g_.q_prep(d)
+    clean_k = g_.k_compress(d, NB, 0, NB, 0)
+    poisoned = wl.cos_sin.copy()
+    poisoned[int(wl.context_lengths.max()):] = np.nan
+    d.cos_sin = g_.dev(poisoned)
+    assert np.array_equal(g_.q_prep(d), clean_q)
+    assert np.array_equal(g_.k_compress(d, NB, 0, NB, 0), clean_k)
+    td = g_.t_dtype(dtype)
+    qn = torch.empty((3, 300, 4, 128), dtype=td, device="cuda")
+    kb = torch.empty((3, NB, 128), dtype=td, device="cuda")
+    qsa.qsa_index_qk_prep(qn, kb, d.index_qk, d.cos_sin, d.ctx, d.w_q, d.w_k, wl.eps, 3, 300, NB, dtype=dtype)
+    torch.cuda.synchronize()
+    assert np.array_equal(qn.view(torch.int16).cpu().numpy().view(np.uint16), clean_q)
+    assert np.array_equal(kb.view(torch.int16).cpu().numpy().view(np.uint16), clean_k)
