@@ -230,3 +230,15 @@ def test_topk_expand_decode_long_rows(maxb):
     qsa.qsa_topk_expand_decode(out.ptr, g_.dev(lg), g_.dev(ctx), split, 3, B, maxb)
     assert np.array_equal(out.numpy(np.int32, (B, W)), oracle.topk_expand_decode(lg, ctx))
     assert not split.any()
+
+
+def test_topk_expand_never_reads_masked_cells():
+    """Logits at g >= nVis (K2's -FLT_MAX cells) replaced by NaN: the same output."""
+    B, S, NB = 2, 3000, 750
+    ctx = [3000, 2222]
+    lg = _logits_like_k2(B, S, NB, ctx, seed=21)
+    ref = _run_topk(lg, ctx, B, S, NB, 0)
+    poisoned = lg.copy()
+    poisoned[poisoned == np.float32(NEG_MAX)] = np.nan
+    assert np.isnan(poisoned).any()
+    assert np.array_equal(_run_topk(poisoned, ctx, B, S, NB, 0), ref)
