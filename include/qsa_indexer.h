@@ -321,6 +321,30 @@ int qsa_topk_expand_decode(int32_t* outIdx, const float* logits, const int32_t* 
                            qsa_stream_t stream);
 
 /*
+ * The decode step in one launch: qsa_indexer_pre_decode, qsa_index_scores_decode and
+ * qsa_topk_expand_decode, in that order, over the same arguments ("Qsa Indexer
+ * Kernels": launchQsaIndexerPreDecode, launchQsaIndexScoresDecode,
+ * launchQsaTopKExpandDecode).  Every output equals, bit for bit, the output of the three
+ * calls: qNormed [B, 1, 4, 128], the pool's K- or V-tail of the new token, logits
+ * [B, maxBlocks] (only g < nVis written), outIdx [B, 1, 2051] and the zeroed split
+ * counters.  (The fusion is an addition of this library; the page has three launches.)
+ * Each CTA computes its sequence's q heads once and scores a run of 128-block chunks
+ * of that sequence (the run length sizes the grid to about one wave of resident
+ * CTAs); the CTA that completes a sequence last runs its selection, so no CTA waits
+ * for another.  Sequences report completion
+ * through a device-side counter set, one of 16 taken in turn by each launch: at most
+ * 16 launches may be in flight on one device at a time, and a CUDA graph that captured
+ * a launch keeps its set on every replay (replays of one graph must not overlap).
+ * Limits: batchSize <= 4096, maxBlocks <= 65536.
+ * Errors: QSA_E_NULL, QSA_E_DTYPE, QSA_E_SHAPE, QSA_E_ALIGN, QSA_E_CUDA.
+ */
+int qsa_indexer_decode_step(qsa_dtype_t dtype, int32_t* outIdx, float* logits, void* qNormed,
+                            const void* indexQk, const float* cosSin, const int32_t* contextLengths,
+                            const void* wQ, const void* wK, float rmsEps, const qsa_pool_state_t* pool,
+                            int32_t* splitCounters, int32_t numKVHeads, int32_t batchSize, int32_t maxBlocks,
+                            qsa_stream_t stream);
+
+/*
  * qsa_index_scores_no_alloc: the K2 scores of qsa_index_scores, for callers that
  * must not allocate device memory.  (No counterpart on the "Qsa Indexer Kernels"
  * page; an addition of this library.)

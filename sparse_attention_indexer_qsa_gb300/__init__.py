@@ -22,7 +22,7 @@ __all__ = [
     "qsa_index_scores_no_alloc", "qsa_index_ids_fill", "qsa_index_expand", "qsa_index_topk_expand",
     "PoolState", "pool_state", "qsa_index_k_compress_paged", "qsa_raw_k_tail_write_prefill",
     "qsa_indexer_pre_decode", "qsa_index_scores_decode", "qsa_topk_expand_decode",
-    "qsa_device_fault_flags",
+    "qsa_indexer_decode_step", "qsa_device_fault_flags",
     "qsa_testing_index_scores_cuda_core", "LIB_PATH",
 ]
 
@@ -33,7 +33,7 @@ STATUS_NAMES = {0: "QSA_OK", -1: "QSA_E_NULL", -2: "QSA_E_SHAPE", -3: "QSA_E_RAN
 EXPORTED = ["qsa_abi_version", "qsa_last_error", "qsa_index_q_prep", "qsa_index_k_compress",
             "qsa_index_qk_prep", "qsa_index_ids_fill", "qsa_index_expand", "qsa_index_topk_expand",
             "qsa_index_k_compress_paged", "qsa_raw_k_tail_write_prefill", "qsa_indexer_pre_decode",
-            "qsa_index_scores_decode", "qsa_topk_expand_decode",
+            "qsa_index_scores_decode", "qsa_topk_expand_decode", "qsa_indexer_decode_step",
             "qsa_index_scores", "qsa_index_scores_no_alloc", "qsa_device_fault_flags",
             "qsa_testing_index_scores_cuda_core"]
 
@@ -103,6 +103,8 @@ def load():
     L.qsa_index_scores_decode.restype = ctypes.c_int
     L.qsa_topk_expand_decode.argtypes = [p, p, p, p, i32, i32, i32, p]
     L.qsa_topk_expand_decode.restype = ctypes.c_int
+    L.qsa_indexer_decode_step.argtypes = [ctypes.c_int, p, p, p, p, p, p, p, p, f32, pp, p, i32, i32, i32, p]
+    L.qsa_indexer_decode_step.restype = ctypes.c_int
     L.qsa_index_scores.argtypes = [ctypes.c_int, p, p, p, p, i32, i32, i32, i32, i32, p]
     L.qsa_index_scores.restype = ctypes.c_int
     L.qsa_index_scores_no_alloc.argtypes = list(L.qsa_index_scores.argtypes)
@@ -256,6 +258,17 @@ def qsa_topk_expand_decode(outIdx, logits, contextLengths, splitCounters, numKVH
     """Decode top-512 + expand (+ split-counter zeroing)."""
     _check(load().qsa_topk_expand_decode(_addr(outIdx), _addr(logits), _addr(contextLengths), _addr(splitCounters),
                                       int(numKVHeads), int(batchSize), int(maxBlocks), _stream(stream)))
+
+
+def qsa_indexer_decode_step(outIdx, logits, qNormed, indexQk, cosSin, contextLengths, wQ, wK, rmsEps,
+                            pool: PoolState, splitCounters, numKVHeads, batchSize, maxBlocks, stream=None,
+                            dtype=None):
+    """The decode step in one launch: pre-decode, paged scores, top-512 + expand."""
+    _check(load().qsa_indexer_decode_step(_dtype(dtype, indexQk, qNormed), _addr(outIdx), _addr(logits),
+                                       _addr(qNormed), _addr(indexQk), _addr(cosSin), _addr(contextLengths),
+                                       _addr(wQ), _addr(wK), float(rmsEps), ctypes.byref(pool),
+                                       _addr(splitCounters), int(numKVHeads), int(batchSize), int(maxBlocks),
+                                       _stream(stream)))
 
 
 def qsa_index_scores_no_alloc(logits, qNormed, kbar, contextLengths, batchSize, seqLen, numBlocks,

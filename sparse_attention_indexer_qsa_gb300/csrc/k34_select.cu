@@ -17,20 +17,11 @@
 #include <cstdint>
 
 #include "qsa_launch.h"
+#include "qsa_select.cuh"
 
 namespace qsa {
 
 namespace sel {
-
-constexpr int kTopK = 512;
-constexpr int kRatio = 4;
-constexpr int kWidth = kTopK * kRatio + kRatio - 1;  // 2051
-
-// bits >= 0 ? bits | 2^31 : ~bits, as b ^ (sign-fill | 2^31): two instructions, no select
-__device__ __forceinline__ uint32_t orderable(float f) {
-  const uint32_t b = __float_as_uint(f);
-  return b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u);
-}
 
 __global__ void ids_fill_kernel(int32_t* __restrict__ ids, int64_t total, int32_t num_blocks) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -58,450 +49,6 @@ __global__ void expand_kernel(int32_t* __restrict__ out_idx, const int32_t* __re
     else if (i < kRatio * k_sel + tail) v = kRatio * n_vis + (i - kRatio * k_sel);
     out[i] = v;
   }
-}
-
-// ---------------------------------------------------------------------------
-// topk: one CTA of T threads per row.
-//
-//  1. histogram of the top kD1 key bits over the visible blocks (coalesced); warp 0
-//     finds the bin b1 holding the kSel-th largest key, the count above it and c1,
-//     its own count;
-//  2. one ordered pass: thread k owns the 32*MW contiguous blocks from 32*MW*k and
-//     records, as bit masks, which lie above b1 (selected) and in b1 (candidates);
-//     candidates' block ids are listed, each thread's in ascending order;
-//  3. unless b1 is filled exactly, the threshold key T inside b1, and how many keys
-//     equal to T are still to be taken, are resolved by 8-bit radix passes: over
-//     the listed candidates by warp 0 alone (up to kWarpCap of them), otherwise by
-//     the whole CTA over the row;
-//  4. candidates above T become selected and ties are taken in ascending block
-//     order; one block scan of packed (selected, tied) counts gives each thread the
-//     position of its first winner; winners are written in ascending order and the
-//     row is expanded.
-// Keys are read from global memory (L1/L2 after the first pass).  Small CTAs (64
-// threads, up to 20 a SM) keep many rows in flight: the warp-0 steps between the
-// passes are serial and would otherwise leave the SM idle.
-#ifndef QSA_SEL_D1_BITS
-#define QSA_SEL_D1_BITS 11
-#endif
-#ifndef QSA_SEL_WARPS_PER_SM
-#define QSA_SEL_WARPS_PER_SM 40
-#endif
-constexpr int kD1 = QSA_SEL_D1_BITS;
-constexpr int kBins1 = 1 << kD1;
-constexpr int kShift1 = 32 - kD1;
-constexpr int kSuper = kBins1 / 128;   // 128-bin super-bins for the two-level search
-constexpr int kCpl = 16;               // listed candidates a lane of warp 0 may hold
-constexpr int kWarpCap = 32 * kCpl;
-constexpr int kMaxBlocks = 65536;
-static_assert(kWarpCap <= kBins1, "the candidate list reuses the histogram's storage");
-
-template <int T>
-struct SelShared {
-  uint32_t hist1[kBins1];  // pass-1 histogram, then the candidate list
-  uint32_t hist2[256];
-  int32_t win[kTopK];
-  uint8_t cls[kWarpCap];   // per listed candidate: 2 above T, 1 tied, 0 below
-  uint32_t warp_tot[T / 32];
-  uint32_t thr_bin, thr_above, thr_count, ncand;
-  int32_t rem;
-};
-
-// The visible keys of one row.
-struct GlobalKeys {
-  const float* p;
-  bool vec;  // p is 16-byte aligned
-  __device__ __forceinline__ float4 ld4(int32_t g) const { return __ldg(reinterpret_cast<const float4*>(p + g)); }
-  __device__ __forceinline__ float ld1(int32_t g) const { return __ldg(p + g); }
-};
-
-// exclusive scan of one value per thread over the CTA of T threads
-template <int T>
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_tot) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t incl = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += x;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  uint32_t base = 0;
-#pragma unroll
-  for (int w = 0; w < T / 32; ++w)
-    if (w < warp) base += warp_tot[w];
-  __syncthreads();  // warp_tot may be reused by the next scan
-  return base + incl - v;
-}
-
-struct Threshold {
-  uint32_t bin, above, count;
-};
-
-__device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t v, int lane) {
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t x = __shfl_up_sync(0xffffffffu, v, off);
-    if (lane >= off) v += x;
-  }
-  return v;
-}
-
-// The lane whose bins hold the k-th count (`hit`) walks its NB bins, highest first,
-// from running count c; the result goes to every lane.
-template <int NB>
-__device__ __forceinline__ Threshold walk_and_share(const uint32_t (&bins)[NB], uint32_t top, uint32_t c,
-                                                    uint32_t k, bool hit) {
-  Threshold th{0u, 0u, 0u};
-  if (hit) {
-    bool done = false;
-#pragma unroll
-    for (int j = 0; j < NB; ++j) {
-      if (!done) {
-        if (c + bins[j] >= k) {
-          th = Threshold{top - j, c, bins[j]};
-          done = true;
-        } else {
-          c += bins[j];
-        }
-      }
-    }
-  }
-  const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
-  th.bin = __shfl_sync(0xffffffffu, th.bin, src);
-  th.above = __shfl_sync(0xffffffffu, th.above, src);
-  th.count = __shfl_sync(0xffffffffu, th.count, src);
-  return th;
-}
-
-// One warp: walk the kBins1 bins from the highest down to where the running count
-// reaches k (1 <= k <= total).  128-bin super-bins are summed first (a 16-byte load
-// and a warp reduction each); the chosen one is searched 4 bins a lane.
-__device__ __forceinline__ Threshold find_first_digit(const uint32_t* hist, uint32_t k) {
-  const int lane = threadIdx.x & 31;
-  const uint4* h4 = reinterpret_cast<const uint4*>(hist);
-  uint32_t ssum[kSuper];
-#pragma unroll
-  for (int s = 0; s < kSuper; ++s) {
-    const uint4 v = h4[s * 32 + lane];
-    ssum[s] = __reduce_add_sync(0xffffffffu, v.x + v.y + v.z + v.w);
-  }
-  uint32_t cum = 0;
-  int sstar = 0;
-  bool found = false;
-#pragma unroll
-  for (int s = kSuper - 1; s >= 0; --s) {
-    if (!found) {
-      if (cum + ssum[s] >= k) {
-        sstar = s;
-        found = true;
-      } else {
-        cum += ssum[s];
-      }
-    }
-  }
-  const uint4 v = h4[sstar * 32 + 31 - lane];  // lane 0 holds the super-bin's top 4 bins
-  const uint32_t b4[4] = {v.w, v.z, v.y, v.x};
-  const uint32_t mine = v.x + v.y + v.z + v.w;
-  const uint32_t incl = cum + warp_inclusive_sum(mine, lane);
-  const uint32_t excl = incl - mine;
-  const uint32_t top = static_cast<uint32_t>(sstar) * 128u + 4u * static_cast<uint32_t>(31 - lane) + 3u;
-  return walk_and_share(b4, top, excl, k, excl < k && k <= incl);
-}
-
-// One warp: the same over 256 bins, 8 a lane.
-__device__ __forceinline__ Threshold find_digit256(const uint32_t* hist, uint32_t k) {
-  const int lane = threadIdx.x & 31;
-  const uint4* h4 = reinterpret_cast<const uint4*>(hist);
-  const uint4 lo = h4[2 * (31 - lane)], hi = h4[2 * (31 - lane) + 1];
-  const uint32_t b8[8] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};
-  uint32_t mine = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) mine += b8[j];
-  const uint32_t incl = warp_inclusive_sum(mine, lane);
-  const uint32_t excl = incl - mine;
-  return walk_and_share(b8, 8u * static_cast<uint32_t>(31 - lane) + 7u, excl, k, excl < k && k <= incl);
-}
-
-// f(key) for every visible block, T-strided (coalesced / conflict-free).
-template <int T, class K, class F>
-__device__ __forceinline__ void for_each_key(const K& keys, int32_t n, F&& f) {
-  int32_t g = threadIdx.x;
-  if (keys.vec) {
-    const int32_t nv = n >> 2;
-#pragma unroll 4
-    for (int32_t v = threadIdx.x; v < nv; v += T) {
-      const float4 x = keys.ld4(4 * v);
-      f(orderable(x.x));
-      f(orderable(x.y));
-      f(orderable(x.z));
-      f(orderable(x.w));
-    }
-    g = 4 * nv + threadIdx.x;
-  }
-  for (; g < n; g += T) f(orderable(keys.ld1(g)));
-}
-
-// The selection of one visible row (n_vis > 512 keys): winners' block ids, ascending,
-// in sh.win[0, 512).  Ends with a CTA barrier.
-template <int T, int MW, class K>
-__device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShared<T>& sh) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int32_t k_sel = kTopK;
-
-  // ---- 1. first-digit histogram and its threshold bin
-  for (int k = tid; k < kBins1 / 4; k += T) reinterpret_cast<uint4*>(sh.hist1)[k] = make_uint4(0u, 0u, 0u, 0u);
-  if (tid == 0) sh.ncand = 0;
-  __syncthreads();
-  for_each_key<T>(keys, n_vis, [&](uint32_t key) { atomicAdd(&sh.hist1[key >> kShift1], 1u); });
-  __syncthreads();
-  if (warp == 0) {
-    const Threshold th = find_first_digit(sh.hist1, static_cast<uint32_t>(k_sel));
-    if (lane == 0) {
-      sh.thr_bin = th.bin;
-      sh.thr_above = th.above;
-      sh.thr_count = th.count;
-    }
-  }
-  __syncthreads();
-  const uint32_t b1 = sh.thr_bin;
-  const uint32_t c1 = sh.thr_count;
-  int32_t rem = k_sel - static_cast<int32_t>(sh.thr_above);
-  const bool exact1 = c1 == static_cast<uint32_t>(rem);
-  const bool listed = !exact1 && c1 <= static_cast<uint32_t>(kWarpCap);
-  const uint32_t lo1 = b1 << kShift1, hi1 = lo1 | ((1u << kShift1) - 1u);
-
-  // ---- 2. ordered pass over this thread's contiguous blocks
-  const int32_t g0 = tid * (32 * MW);
-  uint32_t gtm[MW], cm[MW];
-#pragma unroll
-  for (int w = 0; w < MW; ++w) {
-    gtm[w] = 0u;
-    cm[w] = 0u;
-    const int32_t gb = g0 + 32 * w;
-    if (keys.vec && gb + 32 <= n_vis) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float4 x = keys.ld4(gb + 4 * e);
-        const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t key = orderable(xs[j]);
-          const uint32_t bit = 1u << (4 * e + j);
-          if (key > hi1) gtm[w] |= bit;
-          if ((key >> kShift1) == b1) cm[w] |= bit;
-        }
-      }
-    } else if (gb < n_vis) {
-      const int32_t n = n_vis - gb;  // ragged: fewer than 32, or unaligned
-#pragma unroll 4
-      for (int e = 0; e < 32; ++e) {
-        if (e < n) {
-          const uint32_t key = orderable(keys.ld1(gb + e));
-          if (key > hi1) gtm[w] |= 1u << e;
-          if ((key >> kShift1) == b1) cm[w] |= 1u << e;
-        }
-      }
-    }
-  }
-  uint32_t my_cand = 0, cbase = 0;
-  if (listed) {
-#pragma unroll
-    for (int w = 0; w < MW; ++w) my_cand += __popc(cm[w]);
-    if (my_cand) {
-      cbase = atomicAdd(&sh.ncand, my_cand);
-      uint32_t j = cbase;
-#pragma unroll
-      for (int w = 0; w < MW; ++w) {
-        uint32_t m = cm[w];
-        while (m) {
-          sh.hist1[j++] = static_cast<uint32_t>(g0 + 32 * w + __ffs(m) - 1);
-          m &= m - 1u;
-        }
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---- 3. resolve the threshold inside bin b1
-  if (listed) {
-    if (warp == 0) {
-      const uint32_t nc = c1;
-      const int nq = static_cast<int>((nc + 31u) >> 5);
-      for (int q = 0; q < nq; ++q) {  // candidates' keys, in place of their block ids
-        const uint32_t j = lane + 32u * q;
-        if (j < nc) sh.hist1[j] = orderable(keys.ld1(static_cast<int32_t>(sh.hist1[j])));
-      }
-      __syncwarp();
-      uint32_t prefix = lo1, mask = ~((1u << kShift1) - 1u);
-      int32_t rm = rem;
-#pragma unroll 1
-      for (int top = kShift1; top > 0;) {
-        const int width = min(8, top);
-        const int shift = top - width;
-        const uint32_t dmask = (1u << width) - 1u;
-        reinterpret_cast<uint4*>(sh.hist2)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
-        reinterpret_cast<uint4*>(sh.hist2)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
-        __syncwarp();
-        for (int q = 0; q < nq; ++q) {
-          const uint32_t j = lane + 32u * q;
-          if (j < nc) {
-            const uint32_t key = sh.hist1[j];
-            if ((key & mask) == prefix) atomicAdd(&sh.hist2[(key >> shift) & dmask], 1u);
-          }
-        }
-        __syncwarp();
-        const Threshold th = find_digit256(sh.hist2, static_cast<uint32_t>(rm));
-        rm -= static_cast<int32_t>(th.above);
-        prefix |= th.bin << shift;
-        mask |= dmask << shift;
-        top = shift;
-        if (th.count == static_cast<uint32_t>(rm)) break;
-        __syncwarp();  // every lane has read hist2 before it is cleared
-      }
-      const uint32_t lo = prefix, hi = prefix | ~mask;
-      for (int q = 0; q < nq; ++q) {
-        const uint32_t j = lane + 32u * q;
-        if (j < nc) {
-          const uint32_t key = sh.hist1[j];
-          sh.cls[j] = key > hi ? 2 : (key >= lo ? 1 : 0);
-        }
-      }
-      if (lane == 0) sh.rem = rm;
-    }
-    __syncthreads();
-    rem = sh.rem;
-    if (my_cand) {  // this thread's candidates sit at [cbase, cbase + my_cand), ascending
-      uint32_t j = cbase;
-#pragma unroll
-      for (int w = 0; w < MW; ++w) {
-        uint32_t m = cm[w];
-        while (m) {
-          const uint32_t bit = m & (0u - m);
-          m &= m - 1u;
-          const uint8_t k = sh.cls[j++];
-          if (k == 2) gtm[w] |= bit;
-          if (k != 1) cm[w] &= ~bit;
-        }
-      }
-    }
-  } else if (!exact1) {  // more candidates than warp 0 holds: passes over the row
-    uint32_t prefix = lo1, mask = ~((1u << kShift1) - 1u);
-#pragma unroll 1
-    for (int top = kShift1; top > 0;) {
-      const int width = min(8, top);
-      const int shift = top - width;
-      const uint32_t dmask = (1u << width) - 1u;
-      for (int k = tid; k < 256; k += T) sh.hist2[k] = 0u;
-      __syncthreads();
-      for_each_key<T>(keys, n_vis, [&](uint32_t key) {
-        if ((key & mask) == prefix) atomicAdd(&sh.hist2[(key >> shift) & dmask], 1u);
-      });
-      __syncthreads();
-      if (warp == 0) {
-        const Threshold th = find_digit256(sh.hist2, static_cast<uint32_t>(rem));
-        if (lane == 0) {
-          sh.thr_bin = th.bin;
-          sh.thr_above = th.above;
-          sh.thr_count = th.count;
-        }
-      }
-      __syncthreads();
-      rem -= static_cast<int32_t>(sh.thr_above);
-      prefix |= sh.thr_bin << shift;
-      mask |= dmask << shift;
-      top = shift;
-      if (sh.thr_count == static_cast<uint32_t>(rem)) break;
-    }
-    const uint32_t lo = prefix, hi = prefix | ~mask;
-#pragma unroll
-    for (int w = 0; w < MW; ++w) {
-      uint32_t m = cm[w];
-      while (m) {
-        const int bit = __ffs(m) - 1;
-        m &= m - 1u;
-        const uint32_t key = orderable(keys.ld1(g0 + 32 * w + bit));
-        if (key > hi) gtm[w] |= 1u << bit;
-        if (key > hi || key < lo) cm[w] &= ~(1u << bit);
-      }
-    }
-  }
-
-  // ---- 4. positions: selected count in bits [0, 10), tied count above
-  uint32_t ngt = 0, ntie = 0;
-#pragma unroll
-  for (int w = 0; w < MW; ++w) {
-    ngt += __popc(gtm[w]);
-    ntie += __popc(cm[w]);
-  }
-  const uint32_t ex = block_exclusive_scan<T>(ngt | (ntie << 10), sh.warp_tot);
-  const uint32_t rem_u = static_cast<uint32_t>(rem);
-  const uint32_t tie_before = ex >> 10;
-  uint32_t pos = (ex & 1023u) + min(tie_before, rem_u);
-  uint32_t take = tie_before >= rem_u ? 0u : min(rem_u - tie_before, ntie);
-#pragma unroll
-  for (int w = 0; w < MW; ++w) {
-    uint32_t tm = cm[w];
-    uint32_t keep = 0u;
-    const uint32_t n = __popc(tm);
-    if (take >= n) {
-      keep = tm;
-      take -= n;
-    } else {
-      while (take) {
-        keep |= tm & (0u - tm);
-        tm &= tm - 1u;
-        --take;
-      }
-    }
-    uint32_t wm = gtm[w] | keep;
-    while (wm) {
-      sh.win[pos++] = g0 + 32 * w + __ffs(wm) - 1;
-      wm &= wm - 1u;
-    }
-  }
-  __syncthreads();
-}
-
-__device__ __forceinline__ void st_s32x4(int32_t* p, int32_t a, int32_t b, int32_t c, int32_t d) {
-  asm volatile("st.global.v4.s32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ void st_s32x2(int32_t* p, int32_t a, int32_t b) {
-  asm volatile("st.global.v2.s32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
-}
-
-// A selected row's 2051 token ids: win[p] expands to out[4p + j] = 4*win[p] + j
-// (16-, 8- or 4-byte stores by the row's alignment), then the causal tail tokens
-// 4*nVis + j for j < tail, then -1.
-template <int T>
-__device__ __forceinline__ void write_selected(int32_t* out, const int32_t* win, int32_t tail, int32_t n_vis) {
-  const uint32_t a = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(out) >> 2) & 3u;  // out's offset in 16 B
-  for (int p = threadIdx.x; p < kTopK; p += T) {
-    const int32_t v = win[p] * kRatio;
-    int32_t* o = out + kRatio * p;
-    if (a == 0u) {
-      st_s32x4(o, v, v + 1, v + 2, v + 3);
-    } else if (a == 2u) {
-      st_s32x2(o, v, v + 1);
-      st_s32x2(o + 2, v + 2, v + 3);
-    } else {
-      o[0] = v;
-      st_s32x2(o + 1, v + 1, v + 2);
-      o[3] = v + 3;
-    }
-  }
-  if (threadIdx.x < kRatio - 1) {
-    const int j = threadIdx.x;
-    out[kRatio * kTopK + j] = j < tail ? kRatio * n_vis + j : -1;
-  }
-}
-
-// Rows whose selection needs no logits: padded rows (all -1) and rows with at most
-// 512 visible blocks (every block, ascending, then the tail).
-template <int T>
-__device__ __forceinline__ void write_unselected(int32_t* out, bool padded, int32_t n_vis, int32_t tail) {
-  const int32_t n_all = padded ? 0 : kRatio * n_vis + tail;  // token ids 0 .. n_all-1
-  for (int k = threadIdx.x; k < kWidth; k += T) out[k] = k < n_all ? k : -1;
 }
 
 struct RowInfo {

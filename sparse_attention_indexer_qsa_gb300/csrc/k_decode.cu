@@ -17,17 +17,10 @@
 //                dots per lane, then a lane tree), so equal to K2 within the logits
 //                tolerance, not bit for bit; relu, the ascending head sum and the
 //                scale as in K2.
-#include <cfloat>
-
-#include "qsa_common.cuh"
-#include "qsa_launch.h"
+#include "qsa_decode.cuh"
 
 namespace qsa {
 namespace dec {
-
-__device__ __forceinline__ void copy_tail(uint16_t* dst, const uint16_t* src, int lane) {
-  if (lane < 16) st_v4(dst + 8 * lane, ld_stream_v4(src + 8 * lane));  // 256 bytes, 16 B per lane
-}
 
 // grid (B), 3 warps: warp j handles the j-th token of the open block
 __global__ void raw_k_tail_kernel(const uint16_t* __restrict__ index_qk, const int32_t* __restrict__ ctx,
@@ -64,76 +57,30 @@ __global__ void __launch_bounds__(64) pre_decode_kernel(uint16_t* __restrict__ q
   const int32_t c = __ldg(ctx + b);
   const uint16_t* row = index_qk + static_cast<int64_t>(b) * kRowWidth;
   if (warp == 0) {
+    uint4 oa, ob;
+    q_heads<T>(row, cos_sin, c, g1q, eps, lane, oa, ob);
     uint16_t* dst = q_normed + static_cast<int64_t>(b) * (kNumQHeads * kHeadDim) + h * kHeadDim;
-    uint4 oa = make_uint4(0u, 0u, 0u, 0u), ob = oa;
-    if (c > 0) {  // block-uniform
-      const int32_t pos = c - 1;
-      float a[8], bv[8];
-      unpack8<T>(ld_stream_v4(row + h * kHeadDim + ca), a);
-      unpack8<T>(ld_stream_v4(row + h * kHeadDim + cb), bv);
-      RopeCS cs{};
-      if (j < 4) cs = load_rope(cos_sin + static_cast<int64_t>(pos) * kCsWidth, j);
-      norm_rope_group<T>(a, bv, g1q, eps, cs, j, oa, ob);
-    }
     st_v4(dst + ca, oa);
     st_v4(dst + cb, ob);
     return;
   }
   if (c <= 0) return;
-  const int32_t pos = c - 1;
   if (c % kRatio != 0) {
-    uint16_t* dst = pool_tail(pool, b, 0, pos);
+    uint16_t* dst = pool_tail(pool, b, 0, c - 1);
     if (dst != nullptr) copy_tail(dst, row + kKCol, lane);
     return;
   }
-  // block g = c/4 - 1 just completed: three K-tails plus the new row; every lane
-  // takes part in the group shuffles, lanes of group 0 hold the block
-  const int32_t g = c / kRatio - 1;
-  const uint16_t* k0 = pool_tail(pool, b, 0, kRatio * g);
-  const uint16_t* k1 = pool_tail(pool, b, 0, kRatio * g + 1);
-  const uint16_t* k2 = pool_tail(pool, b, 0, kRatio * g + 2);
-  uint16_t* out = pool_tail(pool, b, 1, kRatio * g);
-  const bool ok = k0 != nullptr && k1 != nullptr && k2 != nullptr && out != nullptr;  // block-uniform
-  float a[8], bv[8];
-  RopeCS cs{};
-  if (ok) {
-    const uint16_t* src[kRatio] = {k0, k1, k2, row + kKCol};
-    float fa[kRatio][8], fb[kRatio][8];
-#pragma unroll
-    for (int q = 0; q < kRatio; ++q) {
-      unpack8<T>(ld_cached_v4(src[q] + ca), fa[q]);
-      unpack8<T>(ld_cached_v4(src[q] + cb), fb[q]);
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float s = __fadd_rn(__fadd_rn(__fadd_rn(fa[0][e], fa[1][e]), fa[2][e]), fa[3][e]);
-      a[e] = T::round_trip(__fmul_rn(s, 0.25f));
-      s = __fadd_rn(__fadd_rn(__fadd_rn(fb[0][e], fb[1][e]), fb[2][e]), fb[3][e]);
-      bv[e] = T::round_trip(__fmul_rn(s, 0.25f));
-    }
-    if (j < 4) cs = load_rope(cos_sin + static_cast<int64_t>(kRatio) * g * kCsWidth, j);
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) { a[e] = 0.0f; bv[e] = 0.0f; }
-  }
   uint4 oa, ob;
-  norm_rope_group<T>(a, bv, g1k, eps, cs, j, oa, ob);
+  uint16_t* vtail = nullptr;
+  const bool ok = compress_block<T>(pool, b, c, row, cos_sin, g1k, eps, lane, oa, ob, &vtail);
   if (ok && h == 0) {
-    st_v4(out + ca, oa);
-    st_v4(out + cb, ob);
+    st_v4(vtail + ca, oa);
+    st_v4(vtail + cb, ob);
   }
 }
 
-// grid (B, ceilDiv(maxBlocks, kDecBlocksPerCta)), kDecThreads threads.  A 16-lane
-// half-warp scores one block at a time: lane c holds dims [8c, 8c+8) of the 4 q heads
-// in registers, reads the matching 16 bytes of the block's V-tail (the half-warp reads
-// the 256-byte row in one coalesced access), forms 4 partial dots, and the half-warp
-// reduces them (a reduce-scatter over lane bits 3 and 2, then bits 1 and 0), so that
-// lanes 0/4/8/12 hold heads 0/1/2/3; lane 0 sums relu of the heads in ascending order.
-constexpr int kDecThreads = 256;
-constexpr int kDecUnroll = 4;                                       // blocks in flight a half-warp
-constexpr int kDecBlocksPerCta = (kDecThreads / 16) * kDecUnroll * 2;  // two rounds
-
+// grid (B, ceilDiv(maxBlocks, kDecBlocksPerCta)), kDecThreads threads: score_range over
+// the CTA's blocks of the valid prefix.
 template <class T>
 __global__ void __launch_bounds__(kDecThreads) scores_decode_kernel(float* __restrict__ logits,
                                                                     const uint16_t* __restrict__ q_normed,
@@ -146,56 +93,11 @@ __global__ void __launch_bounds__(kDecThreads) scores_decode_kernel(float* __res
   const int32_t g_begin = blockIdx.y * kDecBlocksPerCta;
   if (g_begin >= n_vis) return;  // only the valid prefix is written
   const int32_t g_end = min(g_begin + kDecBlocksPerCta, n_vis);
-  const int lane = threadIdx.x & 31, ch = lane & 15, hw = threadIdx.x >> 4;
-  const unsigned half = lane & 16;
+  const uint16_t* q4 = q_normed + static_cast<int64_t>(b) * (kNumQHeads * kHeadDim) + 8 * (threadIdx.x & 15);
   float qf[kNumQHeads][8];
-  const uint16_t* q = q_normed + static_cast<int64_t>(b) * (kNumQHeads * kHeadDim) + 8 * ch;
 #pragma unroll
-  for (int h = 0; h < kNumQHeads; ++h) unpack8<T>(ld_cached_v4(q + h * kHeadDim), qf[h]);
-  float* out = logits + static_cast<int64_t>(b) * max_blocks;
-  const bool keep_hi = (ch & 8) != 0, keep_odd = (ch & 4) != 0;
-#pragma unroll 1
-  for (int32_t base = g_begin; base < g_end; base += 16 * kDecUnroll) {  // warp-uniform: shuffles below
-    const int32_t g0 = base + hw;
-    uint4 raw[kDecUnroll];
-    bool ok[kDecUnroll];
-#pragma unroll
-    for (int u = 0; u < kDecUnroll; ++u) {
-      const int32_t g = g0 + 16 * u;
-      const uint16_t* k = g < g_end ? pool_tail(pool, b, 1, kRatio * g) : nullptr;
-      ok[u] = k != nullptr;
-      raw[u] = ok[u] ? ld_stream_v4(k + 8 * ch) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < kDecUnroll; ++u) {
-      float kf[8];
-      unpack8<T>(raw[u], kf);
-      float d[kNumQHeads];
-#pragma unroll
-      for (int h = 0; h < kNumQHeads; ++h) {
-        float acc = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
-        d[h] = acc;
-      }
-      // lane bit 3: keep heads {2,3} or {0,1}; send the other pair to the partner
-      const float s0 = keep_hi ? d[0] : d[2], s1 = keep_hi ? d[1] : d[3];
-      const float r0 = __shfl_xor_sync(0xffffffffu, s0, 8), r1 = __shfl_xor_sync(0xffffffffu, s1, 8);
-      const float e0 = (keep_hi ? d[2] : d[0]) + r0, e1 = (keep_hi ? d[3] : d[1]) + r1;
-      // lane bit 2: keep the pair's second or first head
-      const float r2 = __shfl_xor_sync(0xffffffffu, keep_odd ? e0 : e1, 4);
-      float f = (keep_odd ? e1 : e0) + r2;
-      f += __shfl_xor_sync(0xffffffffu, f, 2);
-      f += __shfl_xor_sync(0xffffffffu, f, 1);
-      const float rel = fmaxf(0.0f, f);  // head ((ch >> 3) & 1) * 2 + ((ch >> 2) & 1)
-      const float h1 = __shfl_sync(0xffffffffu, rel, half | 4);
-      const float h2 = __shfl_sync(0xffffffffu, rel, half | 8);
-      const float h3 = __shfl_sync(0xffffffffu, rel, half | 12);
-      const int32_t g = g0 + 16 * u;
-      if (ch == 0 && g < g_end) out[g] = ok[u] ? __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(rel, h1), h2), h3), scale)
-                                              : -FLT_MAX;
-    }
-  }
+  for (int h = 0; h < kNumQHeads; ++h) unpack8<T>(ld_cached_v4(q4 + h * kHeadDim), qf[h]);  // global memory
+  score_range<T>(logits + static_cast<int64_t>(b) * max_blocks, qf, pool, b, g_begin, g_end, scale, -1, nullptr);
 }
 
 }  // namespace dec

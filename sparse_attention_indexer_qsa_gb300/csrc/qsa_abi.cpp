@@ -411,6 +411,35 @@ QSA_API int qsa_topk_expand_decode(int32_t* outIdx, const float* logits, const i
                                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
+QSA_API int qsa_indexer_decode_step(qsa_dtype_t dtype, int32_t* outIdx, float* logits, void* qNormed,
+                                    const void* indexQk, const float* cosSin, const int32_t* contextLengths,
+                                    const void* wQ, const void* wK, float rmsEps, const qsa_pool_state_t* pool,
+                                    int32_t* splitCounters, int32_t numKVHeads, int32_t batchSize,
+                                    int32_t maxBlocks, qsa_stream_t stream) {
+  static const char* fn = "qsa_indexer_decode_step";
+  int st;
+  if ((st = check_dtype(fn, dtype)) != QSA_OK) return st;
+  if (!outIdx || !logits || !qNormed || !indexQk || !cosSin || !contextLengths || !wQ || !wK)
+    return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  qsa::PoolDev pd;
+  if ((st = validate_pool(fn, pool, &pd)) != QSA_OK) return st;
+  if (batchSize < 1 || batchSize > qsa::decode_step_max_batch())
+    return fail(QSA_E_SHAPE, "%s: batchSize=%d must be in [1, %d]", fn, batchSize, qsa::decode_step_max_batch());
+  if (maxBlocks < 1 || maxBlocks > qsa::topk_max_blocks())
+    return fail(QSA_E_SHAPE, "%s: maxBlocks=%d must be in [1, %d]", fn, maxBlocks, qsa::topk_max_blocks());
+  if (splitCounters && numKVHeads < 0) return fail(QSA_E_SHAPE, "%s: numKVHeads=%d must be >= 0", fn, numKVHeads);
+  if (!aligned(qNormed, 16) || !aligned(indexQk, 16) || !aligned(cosSin, 16) || !aligned(wQ, 16) ||
+      !aligned(wK, 16) || !aligned(contextLengths, 4) || !aligned(logits, 4) || !aligned(outIdx, 4) ||
+      !aligned(splitCounters, 4))
+    return fail(QSA_E_ALIGN, "%s: T and cosSin arrays must be 16-byte aligned, the others 4-byte", fn);
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  return launched(fn, qsa::launch_decode_step(dtype == QSA_BF16, outIdx, logits, qNormed, indexQk, cosSin,
+                                              contextLengths, wQ, wK, rmsEps, pd, splitCounters,
+                                              splitCounters ? numKVHeads : 0, batchSize, maxBlocks, score_scale(),
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 QSA_API int qsa_testing_index_scores_cuda_core(qsa_dtype_t dtype, float* logits, const void* qNormed,
                                                const void* kbar, const int32_t* contextLengths,
                                                int32_t batchSize, int32_t seqLen, int32_t numBlocks,

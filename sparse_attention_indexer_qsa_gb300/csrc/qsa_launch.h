@@ -126,6 +126,13 @@ cudaError_t launch_topk_expand_decode(int32_t* out_idx, const float* logits, con
                                       int32_t* split_counters, int32_t num_kv_heads, int32_t batch,
                                       int32_t max_blocks, cudaStream_t stream);
 
+// The decode step fused into one launch (k_decode_step.cu); batch <= decode_step_max_batch().
+cudaError_t launch_decode_step(bool bf16, int32_t* out_idx, float* logits, void* q_normed, const void* index_qk,
+                               const float* cos_sin, const int32_t* ctx, const void* w_q, const void* w_k,
+                               float eps, const PoolDev& pool, int32_t* split_counters, int32_t num_kv_heads,
+                               int32_t batch, int32_t max_blocks, float scale, cudaStream_t stream);
+int32_t decode_step_max_batch();
+
 // Device fault flags: bits set by bounded waits that ran out (k2_scores_tc.cu, k1_stream.cu).
 cudaError_t read_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
 cudaError_t read_k1_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);

@@ -190,3 +190,78 @@ def test_decode_validation_rejects_bad_pools():
     with pytest.raises(qsa.QsaError) as e:
         qsa.qsa_raw_k_tail_write_prefill(P, P, null, 2, 8, stream=0, dtype="bf16")
     assert e.value.status == -1
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_fused_decode_step_bit_identical_to_three_calls(dtype):
+    """qsa_indexer_decode_step against qsa_indexer_pre_decode + qsa_index_scores_decode +
+    qsa_topk_expand_decode on two copies of one prefilled pool, token by token: q, the
+    logits prefix, outIdx, the split counters and both pools stay bit-identical.  One
+    sequence has an unusable K page (its block compress is skipped), one runs past its
+    length (ctx 0), and nVis crosses 512 and a 128-block CTA edge."""
+    qsa, g_ = _qsa(), _gu()
+    B = 4
+    total = [2150, 2060, 700, 520]
+    prefill = [2040, 2046, 640, 300]
+    S = max(total)
+    wl = workloads.custom(B, S, total, dtype=dtype, seed=71, nan_padding=True, max_positions=S)
+    d = g_.DevWorkload(wl)
+    NB = (S + 3) // 4
+    maxb = NB + 7
+    unused = ((2, 0, 5),)                           # sequence 2: K page of tokens 640..767 unusable
+    pools = [DevPool(pool_util.make_pool(B, S, seed=12, unused_slots=unused)) for _ in range(2)]
+    pctx = g_.dev(np.array(prefill, np.int32))
+    kb = torch.empty((B, NB, 128), dtype=torch.int16, device="cuda")
+    for dp in pools:
+        qsa.qsa_index_k_compress_paged(kb, d.index_qk, d.cos_sin, pctx, d.w_k, wl.eps, dp.state, B, S, NB, 0, NB,
+                                       0, dtype=dtype)
+        qsa.qsa_raw_k_tail_write_prefill(d.index_qk, pctx, dp.state, B, S, dtype=dtype)
+
+    def bufs():
+        return dict(q=torch.empty((B, 1, 4, 128), dtype=torch.int16, device="cuda"),
+                    logits=torch.full((B, maxb), float("nan"), device="cuda"),
+                    out=torch.empty((B, 2051), dtype=torch.int32, device="cuda"),
+                    split=torch.full((B, 3), 9, dtype=torch.int32, device="cuda"))
+    three, fused = bufs(), bufs()
+    for step in range(max(t - p for t, p in zip(total, prefill))):
+        pos = [p + step for p in prefill]
+        ctx = np.array([ps + 1 if ps < t else 0 for ps, t in zip(pos, total)], np.int32)
+        rows = np.stack([wl.index_qk[b, min(pos[b], S - 1)] for b in range(B)])
+        d_rows, d_ctx = g_.dev(rows), g_.dev(ctx)
+        st0, st1 = pools[0].state, pools[1].state
+        three["logits"].fill_(float("nan"))
+        fused["logits"].fill_(float("nan"))
+        qsa.qsa_indexer_pre_decode(three["q"], d_rows, d.cos_sin, d_ctx, d.w_q, d.w_k, wl.eps, st0, B, dtype=dtype)
+        qsa.qsa_index_scores_decode(three["logits"], three["q"], d_ctx, st0, B, maxb, dtype=dtype)
+        qsa.qsa_topk_expand_decode(three["out"], three["logits"], d_ctx, three["split"], 3, B, maxb)
+        qsa.qsa_indexer_decode_step(fused["out"], fused["logits"], fused["q"], d_rows, d.cos_sin, d_ctx, d.w_q,
+                                    d.w_k, wl.eps, st1, fused["split"], 3, B, maxb, dtype=dtype)
+        torch.cuda.synchronize()
+        for name in ("q", "out", "split"):
+            assert torch.equal(three[name], fused[name]), (step, name)
+        for b in range(B):
+            nv = int(ctx[b]) // 4
+            assert torch.equal(three["logits"][b, :nv].view(torch.int32), fused["logits"][b, :nv].view(torch.int32))
+            assert torch.isnan(fused["logits"][b, nv:]).all(), (step, b)    # only the valid prefix
+        assert not fused["split"].any()
+        three["split"].fill_(9)
+        fused["split"].fill_(9)
+        if step % 16 == 0 or step in (53, 60, 61):
+            assert np.array_equal(pools[0].numpy(), pools[1].numpy()), step
+    assert np.array_equal(pools[0].numpy(), pools[1].numpy())
+    assert qsa.qsa_device_fault_flags() == 0
+
+
+def test_fused_decode_step_validation():
+    qsa = _qsa()
+    P = 0x1000
+    ok = qsa.PoolState(P, P, 4, 8, 2, 384, 256)
+    with pytest.raises(qsa.QsaError) as e:
+        qsa.qsa_indexer_decode_step(P, P, P, P, P, P, P, P, 1e-6, ok, 0, 2, 4097, 16, stream=0, dtype="bf16")
+    assert e.value.status == -2                                       # batch above the counter set
+    with pytest.raises(qsa.QsaError) as e:
+        qsa.qsa_indexer_decode_step(P, P, P, P, P, P, P, P, 1e-6, ok, 0, 2, 4, 65537, stream=0, dtype="bf16")
+    assert e.value.status == -2
+    with pytest.raises(qsa.QsaError) as e:
+        qsa.qsa_indexer_decode_step(P, P, P + 2, P, P, P, P, P, 1e-6, ok, 0, 2, 4, 16, stream=0, dtype="bf16")
+    assert e.value.status == -5
