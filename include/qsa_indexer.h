@@ -379,7 +379,8 @@ int qsa_index_scores_no_alloc(qsa_dtype_t dtype, float* logits, const void* qNor
 /*
  * Device-side fault flags.  Kernels that wait on their own asynchronous copies
  * bound every wait (about two seconds); a wait that runs out sets a bit here
- * (bits 0-3: scoring kernel, bits 8-11: staged q-prep kernels)
+ * (bits 0-3: scoring kernel, bits 8-11: staged q-prep kernels, bits 16-19: paged
+ * decode scores, bits 20-23: the one-launch decode step)
  * instead of hanging, the kernel drains and returns, and the outputs of that
  * launch are undefined.  This call synchronises `stream`, copies the flags of
  * the current device into *flags (0 = no fault since the last clear) and clears

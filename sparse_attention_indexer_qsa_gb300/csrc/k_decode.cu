@@ -13,13 +13,19 @@
 //                prefill K1b) and written to the V-tail of 4g.
 //   scores_decode  K2's scoring at S = 1 over the V-tails: logits[b][g] for
 //                g < ctx/4 only; a block whose page slot is unusable scores -FLT_MAX.
-//                FP32 dot products in another order than K2's (eight-term partial
-//                dots per lane, then a lane tree), so equal to K2 within the logits
-//                tolerance, not bit for bit; relu, the ascending head sum and the
-//                scale as in K2.
+//                On the tensor cores (qsa_decode_tc.cuh): the dots are formed as in
+//                K2, then relu, the ascending head sum and the scale as in K2.
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
 #include "qsa_decode.cuh"
+#include "qsa_decode_tc.cuh"
 
 namespace qsa {
+
+__device__ uint32_t g_dec_fault_flags;
+
 namespace dec {
 
 // grid (B), 3 warps: warp j handles the j-th token of the open block
@@ -79,25 +85,40 @@ __global__ void __launch_bounds__(64) pre_decode_kernel(uint16_t* __restrict__ q
   }
 }
 
-// grid (B, ceilDiv(maxBlocks, kDecBlocksPerCta)), kDecThreads threads: score_range over
-// the CTA's blocks of the valid prefix.
-template <class T>
-__global__ void __launch_bounds__(kDecThreads) scores_decode_kernel(float* __restrict__ logits,
-                                                                    const uint16_t* __restrict__ q_normed,
-                                                                    const int32_t* __restrict__ ctx,
-                                                                    const PoolDev pool, int32_t max_blocks,
-                                                                    float scale) {
+constexpr int kScoresThreads = 32 * dtc::kEngineWarps;
+constexpr uint32_t kScoresSmem = dtc::kEngineBytes + 1024;  // + slack to align the base to 1024
+
+// grid (B, ceilDiv(maxBlocks, run)), kScoresThreads threads: the tensor-core engine
+// over the CTA's run of blocks of the valid prefix, q read from qNormed.
+template <bool kBf16>
+__global__ void __launch_bounds__(kScoresThreads, kScoresCtasPerSm)
+    scores_decode_kernel(const __grid_constant__ CUtensorMap pool_map, float* __restrict__ logits,
+                         const uint16_t* __restrict__ q_normed, const int32_t* __restrict__ ctx,
+                         const PoolDev pool, int32_t max_blocks, float scale, int32_t run) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ int32_t vpages[kPageWindow];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const dtc::Engine en{base, smem_raw + (base - raw), &g_dec_fault_flags};
   const int32_t b = blockIdx.x;
   const int32_t c = __ldg(ctx + b);
   const int32_t n_vis = c > 0 ? min(c / kRatio, max_blocks) : 0;
-  const int32_t g_begin = blockIdx.y * kDecBlocksPerCta;
-  if (g_begin >= n_vis) return;  // only the valid prefix is written
-  const int32_t g_end = min(g_begin + kDecBlocksPerCta, n_vis);
-  const uint16_t* q4 = q_normed + static_cast<int64_t>(b) * (kNumQHeads * kHeadDim) + 8 * (threadIdx.x & 15);
-  float qf[kNumQHeads][8];
-#pragma unroll
-  for (int h = 0; h < kNumQHeads; ++h) unpack8<T>(ld_cached_v4(q4 + h * kHeadDim), qf[h]);  // global memory
-  score_range<T>(logits + static_cast<int64_t>(b) * max_blocks, qf, pool, b, g_begin, g_end, scale, -1, nullptr);
+  const int32_t g_begin = blockIdx.y * run;
+  if (g_begin >= n_vis) return;  // only the valid prefix is written (the whole CTA leaves)
+  const int32_t g_end = min(g_begin + run, n_vis);
+  const int tid = threadIdx.x;
+  stage_vpages(vpages, pool, b, g_begin, g_end);
+  if (tid < kNumQHeads * 16) {
+    const int h = tid >> 4, ch = tid & 15;
+    dtc::put_q_chunk(en, h, ch,
+                     ld_cached_v4(q_normed + static_cast<int64_t>(b) * (kNumQHeads * kHeadDim) + h * kHeadDim + 8 * ch));
+  }
+  dtc::zero_b_padding(en, tid, kScoresThreads);
+  ptx::fence_proxy_async_shared();
+  const uint32_t tmem = dtc::engine_setup(en, &pool_map);
+  dtc::engine_run<kBf16>(en, tmem, &pool_map, vpages, pool.head_size, g_begin, g_end,
+                         logits + static_cast<int64_t>(b) * max_blocks, scale);
+  dtc::engine_teardown(tmem);
 }
 
 }  // namespace dec
@@ -125,14 +146,48 @@ cudaError_t launch_pre_decode(bool bf16, void* q_normed, const void* index_qk, c
 cudaError_t launch_scores_decode(bool bf16, float* logits, const void* q_normed, const int32_t* ctx,
                                  const PoolDev& pool, int32_t batch, int32_t max_blocks, float scale,
                                  cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>(batch),
-                  static_cast<unsigned>((max_blocks + dec::kDecBlocksPerCta - 1) / dec::kDecBlocksPerCta));
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  {
+    static std::mutex mu;
+    static bool attr_set[64][2] = {};
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev][bf16 ? 1 : 0]) {
+      e = bf16 ? cudaFuncSetAttribute(dec::scores_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(dec::kScoresSmem))
+               : cudaFuncSetAttribute(dec::scores_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(dec::kScoresSmem));
+      if (e != cudaSuccess) return e;
+      attr_set[dev][bf16 ? 1 : 0] = true;
+    }
+  }
+  CUtensorMap map;
+  if ((e = encode_vtail_map(&map, pool)) != cudaSuccess) return e;
+  const int32_t run = dec::decode_run_blocks(sms, dec::kScoresCtasPerSm, batch, max_blocks);
+  const dim3 grid(static_cast<unsigned>(batch), static_cast<unsigned>((max_blocks + run - 1) / run));
   auto* q = static_cast<const uint16_t*>(q_normed);
   if (bf16)
-    dec::scores_decode_kernel<Bf16><<<grid, dec::kDecThreads, 0, stream>>>(logits, q, ctx, pool, max_blocks, scale);
+    dec::scores_decode_kernel<true>
+        <<<grid, dec::kScoresThreads, dec::kScoresSmem, stream>>>(map, logits, q, ctx, pool, max_blocks, scale, run);
   else
-    dec::scores_decode_kernel<F16><<<grid, dec::kDecThreads, 0, stream>>>(logits, q, ctx, pool, max_blocks, scale);
+    dec::scores_decode_kernel<false>
+        <<<grid, dec::kScoresThreads, dec::kScoresSmem, stream>>>(map, logits, q, ctx, pool, max_blocks, scale, run);
   return cudaGetLastError();
+}
+
+cudaError_t read_dec_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(flags, g_dec_fault_flags, sizeof(uint32_t), 0,
+                                            cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess && clear) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_dec_fault_flags, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  }
+  return e;
 }
 
 }  // namespace qsa

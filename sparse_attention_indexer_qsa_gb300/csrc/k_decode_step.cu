@@ -1,17 +1,18 @@
 // The whole decode step in one launch ("Qsa Indexer Kernels": launchQsaIndexerPreDecode,
 // launchQsaIndexScoresDecode and launchQsaTopKExpandDecode, in that order, fused).
 //
-// grid (B, Y), kDecThreads threads; CTA (b, y) covers blocks [y * perCta, (y + 1) * perCta),
-// perCta a multiple of kDecBlocksPerCta chosen so that the grid is about one wave.  CTA (b, y):
-//   - warp 0 computes sequence b's q heads into shared memory (CTA y = 0 also writes
-//     qNormed[b]); warp 1 either writes the new token's raw K-tail (CTA y = 0), or, in
-//     the CTA whose blocks include the just-completed block g, compresses g (the
-//     pre-decode routines) into shared memory and the pool's V-tail;
-//   - the CTA scores its blocks of the valid prefix, kDecBlocksPerCta at a time (the
-//     paged-scores routine; block g is read from shared memory), into logits[b];
+// grid (B, Y), kDecThreads threads; CTA (b, y) covers the run of blocks [y * perCta,
+// (y + 1) * perCta), perCta chosen so that the grid is about one wave.  CTA (b, y):
+//   - warp 0 computes sequence b's q heads straight into the tensor-core B operand
+//     (CTA y = 0 also writes qNormed[b]); warp 1 either writes the new token's raw
+//     K-tail (CTA y = 0), or, in the CTA whose run holds the just-completed block g,
+//     compresses g (the pre-decode routines) into the pool's V-tail;
+//   - the tensor-core paged-scores engine scores the run's blocks of the valid prefix
+//     (the owning CTA's TMA copies read block g's fresh V-tail) into logits[b];
 //   - the last CTA of sequence b to finish (a per-sequence arrival counter, no waiting)
 //     runs the top-512 selection of row b on the logits at L2, writes outIdx[b], zeroes
-//     b's split counters and puts the counter back to zero.
+//     b's split counters and puts the counter back to zero.  Its shared memory for the
+//     selection reuses the engine's operand stages.
 // Every value equals the one the three separate kernels give: the same device routines
 // compute it.  Arrival counters: kStepSlots sets of kStepMaxBatch, one set a launch in
 // turn (so up to kStepSlots launches may run at once on a device), zero at module load
@@ -19,33 +20,43 @@
 #include <algorithm>
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "qsa_decode.cuh"
+#include "qsa_decode_tc.cuh"
 #include "qsa_select.cuh"
 
 namespace qsa {
 
 constexpr int kStepSlots = 16;
 constexpr int kStepMaxBatch = 4096;
-constexpr int kStepCtasPerSm = 3;  // the resident CTAs of decode_step_kernel an SM is sized for
+constexpr int kStepCtasPerSm = 2;  // the resident CTAs of decode_step_kernel an SM is sized for
 __device__ __align__(256) uint32_t g_decode_step_arrivals[kStepSlots * kStepMaxBatch];
+__device__ uint32_t g_step_fault_flags;
 
 namespace dec {
 
+constexpr uint32_t kStepSmem = dtc::kEngineBytes + 1024;  // + slack to align the base to 1024
+static_assert(sizeof(sel::SelShared<kDecThreads>) <= dtc::kStages * dtc::kABytes,
+              "the selection's shared memory reuses the engine's A stages");
+
 template <class T, int MW>
 __global__ void __launch_bounds__(kDecThreads, kStepCtasPerSm)
-decode_step_kernel(int32_t* __restrict__ out_idx, float* __restrict__ logits, uint16_t* __restrict__ q_normed,
+decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __restrict__ out_idx,
+                   float* __restrict__ logits, uint16_t* __restrict__ q_normed,
                    const uint16_t* __restrict__ index_qk, const float* __restrict__ cos_sin,
                    const int32_t* __restrict__ ctx, const uint16_t* __restrict__ w_q,
                    const uint16_t* __restrict__ w_k, float eps, const PoolDev pool,
                    int32_t* __restrict__ split_counters, int32_t num_kv_heads, int32_t max_blocks, float scale,
                    int32_t per_cta, uint32_t* __restrict__ arrivals) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(16) float g1q[kHeadDim];
   __shared__ __align__(16) float g1k[kHeadDim];
-  __shared__ __align__(16) uint16_t q4[kNumQHeads * kHeadDim];
-  __shared__ __align__(16) uint16_t kbar_new[kHeadDim];
-  __shared__ __align__(16) sel::SelShared<kDecThreads> sh;
-  __shared__ int32_t own_block;  // block scored from kbar_new, or -1
+  __shared__ int32_t vpages[kPageWindow];
   __shared__ int32_t last;
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const dtc::Engine en{base, smem_raw + (base - raw), &g_step_fault_flags};
   const int32_t b = blockIdx.x, y = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t c = __ldg(ctx + b);
@@ -54,7 +65,8 @@ decode_step_kernel(int32_t* __restrict__ out_idx, float* __restrict__ logits, ui
   const int32_t g_end = min(g_begin + per_cta, n_vis);
   stage_gamma<T>(w_q, g1q);
   stage_gamma<T>(w_k, g1k);
-  if (tid == 0) own_block = -1;
+  stage_vpages(vpages, pool, b, g_begin, g_end);
+  dtc::zero_b_padding(en, tid, kDecThreads);
   __syncthreads();
   const uint16_t* row = index_qk + static_cast<int64_t>(b) * kRowWidth;
   const int h = lane >> 3, j = lane & 7;
@@ -62,8 +74,8 @@ decode_step_kernel(int32_t* __restrict__ out_idx, float* __restrict__ logits, ui
   if (warp == 0) {
     uint4 oa, ob;
     q_heads<T>(row, cos_sin, c, g1q, eps, lane, oa, ob);
-    *reinterpret_cast<uint4*>(q4 + h * kHeadDim + ca) = oa;
-    *reinterpret_cast<uint4*>(q4 + h * kHeadDim + cb) = ob;
+    dtc::put_q_chunk(en, h, ca / 8, oa);
+    dtc::put_q_chunk(en, h, cb / 8, ob);
     if (y == 0) {
       uint16_t* dst = q_normed + static_cast<int64_t>(b) * (kNumQHeads * kHeadDim) + h * kHeadDim;
       st_v4(dst + ca, oa);
@@ -82,25 +94,18 @@ decode_step_kernel(int32_t* __restrict__ out_idx, float* __restrict__ logits, ui
       if (ok && h == 0) {
         st_v4(vtail + ca, oa);
         st_v4(vtail + cb, ob);
-        *reinterpret_cast<uint4*>(kbar_new + ca) = oa;
-        *reinterpret_cast<uint4*>(kbar_new + cb) = ob;
       }
-      if (ok && lane == 0) own_block = c / kRatio - 1;
+      ptx::fence_proxy_async_global();  // the V-tail, before this CTA's TMA copies read it
     }
   }
-  __syncthreads();
+  ptx::fence_proxy_async_shared();  // the B operand, before the MMAs read it
+  const uint32_t tmem = dtc::engine_setup(en, &pool_map);
+  if (tid == 0) ptx::fence_proxy_async_global();
   float* lrow = logits + static_cast<int64_t>(b) * max_blocks;
-  if (g_begin < g_end) {
-    float qf[kNumQHeads][8];
-#pragma unroll
-    for (int h = 0; h < kNumQHeads; ++h)  // shared memory: a plain (generic) load
-      unpack8<T>(*reinterpret_cast<const uint4*>(q4 + h * kHeadDim + 8 * (tid & 15)), qf[h]);
-    for (int32_t g0 = g_begin; g0 < g_end; g0 += kDecBlocksPerCta)
-      score_range<T>(lrow, qf, pool, b, g0, min(g0 + kDecBlocksPerCta, g_end), scale, own_block, kbar_new);
-  }
+  dtc::engine_run<T::kIsBf16>(en, tmem, &pool_map, vpages, pool.head_size, g_begin, g_end, lrow, scale);
+  dtc::engine_teardown(tmem);
 
   // ---- the last CTA of sequence b selects its row
-  __syncthreads();
   if (tid == 0) {
     __threadfence();  // this CTA's logits, before its arrival
     last = atomicAdd(arrivals + b, 1u) == gridDim.y - 1 ? 1 : 0;
@@ -117,6 +122,7 @@ decode_step_kernel(int32_t* __restrict__ out_idx, float* __restrict__ logits, ui
     sel::write_unselected<kDecThreads>(out, c <= 0, n_vis, tail);
     return;
   }
+  sel::SelShared<kDecThreads>& sh = *reinterpret_cast<sel::SelShared<kDecThreads>*>(en.ptr + dtc::kOffA);
   const sel::L2Keys keys{lrow, (reinterpret_cast<uintptr_t>(lrow) & 15u) == 0};
   sel::select_row<kDecThreads, MW>(keys, n_vis, sh);
   sel::write_selected<kDecThreads>(out, sh.win, tail, n_vis);
@@ -150,24 +156,45 @@ cudaError_t launch_decode_step(bool bf16, int32_t* out_idx, float* logits, void*
     }
     arrivals = g_step_base[dev] + static_cast<int64_t>(g_step_seq[dev]++ % kStepSlots) * kStepMaxBatch;
   }
-  // Y CTAs a sequence, each over per_cta (a multiple of kDecBlocksPerCta) blocks: about one
-  // wave of resident CTAs over the batch, so that each CTA computes the q heads once
+  // Y CTAs a sequence, each over a run of per_cta blocks: about one wave of resident CTAs
+  // over the batch, so that each CTA computes the q heads once
   int sms = 0;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int32_t chunks = (max_blocks + dec::kDecBlocksPerCta - 1) / dec::kDecBlocksPerCta;
-  const int32_t want_y = std::max<int32_t>(1, sms * kStepCtasPerSm / std::max<int32_t>(batch, 1));
-  const int32_t per_chunks = (chunks + want_y - 1) / want_y;
-  const int32_t per_cta = std::max<int32_t>(1, per_chunks) * dec::kDecBlocksPerCta;
+  const int32_t per_cta = dec::decode_run_blocks(sms, kStepCtasPerSm, batch, max_blocks);
   const dim3 grid(static_cast<unsigned>(batch), static_cast<unsigned>((max_blocks + per_cta - 1) / per_cta));
   const int32_t words = (max_blocks + dec::kDecThreads * 32 - 1) / (dec::kDecThreads * 32);
+  const int mw_index = words <= 1 ? 0 : words <= 2 ? 1 : words <= 4 ? 2 : 3;
+  {
+    static std::mutex mu;
+    static bool attr_set[64][2][4] = {};
+    std::lock_guard<std::mutex> lk(mu);
+    bool& done = attr_set[dev][bf16 ? 1 : 0][mw_index];
+    if (!done) {
+      const void* fns[2][4] = {
+          {reinterpret_cast<const void*>(dec::decode_step_kernel<F16, 1>),
+           reinterpret_cast<const void*>(dec::decode_step_kernel<F16, 2>),
+           reinterpret_cast<const void*>(dec::decode_step_kernel<F16, 4>),
+           reinterpret_cast<const void*>(dec::decode_step_kernel<F16, 8>)},
+          {reinterpret_cast<const void*>(dec::decode_step_kernel<Bf16, 1>),
+           reinterpret_cast<const void*>(dec::decode_step_kernel<Bf16, 2>),
+           reinterpret_cast<const void*>(dec::decode_step_kernel<Bf16, 4>),
+           reinterpret_cast<const void*>(dec::decode_step_kernel<Bf16, 8>)}};
+      e = cudaFuncSetAttribute(fns[bf16 ? 1 : 0][mw_index], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(dec::kStepSmem));
+      if (e != cudaSuccess) return e;
+      done = true;
+    }
+  }
+  CUtensorMap map;
+  if ((e = encode_vtail_map(&map, pool)) != cudaSuccess) return e;
   auto* q = static_cast<uint16_t*>(q_normed);
   auto* iq = static_cast<const uint16_t*>(index_qk);
   auto* wq = static_cast<const uint16_t*>(w_q);
   auto* wk = static_cast<const uint16_t*>(w_k);
 #define QSA_STEP_LAUNCH(T, MW)                                                                             \
-  dec::decode_step_kernel<T, MW><<<grid, dec::kDecThreads, 0, stream>>>(                                   \
-      out_idx, logits, q, iq, cos_sin, ctx, wq, wk, eps, pool, split_counters, num_kv_heads, max_blocks, scale, \
-      per_cta, arrivals)
+  dec::decode_step_kernel<T, MW><<<grid, dec::kDecThreads, dec::kStepSmem, stream>>>(                     \
+      map, out_idx, logits, q, iq, cos_sin, ctx, wq, wk, eps, pool, split_counters, num_kv_heads, max_blocks,     \
+      scale, per_cta, arrivals)
 #define QSA_STEP_DISPATCH(T)                 \
   do {                                       \
     if (words <= 1) QSA_STEP_LAUNCH(T, 1);   \
@@ -180,6 +207,18 @@ cudaError_t launch_decode_step(bool bf16, int32_t* out_idx, float* logits, void*
 #undef QSA_STEP_DISPATCH
 #undef QSA_STEP_LAUNCH
   return cudaGetLastError();
+}
+
+cudaError_t read_step_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(flags, g_step_fault_flags, sizeof(uint32_t), 0,
+                                            cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess && clear) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_step_fault_flags, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  }
+  return e;
 }
 
 }  // namespace qsa

@@ -467,11 +467,14 @@ QSA_API int qsa_device_fault_flags(uint32_t* flags, int clear, qsa_stream_t stre
   DeviceInfo d;
   int st = current_device(fn, &d);
   if (st != QSA_OK) return st;
-  uint32_t k2 = 0, k1 = 0;
-  cudaError_t e = qsa::read_fault_flags(&k2, clear != 0, reinterpret_cast<cudaStream_t>(stream));
-  if (e == cudaSuccess) e = qsa::read_k1_fault_flags(&k1, clear != 0, reinterpret_cast<cudaStream_t>(stream));
+  uint32_t k2 = 0, k1 = 0, dec = 0, step = 0;
+  const auto cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = qsa::read_fault_flags(&k2, clear != 0, cs);
+  if (e == cudaSuccess) e = qsa::read_k1_fault_flags(&k1, clear != 0, cs);
+  if (e == cudaSuccess) e = qsa::read_dec_fault_flags(&dec, clear != 0, cs);
+  if (e == cudaSuccess) e = qsa::read_step_fault_flags(&step, clear != 0, cs);
   if (e != cudaSuccess) return fail(QSA_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
-  *flags = k2 | (k1 << 8);
+  *flags = k2 | (k1 << 8) | (dec << 16) | (step << 20);
   g_last_error[0] = '\0';
   return QSA_OK;
 }

@@ -21,6 +21,7 @@ constexpr int kCsWidth = 64;
 // ---------------------------------------------------------------- element types
 
 struct Bf16 {
+  static constexpr bool kIsBf16 = true;
   static __device__ __forceinline__ float one(uint16_t u) { return __uint_as_float(static_cast<uint32_t>(u) << 16); }
   static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
   static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -34,6 +35,7 @@ struct Bf16 {
 };
 
 struct F16 {
+  static constexpr bool kIsBf16 = false;
   static __device__ __forceinline__ float one(uint16_t u) { return __half2float(__ushort_as_half(u)); }
   static __device__ __forceinline__ float lo(uint32_t w) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));

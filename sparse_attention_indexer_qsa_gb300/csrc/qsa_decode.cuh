@@ -77,97 +77,42 @@ __device__ __forceinline__ bool compress_block(const PoolDev& pool, int32_t b, i
   return ok;
 }
 
-// Paged scores.  A 16-lane half-warp scores one block: lane ch holds dims [8ch, 8ch+8)
-// of the 4 q heads (qf) and 16 bytes of the block's kbar (raw), forms 4 partial dots,
-// and the half-warp reduces them (a reduce-scatter over lane bits 3 and 2, then bits 1
-// and 0), so that lanes 0/4/8/12 hold heads 0/1/2/3.  Returns, on lane ch == 0, the sum
-// of relu of the heads in ascending order (before the scale).  Every lane of the warp
-// must call it.
-template <class T>
-__device__ __forceinline__ float score_block(const float (&qf)[kNumQHeads][8], uint4 raw, int ch) {
-  const unsigned half = threadIdx.x & 16;
-  const bool keep_hi = (ch & 8) != 0, keep_odd = (ch & 4) != 0;
-  float kf[8];
-  unpack8<T>(raw, kf);
-  float d[kNumQHeads];
-#pragma unroll
-  for (int h = 0; h < kNumQHeads; ++h) {
-    float acc = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
-    d[h] = acc;
-  }
-  // lane bit 3: keep heads {2,3} or {0,1}; send the other pair to the partner
-  const float s0 = keep_hi ? d[0] : d[2], s1 = keep_hi ? d[1] : d[3];
-  const float r0 = __shfl_xor_sync(0xffffffffu, s0, 8), r1 = __shfl_xor_sync(0xffffffffu, s1, 8);
-  const float e0 = (keep_hi ? d[2] : d[0]) + r0, e1 = (keep_hi ? d[3] : d[1]) + r1;
-  // lane bit 2: keep the pair's second or first head
-  const float r2 = __shfl_xor_sync(0xffffffffu, keep_odd ? e0 : e1, 4);
-  float f = (keep_odd ? e1 : e0) + r2;
-  f += __shfl_xor_sync(0xffffffffu, f, 2);
-  f += __shfl_xor_sync(0xffffffffu, f, 1);
-  const float rel = fmaxf(0.0f, f);  // head ((ch >> 3) & 1) * 2 + ((ch >> 2) & 1)
-  const float h1 = __shfl_sync(0xffffffffu, rel, half | 4);
-  const float h2 = __shfl_sync(0xffffffffu, rel, half | 8);
-  const float h3 = __shfl_sync(0xffffffffu, rel, half | 12);
-  return __fadd_rn(__fadd_rn(__fadd_rn(rel, h1), h2), h3);
+constexpr int kDecThreads = 256;                              // threads of the one-launch decode step
+constexpr int kDecBlocksPerCta = 128;                         // the unit a CTA's run is made of
+constexpr int kPageWindow = 64;                               // V pages a run may span
+constexpr int kDecRunMax = kPageWindow * (128 / kRatio);      // blocks a run may hold (2048)
+constexpr int kScoresCtasPerSm = 2;                           // resident CTAs the run length assumes
+
+// Blocks per CTA (a multiple of kDecBlocksPerCta, at most kDecRunMax) so that a grid of
+// (batch, ceilDiv(max_blocks, run)) CTAs is about one wave of ctas_per_sm CTAs per SM.
+inline int32_t decode_run_blocks(int sms, int ctas_per_sm, int32_t batch, int32_t max_blocks) {
+  const int32_t units = (max_blocks + kDecBlocksPerCta - 1) / kDecBlocksPerCta;
+  int32_t want_y = sms * ctas_per_sm / (batch > 0 ? batch : 1);
+  if (want_y < 1) want_y = 1;
+  int32_t per = (units + want_y - 1) / want_y;
+  if (per < 1) per = 1;
+  if (per > kDecRunMax / kDecBlocksPerCta) per = kDecRunMax / kDecBlocksPerCta;
+  return per * kDecBlocksPerCta;
 }
 
-constexpr int kDecThreads = 256;
-constexpr int kDecUnroll = 4;   // blocks a half-warp has in flight in one round
-constexpr int kDecRounds = 2;
-constexpr int kDecBlocksPerCta = (kDecThreads / 16) * kDecUnroll * kDecRounds;
-
-// One round of a half-warp: blocks g0 + 16*u, u < kDecUnroll; lane ch's 16 bytes of each
-// block's V-tail (zeros where the block is past g_end or its page slot is unusable).
-struct Round {
-  uint4 raw[kDecUnroll];
-  bool ok[kDecUnroll];
-};
-
-__device__ __forceinline__ void load_round(Round& r, const PoolDev& pool, int32_t b, int32_t g0, int32_t g_end,
-                                           int ch) {
-#pragma unroll
-  for (int u = 0; u < kDecUnroll; ++u) {
-    const int32_t g = g0 + 16 * u;
-    const uint16_t* k = g < g_end ? pool_tail(pool, b, 1, kRatio * g) : nullptr;
-    r.ok[u] = k != nullptr;
-    r.raw[u] = r.ok[u] ? ld_stream_v4(k + 8 * ch) : make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
-// Scores one loaded round into the logits row `out`; block `own` (>= 0) takes its kbar
-// from `own_kbar` (shared memory) instead of the pool.  Every lane of the warp calls it.
-template <class T>
-__device__ __forceinline__ void score_round(float* out, const float (&qf)[kNumQHeads][8], Round& r, int32_t g0,
-                                            int32_t g_end, float scale, int32_t own, const uint16_t* own_kbar,
-                                            int ch) {
-#pragma unroll
-  for (int u = 0; u < kDecUnroll; ++u) {
-    const int32_t g = g0 + 16 * u;
-    if (g == own) {
-      r.ok[u] = true;
-      r.raw[u] = *reinterpret_cast<const uint4*>(own_kbar + 8 * ch);
+// The V page of each 128-token slot that blocks [g_begin, g_end) of sequence b touch
+// (g_begin a multiple of 32, g_end - g_begin <= kDecRunMax), into pages[0, ..): the
+// pool page, or -1 where pool_tail gives no address (slot past maxPagesPerSeq, -1 or
+// outside the pool).  The caller synchronises before reading them.
+__device__ __forceinline__ void stage_vpages(int32_t* pages, const PoolDev& pool, int32_t b, int32_t g_begin,
+                                             int32_t g_end) {
+  if (g_end <= g_begin) return;
+  const int32_t s0 = (kRatio * g_begin) >> 7;
+  const int32_t n = ((kRatio * (g_end - 1)) >> 7) - s0 + 1;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int32_t slot = s0 + i;
+    int32_t page = -1;
+    if (slot < pool.max_pages) {
+      page = __ldg(pool.table + (static_cast<int64_t>(b) * 2 + 1) * pool.max_pages + slot);
+      if (page < 0 || page >= 2 * pool.num_pages) page = -1;
     }
-    const float sum = score_block<T>(qf, r.raw[u], ch);
-    if (ch == 0 && g < g_end) out[g] = r.ok[u] ? __fmul_rn(sum, scale) : -FLT_MAX;
+    pages[i] = page;
   }
-}
-
-// The paged scores of blocks [g_begin, g_end) (g_end - g_begin <= kDecBlocksPerCta) of
-// sequence b by a CTA of kDecThreads threads; logits row `out`.  qf holds this lane's 8
-// dims (8 * (lane % 16) ..) of the 4 q heads.  All rounds' loads are issued first.
-template <class T>
-__device__ __forceinline__ void score_range(float* out, const float (&qf)[kNumQHeads][8], const PoolDev& pool,
-                                            int32_t b, int32_t g_begin, int32_t g_end, float scale, int32_t own,
-                                            const uint16_t* own_kbar) {
-  const int ch = threadIdx.x & 15, hw = threadIdx.x >> 4;
-  Round r[kDecRounds];
-#pragma unroll
-  for (int k = 0; k < kDecRounds; ++k) load_round(r[k], pool, b, g_begin + 16 * kDecUnroll * k + hw, g_end, ch);
-#pragma unroll
-  for (int k = 0; k < kDecRounds; ++k)
-    score_round<T>(out, qf, r[k], g_begin + 16 * kDecUnroll * k + hw, g_end, scale, own, own_kbar, ch);
 }
 
 }  // namespace dec

@@ -133,9 +133,16 @@ cudaError_t launch_decode_step(bool bf16, int32_t* out_idx, float* logits, void*
                                int32_t batch, int32_t max_blocks, float scale, cudaStream_t stream);
 int32_t decode_step_max_batch();
 
-// Device fault flags: bits set by bounded waits that ran out (k2_scores_tc.cu, k1_stream.cu).
+// Device fault flags: bits set by bounded waits that ran out (k2_scores_tc.cu,
+// k1_stream.cu, k_decode.cu, k_decode_step.cu).
 cudaError_t read_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
 cudaError_t read_k1_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
+cudaError_t read_dec_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
+cudaError_t read_step_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
+
+// TMA map (a CUtensorMap, 64-byte aligned) over the pool's V-tails for the tensor-core
+// decode scoring (k2_scores_tc.cu).
+cudaError_t encode_vtail_map(void* map, const PoolDev& pool);
 
 // Cached cudaOccupancyMaxActiveBlocksPerMultiprocessor for (kernel, device).
 cudaError_t occupancy_blocks_per_sm(const void* kernel, int threads, size_t smem, int* out);

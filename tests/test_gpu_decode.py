@@ -5,8 +5,10 @@ launchQsaIndexerPreDecode, launchQsaIndexScoresDecode, launchQsaTopKExpandDecode
 Bit-exact where the page demands it: the paged K1b's dense output equals the plain
 K1b, pool writes land exactly where the addressing contract puts them, raw K tails
 are bit copies, the decode block compression equals prefill K1b, decode q equals
-prefill q at the same position, and the decode top-k equals the oracle on the same
-logits.  Decode scores are compared with the oracle within the logits tolerance.
+prefill q at the same position, decode scores equal prefill K2's row of the same
+token (both on the tensor cores, the same MMA along K), and the decode top-k equals
+the oracle on the same logits.  Decode scores are also compared with the oracle
+within the logits tolerance.
 """
 import numpy as np
 import pytest
@@ -117,6 +119,8 @@ def test_decode_loop_matches_oracle_and_prefill(dtype):
     # reference: the whole sequences through prefill K1a / K1b on the GPU
     full_q = g_.q_prep(d)
     full_k = g_.k_compress(d, NB, 0, NB, 0)
+    # prefill K2 over the whole sequences: the decode scores of token t are its row t
+    k2 = g_.scores(dtype, g_.dev(full_q), g_.dev(full_k), g_.dev(np.array(total, np.int32)), B, S, NB, 0, B * S)
     q = torch.empty((B, 1, 4, 128), dtype=torch.int16, device="cuda")
     logits = torch.full((B, maxb), float("nan"), dtype=torch.float32, device="cuda")
     out = torch.empty((B, 2051), dtype=torch.int32, device="cuda")
@@ -153,6 +157,8 @@ def test_decode_loop_matches_oracle_and_prefill(dtype):
                 fl = logits_floor(qh[b, 0][None], kb_b, dtype)
                 ok, st = check_logits(lg[b, :nv][None], ref[b, :nv][None], dtype, fl)
                 assert ok, (step, b, st)
+                # the same MMA shape along K and the same K order as prefill K2: the same bits
+                assert np.array_equal(lg[b, :nv].view(np.uint32), k2[b * S + pos[b], :nv].view(np.uint32)), (step, b)
         # top-k: bit-exact against the oracle on the same logits
         assert np.array_equal(oh, oracle.topk_expand_decode(lg, ctx)), step
         # and the prefill selection kernel picks the same blocks for the same logits
@@ -172,6 +178,52 @@ def test_decode_loop_matches_oracle_and_prefill(dtype):
             assert np.array_equal(pool_util.v_tail(pool_end, b, g), full_k[b, g]), (b, g)
         for t in range(total[b] - total[b] % 4, total[b]):
             assert np.array_equal(pool_util.k_tail(pool_end, b, t), wl.index_qk[b, t, 512:])
+    assert qsa.qsa_device_fault_flags() == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("nkv,phd,hs,B,max_tokens", [(1, 128, 0, 40, 4100), (2, 384, 256, 6, 4100),
+                                                     (4, 200, 72, 3, 2000)])
+def test_paged_scores_layouts_and_unusable_slots(dtype, nkv, phd, hs, B, max_tokens):
+    """qsa_index_scores_decode against the oracle on pools of several head layouts, with
+    V page slots that are -1, point outside the pool or lie past maxPagesPerSeq (those
+    blocks score -FLT_MAX), nVis from 0 to past the table, runs of several 128-block
+    tiles (B=40) and partial tiles and pages."""
+    qsa, g_ = _qsa(), _gu()
+    rng = np.random.default_rng(90 + nkv)
+    hp = pool_util.make_pool(B, max_tokens, seed=41 + nkv, num_kv_heads=nkv, pool_head_dim=phd, head_size=hs)
+    hp.pool[...] = workloads.round_to_t(rng.standard_normal(hp.pool.shape), dtype).reshape(hp.pool.shape)
+    max_pages = hp.page_table.shape[2]
+    hp.page_table[0, 1, 3] = -1                               # a hole in sequence 0
+    hp.page_table[1 % B, 1, 5] = 2 * hp.num_pages + 7         # outside the pool
+    hp.page_table[2 % B, 1, 0] = -1                           # the first page
+    maxb = max_pages * 32 + 40                                # the last 40 blocks lie past the table
+    fixed = [4 * maxb, 0, 1, 3, 4, 5, 2047, 2048, 4 * 32 * max_pages + 3, 4 * 129 + 2]
+    ctx = np.array([fixed[b] if b < len(fixed) else int(rng.integers(0, 4 * maxb + 1)) for b in range(B)], np.int32)
+    q = workloads.round_to_t(rng.standard_normal((B, 1, 4, 128)), dtype).reshape(B, 1, 4, 128)
+    dp = DevPool(hp)
+    logits = torch.full((B, maxb), float("nan"), dtype=torch.float32, device="cuda")
+    qsa.qsa_index_scores_decode(logits, g_.dev(q), g_.dev(ctx), dp.state, B, maxb, dtype=dtype)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    ref = oracle.scores_decode(dtype, q, ctx, hp, maxb)
+    n_unusable = 0
+    for b in range(B):
+        nv = min(int(ctx[b]) // 4, maxb)
+        assert np.all(np.isnan(lg[b, nv:])), b                       # only the valid prefix
+        if nv == 0:
+            continue
+        tails = [pool_util.v_tail(hp, b, g) if (4 * g) // 128 < max_pages else None for g in range(nv)]
+        unusable = np.array([t is None or not (0 <= hp.page_table[b, 1, (4 * g) // 128] < 2 * hp.num_pages)
+                             for g, t in enumerate(tails)])
+        n_unusable += int(unusable.sum())
+        assert np.array_equal(ref[b, :nv] == NEG_MAX, unusable), b
+        kb_b = np.stack([t if (t is not None and not u) else np.zeros(128, np.uint16)
+                         for t, u in zip(tails, unusable)])
+        fl = logits_floor(q[b, 0][None], kb_b, dtype)
+        ok, st = check_logits(lg[b, :nv][None], ref[b, :nv][None], dtype, fl)
+        assert ok, (b, st)
+    assert n_unusable > 40
     assert qsa.qsa_device_fault_flags() == 0
 
 
