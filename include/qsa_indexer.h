@@ -295,7 +295,9 @@ int qsa_indexer_pre_decode(qsa_dtype_t dtype, void* qNormed, const void* indexQk
  * launchQsaIndexScoresDecode: logits[b][g] = (1/sqrtf(128)) * sum_h relu(q[b][h] .
  * kbar[b][g]) (FP32, ascending h, scale after the sum) for g < nVis = ctx/4, with
  * kbar read from the V-tail of token 4g.  ONLY [0, nVis) of each row is written.  A
- * block whose V page slot is unusable scores -FLT_MAX.
+ * block whose V page slot is unusable scores -FLT_MAX.  The dots run on the tensor
+ * cores with qsa_index_scores' MMA shape along K and K order, so each logit equals,
+ * bit for bit, qsa_index_scores' logit of the same token given the same q and kbar.
  *  logits   [out] FP32 [batchSize, maxBlocks]; maxBlocks >= ceilDiv(max ctx, 4)
  *  qNormed  [in]  T [batchSize, 1, 4, 128] (qsa_indexer_pre_decode's output)
  */
