@@ -178,6 +178,33 @@ cudaError_t launch_scores_decode(bool bf16, float* logits, const void* q_normed,
   return cudaGetLastError();
 }
 
+// The pool's V-tails as a 3-D map {poolHeadDim, 4 x numKVHeads, 2 x numPages x 32}
+// (element within a token-head row, token-head row within a 4-token block, block),
+// box {64, 1, 32}: one page's 32 V-tail halves per copy, 128-byte swizzle.
+cudaError_t encode_vtail_map(void* map, const PoolDev& pool) {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static cudaError_t status = cudaSuccess;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+    if (status == cudaSuccess && q != cudaDriverEntryPointSuccess) status = cudaErrorNotSupported;
+    if (status == cudaSuccess) encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  if (status != cudaSuccess) return status;
+  const uint64_t phd = static_cast<uint64_t>(pool.pool_head_dim);
+  const uint64_t rows = 4ull * static_cast<uint64_t>(pool.num_kv_heads);
+  cuuint64_t dims[3] = {phd, rows, 2ull * static_cast<uint64_t>(pool.num_pages) * 32ull};
+  cuuint64_t strides[2] = {phd * 2, rows * phd * 2};
+  cuuint32_t box[3] = {64, 1, 32};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, pool.pool, dims, strides,
+                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t read_dec_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream) {
   cudaError_t e = cudaMemcpyFromSymbolAsync(flags, g_dec_fault_flags, sizeof(uint32_t), 0,
                                             cudaMemcpyDeviceToHost, stream);

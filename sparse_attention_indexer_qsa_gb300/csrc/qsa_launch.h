@@ -141,7 +141,7 @@ cudaError_t read_dec_fault_flags(uint32_t* flags, bool clear, cudaStream_t strea
 cudaError_t read_step_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
 
 // TMA map (a CUtensorMap, 64-byte aligned) over the pool's V-tails for the tensor-core
-// decode scoring (k2_scores_tc.cu).
+// decode scoring (k_decode.cu).
 cudaError_t encode_vtail_map(void* map, const PoolDev& pool);
 
 // Cached cudaOccupancyMaxActiveBlocksPerMultiprocessor for (kernel, device).

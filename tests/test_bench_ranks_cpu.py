@@ -71,3 +71,11 @@ def test_single_rank_helpers_need_no_process_group():
     assert bench.max_over_ranks_of(2.5, 1) == 2.5
     assert bench.whole_job_rows_per_s(1000, 2.0, 1) == pytest.approx(5e5)
     json.dumps({"v": bench.whole_job_rows_per_s(1, 1.0, 4)})
+
+
+def test_k2_traffic_profile_matches_the_kernel_source():
+    """The bench line's roofline traffic comes from the committed K2 ncu summary, which
+    records the hash of the K2 source it was captured on: the two must still agree."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.k2_profiled_traffic(8) == 2168935424
