@@ -304,6 +304,56 @@ def test_fused_decode_step_bit_identical_to_three_calls(dtype):
     assert qsa.qsa_device_fault_flags() == 0
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_fused_decode_step_long_rows(dtype):
+    """The one-launch step against the three calls on rows of ~40000 visible blocks: the
+    selection's widest mask path (8 words a thread at 256 threads; 16 at the separate
+    top-k's 128), runs of many 128-block tiles and a block compress at a page edge.  The
+    pool (one KV head, 128-dim rows, the V-tail the whole row) is filled with random T
+    values directly."""
+    qsa, g_ = _qsa(), _gu()
+    B = 2
+    ctx = np.array([4 * 40000, 4 * 39000 + 2], np.int32)   # a block completes / a K-tail is written
+    maxb = 40005
+    rng = np.random.default_rng(77)
+    hp = pool_util.make_pool(B, int(ctx.max()) + 8, seed=13, num_kv_heads=1, pool_head_dim=128, head_size=0)
+    hp.pool[...] = workloads.round_to_t(rng.standard_normal(hp.pool.shape, dtype=np.float32),
+                                        dtype).reshape(hp.pool.shape)
+    rows = workloads.round_to_t(rng.standard_normal((B, 640)), dtype).reshape(B, 640)
+    cos_sin = g_.dev(workloads.cos_sin_table(int(ctx.max()) + 8))
+    w_q = g_.dev(workloads.gamma(rng, dtype))
+    w_k = g_.dev(workloads.gamma(rng, dtype))
+    pools = [DevPool(hp) for _ in range(2)]
+    d_rows, d_ctx = g_.dev(rows), g_.dev(ctx)
+
+    def bufs():
+        return dict(q=torch.empty((B, 1, 4, 128), dtype=torch.int16, device="cuda"),
+                    logits=torch.full((B, maxb), float("nan"), device="cuda"),
+                    out=torch.empty((B, 2051), dtype=torch.int32, device="cuda"),
+                    split=torch.full((B, 3), 9, dtype=torch.int32, device="cuda"))
+    three, fused = bufs(), bufs()
+    st0, st1 = pools[0].state, pools[1].state
+    qsa.qsa_indexer_pre_decode(three["q"], d_rows, cos_sin, d_ctx, w_q, w_k, 1e-6, st0, B, dtype=dtype)
+    qsa.qsa_index_scores_decode(three["logits"], three["q"], d_ctx, st0, B, maxb, dtype=dtype)
+    qsa.qsa_topk_expand_decode(three["out"], three["logits"], d_ctx, three["split"], 3, B, maxb)
+    qsa.qsa_indexer_decode_step(fused["out"], fused["logits"], fused["q"], d_rows, cos_sin, d_ctx, w_q, w_k, 1e-6,
+                                st1, fused["split"], 3, B, maxb, dtype=dtype)
+    torch.cuda.synchronize()
+    for name in ("q", "out", "split"):
+        assert torch.equal(three[name], fused[name]), name
+    for b in range(B):
+        nv = int(ctx[b]) // 4
+        assert torch.equal(three["logits"][b, :nv].view(torch.int32), fused["logits"][b, :nv].view(torch.int32)), b
+        assert torch.isnan(fused["logits"][b, nv:]).all(), b
+        assert not torch.isnan(fused["logits"][b, :nv]).any(), b
+    assert not fused["split"].any()
+    assert np.array_equal(pools[0].numpy(), pools[1].numpy())
+    # the selection itself, against the oracle on the same logits
+    assert np.array_equal(fused["out"].cpu().numpy(),
+                          oracle.topk_expand_decode(fused["logits"].cpu().numpy(), ctx))
+    assert qsa.qsa_device_fault_flags() == 0
+
+
 def test_fused_decode_step_validation():
     qsa = _qsa()
     P = 0x1000

@@ -97,9 +97,11 @@ def test_prefill_step_graph_replays_bit_identical():
     assert _qsa().qsa_device_fault_flags() == 0
 
 
-def test_decode_step_graph_replays_match_eager():
-    """Two copies of a prefilled pool advance token by token: one by eager calls, one by
-    replays of a graph of the three decode launches; every output and both pools stay
+@pytest.mark.parametrize("fused", [False, True])
+def test_decode_step_graph_replays_match_eager(fused):
+    """Two copies of a prefilled pool advance token by token: one by eager calls of the
+    three decode launches, one by replays of a graph of the same three launches or of the
+    one-launch step (qsa_indexer_decode_step); every output and both pools stay
     bit-identical."""
     qsa, g_ = _qsa(), _gu()
     B, S, prefill = 3, 1100, [1020, 1023, 600]
@@ -143,9 +145,17 @@ def test_decode_step_graph_replays_match_eager():
         bf["ctx"].copy_(torch.from_numpy(ctx))
         bf["split"].fill_(5)
 
+    def step_fused(bf, st):
+        qsa.qsa_indexer_decode_step(bf["out"], bf["logits"], bf["q"], bf["row"], d.cos_sin, bf["ctx"], d.w_q,
+                                    d.w_k, wl.eps, st, bf["split"], 2, B, maxb, dtype="bf16")
+
+    graph_step = step_fused if fused else step
     eager_bf, graph_bf = buffers(), buffers()
     feed(eager_bf, 0)
     step(eager_bf, states[0])                        # first-call set-up outside the capture
+    if fused:                                        # (token 0's writes again, so idempotent)
+        feed(graph_bf, 0)
+        graph_step(graph_bf, states[1])
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
@@ -154,7 +164,7 @@ def test_decode_step_graph_replays_match_eager():
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
-            step(graph_bf, states[1])
+            graph_step(graph_bf, states[1])
     torch.cuda.current_stream().wait_stream(s)
     for k in range(0, 70):                           # crosses a 4-token block edge many times
         if k > 0:
