@@ -252,19 +252,20 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
     step (ctx % 4 == 0), so the pre-decode compresses a block from three K-tails."""
     import torch
     sp = stream.cuda_stream
+    gen = torch.Generator(device="cuda").manual_seed(6)
     pages = (ctx_len + 127) // 128
     num_pages = B * pages
-    pool = torch.randn((2 * num_pages, 128, 2, 384), device="cuda").to(torch.bfloat16)
+    pool = torch.randn((2 * num_pages, 128, 2, 384), device="cuda", generator=gen).to(torch.bfloat16)
     table = torch.empty((B, 2, pages), dtype=torch.int32, device="cuda")
     ids = torch.arange(num_pages, dtype=torch.int32, device="cuda").view(B, pages)
     table[:, 0] = ids
     table[:, 1] = ids + num_pages
     state = qsa.pool_state(pool, table, num_pages)
-    rows = torch.randn((B, 1, 640), device="cuda").to(torch.bfloat16)
-    cs = torch.randn((ctx_len, 64), device="cuda")
+    rows = torch.randn((B, 1, 640), device="cuda", generator=gen).to(torch.bfloat16)
+    cs = torch.randn((ctx_len, 64), device="cuda", generator=gen)
     ctx = torch.full((B,), ctx_len, dtype=torch.int32, device="cuda")
-    wq = (torch.randn(128, device="cuda") * 0.1).to(torch.bfloat16)
-    wk = (torch.randn(128, device="cuda") * 0.1).to(torch.bfloat16)
+    wq = (torch.randn(128, device="cuda", generator=gen) * 0.1).to(torch.bfloat16)
+    wk = (torch.randn(128, device="cuda", generator=gen) * 0.1).to(torch.bfloat16)
     q = torch.empty((B, 1, 4, 128), dtype=torch.bfloat16, device="cuda")
     maxb = (ctx_len + 3) // 4
     logits = torch.empty((B, maxb), dtype=torch.float32, device="cuda")
@@ -370,10 +371,10 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
            "topk_expand_decode": B * (nvis * 4 + 2051 * 4)}
     # prefill persistence into the same pool: K1b with the V-tail write over every
     # sequence's ctx-1 tokens (4095 complete blocks each), then the 3 raw K-tails
-    iq_full = torch.randn((B, ctx_len, 640), device="cuda").to(torch.bfloat16)
+    iq_full = torch.randn((B, ctx_len, 640), device="cuda", generator=gen).to(torch.bfloat16)
     kb_dense = torch.empty((B, maxb, 128), dtype=torch.bfloat16, device="cuda")
     pctx = torch.full((B,), ctx_len - 1, dtype=torch.int32, device="cuda")
-    cs_full = torch.randn((ctx_len, 64), device="cuda")
+    cs_full = torch.randn((ctx_len, 64), device="cuda", generator=gen)
 
     def compress_paged(st):
         return lib.qsa_index_k_compress_paged(qsa.QSA_BF16, kb_dense.data_ptr(), iq_full.data_ptr(),
