@@ -26,6 +26,17 @@ int qsa_testing_index_scores_cuda_core(qsa_dtype_t dtype, float* logits, const v
                                        int32_t batchSize, int32_t seqLen, int32_t numBlocks,
                                        int32_t rowStart, int32_t numRows, qsa_stream_t stream);
 
+/*
+ * Exercises the bounded-wait error path of the tensor-core decode scoring: one warp
+ * waits, through the same device routine the decode engine uses, on an mbarrier that
+ * nothing arrives on.  After timeoutMs milliseconds (1..10000) the wait gives up, sets
+ * bit 2 of the paged-decode-scores field of qsa_device_fault_flags (bit 18 of the
+ * word) and the kernel returns; the context stays usable.  No fault, trap or
+ * unbounded spin is involved.
+ * Errors: QSA_E_RANGE (timeoutMs), QSA_E_CUDA.
+ */
+int qsa_testing_bounded_wait_probe(int32_t timeoutMs, qsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

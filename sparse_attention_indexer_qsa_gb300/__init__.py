@@ -23,7 +23,7 @@ __all__ = [
     "PoolState", "pool_state", "qsa_index_k_compress_paged", "qsa_raw_k_tail_write_prefill",
     "qsa_indexer_pre_decode", "qsa_index_scores_decode", "qsa_topk_expand_decode",
     "qsa_indexer_decode_step", "qsa_device_fault_flags",
-    "qsa_testing_index_scores_cuda_core", "LIB_PATH",
+    "qsa_testing_index_scores_cuda_core", "qsa_testing_bounded_wait_probe", "LIB_PATH",
 ]
 
 QSA_BF16 = 0
@@ -35,7 +35,7 @@ EXPORTED = ["qsa_abi_version", "qsa_last_error", "qsa_index_q_prep", "qsa_index_
             "qsa_index_k_compress_paged", "qsa_raw_k_tail_write_prefill", "qsa_indexer_pre_decode",
             "qsa_index_scores_decode", "qsa_topk_expand_decode", "qsa_indexer_decode_step",
             "qsa_index_scores", "qsa_index_scores_no_alloc", "qsa_device_fault_flags",
-            "qsa_testing_index_scores_cuda_core"]
+            "qsa_testing_index_scores_cuda_core", "qsa_testing_bounded_wait_probe"]
 
 
 class QsaError(RuntimeError):
@@ -111,6 +111,8 @@ def load():
     L.qsa_index_scores_no_alloc.restype = ctypes.c_int
     L.qsa_testing_index_scores_cuda_core.argtypes = list(L.qsa_index_scores.argtypes)
     L.qsa_testing_index_scores_cuda_core.restype = ctypes.c_int
+    L.qsa_testing_bounded_wait_probe.argtypes = [i32, p]
+    L.qsa_testing_bounded_wait_probe.restype = ctypes.c_int
     L.qsa_device_fault_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, p]
     L.qsa_device_fault_flags.restype = ctypes.c_int
     _lib = L
@@ -278,6 +280,12 @@ def qsa_index_scores_no_alloc(logits, qNormed, kbar, contextLengths, batchSize, 
     _check(load().qsa_index_scores_no_alloc(_dtype(dtype, qNormed, kbar), _addr(logits), _addr(qNormed),
                                          _addr(kbar), _addr(contextLengths), int(batchSize), int(seqLen),
                                          int(numBlocks), int(rowStart), int(numRows), _stream(stream)))
+
+
+def qsa_testing_bounded_wait_probe(timeoutMs, stream=None):
+    """A bounded wait that runs out on purpose (include/qsa_indexer_testing.h): sets a
+    device fault bit after timeoutMs, faults nothing."""
+    _check(load().qsa_testing_bounded_wait_probe(int(timeoutMs), _stream(stream)))
 
 
 def qsa_testing_index_scores_cuda_core(logits, qNormed, kbar, contextLengths, batchSize, seqLen,

@@ -121,6 +121,22 @@ __global__ void __launch_bounds__(kScoresThreads, kScoresCtasPerSm)
   dtc::engine_teardown(tmem);
 }
 
+// Test-only: the engine's bounded wait on an mbarrier that nothing arrives on.  Every
+// thread of one warp waits; the wait runs out after limit_ns, sets the epilogue fault
+// bit of this module's fault word and the CTA's abort flag, and the kernel returns.
+__global__ void bounded_wait_probe_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar_word;
+  __shared__ int abort_flag;
+  const uint32_t bar = ptx::smem_u32(&bar_word);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar, 1);
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncwarp();
+  dtc::wait_bounded_raw(bar, 0, &abort_flag, &g_dec_fault_flags, dtc::kFaultEpilogue, limit_ns);
+}
+
 }  // namespace dec
 
 cudaError_t launch_raw_k_tail_write_prefill(bool bf16, const void* index_qk, const int32_t* ctx, const PoolDev& pool,
@@ -203,6 +219,11 @@ cudaError_t encode_vtail_map(void* map, const PoolDev& pool) {
                       box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bounded_wait_probe(uint64_t limit_ns, cudaStream_t stream) {
+  dec::bounded_wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t read_dec_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream) {

@@ -440,6 +440,16 @@ QSA_API int qsa_indexer_decode_step(qsa_dtype_t dtype, int32_t* outIdx, float* l
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+QSA_API int qsa_testing_bounded_wait_probe(int32_t timeoutMs, qsa_stream_t stream) {
+  static const char* fn = "qsa_testing_bounded_wait_probe";
+  if (timeoutMs < 1 || timeoutMs > 10000) return fail(QSA_E_RANGE, "%s: timeoutMs must be in [1, 10000]", fn);
+  DeviceInfo d;
+  int st = current_device(fn, &d);
+  if (st != QSA_OK) return st;
+  return launched(fn, qsa::launch_bounded_wait_probe(static_cast<uint64_t>(timeoutMs) * 1000000ull,
+                                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 QSA_API int qsa_testing_index_scores_cuda_core(qsa_dtype_t dtype, float* logits, const void* qNormed,
                                                const void* kbar, const int32_t* contextLengths,
                                                int32_t batchSize, int32_t seqLen, int32_t numBlocks,

@@ -72,19 +72,26 @@ struct Engine {
   }
 };
 
-__device__ __forceinline__ bool wait_bounded(const Engine& en, uint32_t bar, uint32_t parity, uint32_t code) {
+// Wait for the phase of `bar` with the given parity for at most `limit_ns`; on time-out
+// set `code` in the fault word and the CTA's abort flag.  Returns false (without
+// waiting further) once the abort flag is set by any thread of the CTA.
+__device__ __forceinline__ bool wait_bounded_raw(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                 uint32_t* fault, uint32_t code, uint64_t limit_ns) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
-  volatile int* abort_flag = en.abort_flag();
   const uint64_t start = ptx::global_timer_ns();
   while (true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (ptx::global_timer_ns() - start > kWaitLimitNs) {
-      atomicOr(en.fault, code);
+    if (ptx::global_timer_ns() - start > limit_ns) {
+      atomicOr(fault, code);
       *abort_flag = 1;
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool wait_bounded(const Engine& en, uint32_t bar, uint32_t parity, uint32_t code) {
+  return wait_bounded_raw(bar, parity, en.abort_flag(), en.fault, code, kWaitLimitNs);
 }
 
 __device__ __forceinline__ void drain_wait(const Engine& en, uint32_t bar, uint32_t parity) {

@@ -138,6 +138,8 @@ int32_t decode_step_max_batch();
 cudaError_t read_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
 cudaError_t read_k1_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
 cudaError_t read_dec_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
+// Test-only: one warp's bounded wait on an mbarrier nothing arrives on (k_decode.cu).
+cudaError_t launch_bounded_wait_probe(uint64_t limit_ns, cudaStream_t stream);
 cudaError_t read_step_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
 
 // TMA map (a CUtensorMap, 64-byte aligned) over the pool's V-tails for the tensor-core

@@ -80,6 +80,8 @@ def test_null_dtype_shape_range_align_rejected(qsa):
     assert "aligned" in qsa.qsa_last_error()
     # the testing entry point validates the same way
     assert L.qsa_testing_index_scores_cuda_core(0, P, P, None, P, 1, 8, 2, 0, 8, None) == -1
+    assert L.qsa_testing_bounded_wait_probe(0, None) == -3          # timeout out of range
+    assert L.qsa_testing_bounded_wait_probe(10001, None) == -3
 
 
 def test_empty_work_is_a_no_op(qsa):

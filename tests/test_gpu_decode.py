@@ -227,6 +227,40 @@ def test_paged_scores_layouts_and_unusable_slots(dtype, nkv, phd, hs, B, max_tok
     assert qsa.qsa_device_fault_flags() == 0
 
 
+def test_bounded_wait_runs_out_reports_and_leaves_the_context_usable():
+    """The decode engine's bounded wait, on an mbarrier nothing arrives on, gives up after
+    its limit, sets its fault bit (read on the host, then cleared), and the next launches
+    on the same context compute correct scores."""
+    import time
+    qsa, g_ = _qsa(), _gu()
+    assert qsa.qsa_device_fault_flags(clear=True) == 0
+    t0 = time.perf_counter()
+    qsa.qsa_testing_bounded_wait_probe(200)
+    flags = qsa.qsa_device_fault_flags(clear=True)
+    assert time.perf_counter() - t0 >= 0.2
+    assert flags == 4 << 16
+    assert qsa.qsa_device_fault_flags() == 0
+    # the context still works
+    B, dtype = 2, "bf16"
+    rng = np.random.default_rng(5)
+    hp = pool_util.make_pool(B, 600, seed=6)
+    hp.pool[...] = workloads.round_to_t(rng.standard_normal(hp.pool.shape, dtype=np.float32),
+                                        dtype).reshape(hp.pool.shape)
+    ctx = np.array([600, 517], np.int32)
+    maxb = 152
+    q = workloads.round_to_t(rng.standard_normal((B, 1, 4, 128)), dtype).reshape(B, 1, 4, 128)
+    logits = torch.full((B, maxb), float("nan"), dtype=torch.float32, device="cuda")
+    qsa.qsa_index_scores_decode(logits, g_.dev(q), g_.dev(ctx), DevPool(hp).state, B, maxb, dtype=dtype)
+    lg = logits.cpu().numpy()
+    ref = oracle.scores_decode(dtype, q, ctx, hp, maxb)
+    for b in range(B):
+        nv = int(ctx[b]) // 4
+        kb_b = np.stack([pool_util.v_tail(hp, b, g) for g in range(nv)])
+        ok, st = check_logits(lg[b, :nv][None], ref[b, :nv][None], dtype, logits_floor(q[b, 0][None], kb_b, dtype))
+        assert ok, (b, st)
+    assert qsa.qsa_device_fault_flags() == 0
+
+
 def test_decode_validation_rejects_bad_pools():
     qsa = _qsa()
     P = 0x1000
