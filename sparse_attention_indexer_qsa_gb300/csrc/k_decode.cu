@@ -106,18 +106,25 @@ __global__ void __launch_bounds__(kScoresThreads, kScoresCtasPerSm)
   const int32_t g_begin = blockIdx.y * run;
   if (g_begin >= n_vis) return;  // only the valid prefix is written (the whole CTA leaves)
   const int32_t g_end = min(g_begin + run, n_vis);
-  const int tid = threadIdx.x;
-  stage_vpages(vpages, pool, b, g_begin, g_end);
-  if (tid < kNumQHeads * 16) {
-    const int h = tid >> 4, ch = tid & 15;
-    dtc::put_q_chunk(en, h, ch,
-                     ld_cached_v4(q_normed + static_cast<int64_t>(b) * (kNumQHeads * kHeadDim) + h * kHeadDim + 8 * ch));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp == 0) {  // the page entries, then the first tiles' copies, before the CTA barrier
+    stage_vpages(vpages, pool, b, g_begin, g_end, tid, 32);
+    __syncwarp();
+    dtc::engine_start(en, &pool_map, vpages, pool.head_size, g_begin, g_end, dtc::kStages);
+  } else {
+    const int k = tid - 32;
+    if (k < kNumQHeads * 16) {
+      const int h = k >> 4, ch = k & 15;
+      dtc::put_q_chunk(en, h, ch,
+                       ld_cached_v4(q_normed + static_cast<int64_t>(b) * (kNumQHeads * kHeadDim) + h * kHeadDim +
+                                    8 * ch));
+    }
+    dtc::zero_b_padding(en, k, kScoresThreads - 32);
+    ptx::fence_proxy_async_shared();
   }
-  dtc::zero_b_padding(en, tid, kScoresThreads);
-  ptx::fence_proxy_async_shared();
-  const uint32_t tmem = dtc::engine_setup(en, &pool_map);
+  const uint32_t tmem = dtc::engine_setup(en);
   dtc::engine_run<kBf16>(en, tmem, &pool_map, vpages, pool.head_size, g_begin, g_end,
-                         logits + static_cast<int64_t>(b) * max_blocks, scale);
+                         logits + static_cast<int64_t>(b) * max_blocks, scale, dtc::kStages);
   dtc::engine_teardown(tmem);
 }
 

@@ -3,10 +3,13 @@
 //
 // grid (B, Y), kDecThreads threads; CTA (b, y) covers the run of blocks [y * perCta,
 // (y + 1) * perCta), perCta chosen so that the grid is about one wave.  CTA (b, y):
-//   - warp 0 computes sequence b's q heads straight into the tensor-core B operand
-//     (CTA y = 0 also writes qNormed[b]); warp 1 either writes the new token's raw
-//     K-tail (CTA y = 0), or, in the CTA whose run holds the just-completed block g,
-//     compresses g (the pre-decode routines) into the pool's V-tail;
+//   - warp 0 stages the run's page entries and issues the first tiles' TMA copies at
+//     once (in the CTA that compresses block g below, none from g's tile on);
+//   - warp 2 computes sequence b's q heads straight into the tensor-core B operand
+//     (CTA y = 0 also writes qNormed[b]); warp 3 either writes the new token's raw
+//     K-tail (CTA y = 0), or, in the CTA whose run holds the just-completed block g
+//     (the last CTA if g lies past maxBlocks), compresses g (the pre-decode
+//     routines) into the pool's V-tail;
 //   - the tensor-core paged-scores engine scores the run's blocks of the valid prefix
 //     (the owning CTA's TMA copies read block g's fresh V-tail) into logits[b];
 //   - the last CTA of sequence b to finish (a per-sequence arrival counter, no waiting)
@@ -63,15 +66,27 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
   const int32_t n_vis = c > 0 ? min(c / kRatio, max_blocks) : 0;
   const int32_t g_begin = y * per_cta;
   const int32_t g_end = min(g_begin + per_cta, n_vis);
-  stage_gamma<T>(w_q, g1q);
-  stage_gamma<T>(w_k, g1k);
-  stage_vpages(vpages, pool, b, g_begin, g_end);
-  dtc::zero_b_padding(en, tid, kDecThreads);
+  // the CTA that compresses block g_new = c/4 - 1 (if this step completes one): the
+  // one whose run holds it, or the last one if g_new lies past maxBlocks
+  const int32_t g_new = c > 0 && c % kRatio == 0 ? c / kRatio - 1 : -1;
+  const bool owner = g_new >= 0 && min(g_new / per_cta, static_cast<int32_t>(gridDim.y) - 1) == y;
+  // tiles copied before the CTA barrier: in the owning CTA, none from g_new's tile on
+  // (its V-tail is written below)
+  const int pre_limit = owner && g_new < g_end ? (g_new - g_begin) / dtc::kTile : dtc::kStages;
+  if (warp == 0) {
+    stage_vpages(vpages, pool, b, g_begin, g_end, tid, 32);
+    __syncwarp();
+    dtc::engine_start(en, &pool_map, vpages, pool.head_size, g_begin, g_end, pre_limit);
+  } else {
+    stage_gamma<T>(w_q, g1q, tid - 32, kDecThreads - 32);
+    stage_gamma<T>(w_k, g1k, tid - 32, kDecThreads - 32);
+    dtc::zero_b_padding(en, tid - 32, kDecThreads - 32);
+  }
   __syncthreads();
   const uint16_t* row = index_qk + static_cast<int64_t>(b) * kRowWidth;
   const int h = lane >> 3, j = lane & 7;
   const int ca = chunk_a(j), cb = chunk_b(j);
-  if (warp == 0) {
+  if (warp == 2) {
     uint4 oa, ob;
     q_heads<T>(row, cos_sin, c, g1q, eps, lane, oa, ob);
     dtc::put_q_chunk(en, h, ca / 8, oa);
@@ -81,13 +96,13 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
       st_v4(dst + ca, oa);
       st_v4(dst + cb, ob);
     }
-  } else if (warp == 1 && c > 0) {
+  } else if (warp == 3 && c > 0) {
     if (c % kRatio != 0) {
       if (y == 0) {
         uint16_t* dst = pool_tail(pool, b, 0, c - 1);
         if (dst != nullptr) copy_tail(dst, row + kKCol, lane);
       }
-    } else if ((c / kRatio - 1) / per_cta == y) {
+    } else if (owner) {
       uint4 oa, ob;
       uint16_t* vtail = nullptr;
       const bool ok = compress_block<T>(pool, b, c, row, cos_sin, g1k, eps, lane, oa, ob, &vtail);
@@ -99,10 +114,11 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
     }
   }
   ptx::fence_proxy_async_shared();  // the B operand, before the MMAs read it
-  const uint32_t tmem = dtc::engine_setup(en, &pool_map);
+  const uint32_t tmem = dtc::engine_setup(en);
   if (tid == 0) ptx::fence_proxy_async_global();
   float* lrow = logits + static_cast<int64_t>(b) * max_blocks;
-  dtc::engine_run<T::kIsBf16>(en, tmem, &pool_map, vpages, pool.head_size, g_begin, g_end, lrow, scale);
+  dtc::engine_run<T::kIsBf16>(en, tmem, &pool_map, vpages, pool.head_size, g_begin, g_end, lrow, scale,
+                              pre_limit);
   dtc::engine_teardown(tmem);
 
   // ---- the last CTA of sequence b selects its row

@@ -112,8 +112,9 @@ __device__ __forceinline__ int chunk_b(int j) { return j < 4 ? 32 + 8 * j : 96 +
 // (1 + w) for all 128 dims into shared memory, once per CTA (w is the raw
 // checkpoint gamma [128] in T).  Call before the CTA's first __syncthreads().
 template <class T>
-__device__ __forceinline__ void stage_gamma(const uint16_t* w, float* g1) {
-  for (int d = threadIdx.x; d < kHeadDim; d += blockDim.x) g1[d] = __fadd_rn(1.0f, T::one(w[d]));
+__device__ __forceinline__ void stage_gamma(const uint16_t* w, float* g1, int first = threadIdx.x,
+                                            int stride = blockDim.x) {
+  for (int d = first; d < kHeadDim; d += stride) g1[d] = __fadd_rn(1.0f, T::one(w[d]));
 }
 
 // The lane's cos/sin values for rope position row `cs` (only lanes j < 4 rotate).

@@ -100,11 +100,11 @@ inline int32_t decode_run_blocks(int sms, int ctas_per_sm, int32_t batch, int32_
 // pool page, or -1 where pool_tail gives no address (slot past maxPagesPerSeq, -1 or
 // outside the pool).  The caller synchronises before reading them.
 __device__ __forceinline__ void stage_vpages(int32_t* pages, const PoolDev& pool, int32_t b, int32_t g_begin,
-                                             int32_t g_end) {
+                                             int32_t g_end, int first = threadIdx.x, int stride = blockDim.x) {
   if (g_end <= g_begin) return;
   const int32_t s0 = (kRatio * g_begin) >> 7;
   const int32_t n = ((kRatio * (g_end - 1)) >> 7) - s0 + 1;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+  for (int i = first; i < n; i += stride) {
     const int32_t slot = s0 + i;
     int32_t page = -1;
     if (slot < pool.max_pages) {

@@ -126,25 +126,63 @@ __device__ __forceinline__ void put_q_chunk(const Engine& en, int h, int c, cons
   *reinterpret_cast<uint4*>(en.ptr + kOffB + b_chunk_offset(h, c)) = v;
 }
 
-// Barriers and TMEM; every thread of the CTA calls it (contains __syncthreads).  The
-// caller has written the B operand (and fenced it for the async proxy) before.
-__device__ __forceinline__ uint32_t engine_setup(const Engine& en, const CUtensorMap* map) {
-  const int warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(en.bar(kBarFull + s), 1);
-      ptx::mbar_init(en.bar(kBarEmpty + s), 1);
-    }
-    for (int s = 0; s < kAccStages; ++s) {
-      ptx::mbar_init(en.bar(kBarAccFull + s), 1);
-      ptx::mbar_init(en.bar(kBarAccEmpty + s), 4);
-    }
-    ptx::mbar_init(en.bar(kBarDrain), 1);
-    *en.abort_flag() = 0;
-    ptx::fence_barrier_init();
-    ptx::prefetch_tensormap(map);
+// Whether page j of tile t holds a block of [g_run, g_end) with a usable page slot.
+__device__ __forceinline__ bool page_active(const int32_t* pages, int32_t g_run, int32_t g_end, int t, int j) {
+  return g_run + kTile * t + 32 * j < g_end && pages[kPagesPerTile * t + j] >= 0;
+}
+
+__device__ __forceinline__ int run_tiles(int32_t g_run, int32_t g_end) {
+  return g_end > g_run ? (g_end - g_run + kTile - 1) / kTile : 0;
+}
+
+// Tiles whose copies engine_start issues before the CTA's setup barrier: at most one
+// per stage, and none from tile `limit` on.
+__device__ __forceinline__ int pre_tiles(int nt, int limit) { return min(min(nt, kStages), limit); }
+
+// The copies of tile t into stage s, completing on its full barrier (producer thread).
+__device__ __forceinline__ void issue_tile(const Engine& en, const CUtensorMap* map, const int32_t* pages,
+                                           int32_t head_size, int32_t g_run, int32_t g_end, int t, int s) {
+  uint32_t bytes = 0;
+#pragma unroll
+  for (int j = 0; j < kPagesPerTile; ++j)
+    if (page_active(pages, g_run, g_end, t, j)) bytes += 2 * kPageBox;
+  ptx::mbar_arrive_expect_tx(en.bar(kBarFull + s), bytes);
+  const uint32_t dst = en.base + kOffA + static_cast<uint32_t>(s) * kABytes;
+#pragma unroll
+  for (int j = 0; j < kPagesPerTile; ++j) {
+    if (!page_active(pages, g_run, g_end, t, j)) continue;
+    const int32_t row = pages[kPagesPerTile * t + j] * 32;  // the page's first block
+    ptx::tma_load_3d(dst + j * kPageBox, map, en.bar(kBarFull + s), head_size, 0, row);
+    ptx::tma_load_3d(dst + kAHalf + j * kPageBox, map, en.bar(kBarFull + s), head_size + 64, 0, row);
   }
-  if (warp == 1) {
+}
+
+// Warp 0, before the CTA's setup barrier (after it staged `pages` and a __syncwarp):
+// lane 0 initialises the barriers and issues the copies of the first
+// pre_tiles(nt, limit) tiles, so that they are in flight while the other warps prepare.
+__device__ __forceinline__ void engine_start(const Engine& en, const CUtensorMap* map, const int32_t* pages,
+                                             int32_t head_size, int32_t g_run, int32_t g_end, int limit) {
+  if ((threadIdx.x & 31) != 0) return;
+  for (int s = 0; s < kStages; ++s) {
+    ptx::mbar_init(en.bar(kBarFull + s), 1);
+    ptx::mbar_init(en.bar(kBarEmpty + s), 1);
+  }
+  for (int s = 0; s < kAccStages; ++s) {
+    ptx::mbar_init(en.bar(kBarAccFull + s), 1);
+    ptx::mbar_init(en.bar(kBarAccEmpty + s), 4);
+  }
+  ptx::mbar_init(en.bar(kBarDrain), 1);
+  *en.abort_flag() = 0;
+  ptx::fence_barrier_init();
+  ptx::prefetch_tensormap(map);
+  const int np = pre_tiles(run_tiles(g_run, g_end), limit);
+  for (int t = 0; t < np; ++t) issue_tile(en, map, pages, head_size, g_run, g_end, t, t);
+}
+
+// TMEM; every thread of the CTA calls it after engine_start (contains __syncthreads).
+// The caller has written the B operand (and fenced it for the async proxy) before.
+__device__ __forceinline__ uint32_t engine_setup(const Engine& en) {
+  if ((threadIdx.x >> 5) == 1) {
     __syncwarp();
     ptx::tmem_alloc(en.base + kOffTmem, kTmemCols);
     ptx::tmem_relinquish();
@@ -166,41 +204,25 @@ __device__ __forceinline__ void engine_teardown(uint32_t tmem) {
   }
 }
 
-// Whether page j of tile t holds a block of [g_run, g_end) with a usable page slot.
-__device__ __forceinline__ bool page_active(const int32_t* pages, int32_t g_run, int32_t g_end, int t, int j) {
-  return g_run + kTile * t + 32 * j < g_end && pages[kPagesPerTile * t + j] >= 0;
-}
-
-// The roles over the run's tiles.  pages: stage_vpages of the run (visible to every
-// thread); out: the sequence's logits row; pool map: 3-D {poolHeadDim, 4 x numKVHeads,
-// 2 x numPages x 32} over the pool, box {64, 1, 32}, 128-byte swizzle.  Warps 6+ (if
-// any) return at once.
+// The roles over the run's tiles, after engine_setup.  pages: stage_vpages of the run
+// (visible to every thread); out: the sequence's logits row; pool map: 3-D
+// {poolHeadDim, 4 x numKVHeads, 2 x numPages x 32} over the pool, box {64, 1, 32},
+// 128-byte swizzle; limit: the one given to engine_start.  Warps 6+ (if any) return
+// at once.
 template <bool kBf16>
 __device__ __forceinline__ void engine_run(const Engine& en, uint32_t tmem, const CUtensorMap* map,
                                            const int32_t* pages, int32_t head_size, int32_t g_run, int32_t g_end,
-                                           float* out, float scale) {
+                                           float* out, float scale, int limit) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt = g_end > g_run ? (g_end - g_run + kTile - 1) / kTile : 0;
+  const int nt = run_tiles(g_run, g_end);
   if (warp == 0) {
     if (lane != 0) return;
-    // ---------------------------------------------------------------- producer
-    int t = 0;
+    // ------------------------------------------- producer (after engine_start's tiles)
+    int t = pre_tiles(nt, limit);
     for (; t < nt; ++t) {
       const int s = t % kStages;
       if (!wait_bounded(en, en.bar(kBarEmpty + s), ((t / kStages) & 1) ^ 1, kFaultProducer)) break;
-      uint32_t bytes = 0;
-#pragma unroll
-      for (int j = 0; j < kPagesPerTile; ++j)
-        if (page_active(pages, g_run, g_end, t, j)) bytes += 2 * kPageBox;
-      ptx::mbar_arrive_expect_tx(en.bar(kBarFull + s), bytes);
-      const uint32_t dst = en.base + kOffA + static_cast<uint32_t>(s) * kABytes;
-#pragma unroll
-      for (int j = 0; j < kPagesPerTile; ++j) {
-        if (!page_active(pages, g_run, g_end, t, j)) continue;
-        const int32_t row = pages[kPagesPerTile * t + j] * 32;  // the page's first block
-        ptx::tma_load_3d(dst + j * kPageBox, map, en.bar(kBarFull + s), head_size, 0, row);
-        ptx::tma_load_3d(dst + kAHalf + j * kPageBox, map, en.bar(kBarFull + s), head_size + 64, 0, row);
-      }
+      issue_tile(en, map, pages, head_size, g_run, g_end, t, s);
     }
     if (*en.abort_flag()) {  // the last copy issued into each stage lands before the CTA exits
       for (int s = 0; s < kStages; ++s)
