@@ -212,17 +212,43 @@ __device__ __forceinline__ void for_each_key(const K& keys, int32_t n, F&& f) {
 }
 
 // The selection of one visible row (n_vis > 512 keys): winners' block ids, ascending,
-// in sh.win[0, 512).  Ends with a CTA barrier.
-template <int T, int MW, class K>
+// in sh.win[0, 512).  Ends with a CTA barrier.  kRegs (MW == 1 only): each thread loads
+// its 32 contiguous keys once and keeps them in registers, so the ordered pass and the
+// candidate resolution read no key from memory again.
+template <int T, int MW, bool kRegs = false, class K>
 __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShared<T>& sh) {
+  static_assert(!kRegs || MW == 1, "keys in registers: one 32-key word a thread");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t k_sel = kTopK;
+  const int32_t g0 = tid * (32 * MW);
 
   // ---- 1. first-digit histogram and its threshold bin
+  uint32_t kr[kRegs ? 32 : 1];  // kRegs: keys of blocks g0 .. g0 + 31 (those >= n_vis unused)
+  if constexpr (kRegs) {
+    if (keys.vec && g0 + 32 <= n_vis) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float4 x = keys.ld4(g0 + 4 * e);
+        kr[4 * e] = orderable(x.x);
+        kr[4 * e + 1] = orderable(x.y);
+        kr[4 * e + 2] = orderable(x.z);
+        kr[4 * e + 3] = orderable(x.w);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) kr[e] = g0 + e < n_vis ? orderable(keys.ld1(g0 + e)) : 0u;
+    }
+  }
   for (int k = tid; k < kBins1 / 4; k += T) reinterpret_cast<uint4*>(sh.hist1)[k] = make_uint4(0u, 0u, 0u, 0u);
   if (tid == 0) sh.ncand = 0;
   __syncthreads();
-  for_each_key<T>(keys, n_vis, [&](uint32_t key) { atomicAdd(&sh.hist1[key >> kShift1], 1u); });
+  if constexpr (kRegs) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (g0 + e < n_vis) atomicAdd(&sh.hist1[kr[e] >> kShift1], 1u);
+  } else {
+    for_each_key<T>(keys, n_vis, [&](uint32_t key) { atomicAdd(&sh.hist1[key >> kShift1], 1u); });
+  }
   __syncthreads();
   if (warp == 0) {
     const Threshold th = find_first_digit(sh.hist1, static_cast<uint32_t>(k_sel));
@@ -241,14 +267,21 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
   const uint32_t lo1 = b1 << kShift1, hi1 = lo1 | ((1u << kShift1) - 1u);
 
   // ---- 2. ordered pass over this thread's contiguous blocks
-  const int32_t g0 = tid * (32 * MW);
   uint32_t gtm[MW], cm[MW];
 #pragma unroll
   for (int w = 0; w < MW; ++w) {
     gtm[w] = 0u;
     cm[w] = 0u;
     const int32_t gb = g0 + 32 * w;
-    if (keys.vec && gb + 32 <= n_vis) {
+    if constexpr (kRegs) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        if (gb + e < n_vis) {
+          if (kr[e] > hi1) gtm[w] |= 1u << e;
+          if ((kr[e] >> kShift1) == b1) cm[w] |= 1u << e;
+        }
+      }
+    } else if (keys.vec && gb + 32 <= n_vis) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float4 x = keys.ld4(gb + 4 * e);
@@ -280,12 +313,18 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
     if (my_cand) {
       cbase = atomicAdd(&sh.ncand, my_cand);
       uint32_t j = cbase;
+      if constexpr (kRegs) {  // the keys themselves, in ascending block order
 #pragma unroll
-      for (int w = 0; w < MW; ++w) {
-        uint32_t m = cm[w];
-        while (m) {
-          sh.hist1[j++] = static_cast<uint32_t>(g0 + 32 * w + __ffs(m) - 1);
-          m &= m - 1u;
+        for (int e = 0; e < 32; ++e)
+          if ((cm[0] >> e) & 1u) sh.hist1[j++] = kr[e];
+      } else {  // block ids; warp 0 loads their keys
+#pragma unroll
+        for (int w = 0; w < MW; ++w) {
+          uint32_t m = cm[w];
+          while (m) {
+            sh.hist1[j++] = static_cast<uint32_t>(g0 + 32 * w + __ffs(m) - 1);
+            m &= m - 1u;
+          }
         }
       }
     }
@@ -297,11 +336,13 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
     if (warp == 0) {
       const uint32_t nc = c1;
       const int nq = static_cast<int>((nc + 31u) >> 5);
-      for (int q = 0; q < nq; ++q) {  // candidates' keys, in place of their block ids
-        const uint32_t j = lane + 32u * q;
-        if (j < nc) sh.hist1[j] = orderable(keys.ld1(static_cast<int32_t>(sh.hist1[j])));
+      if constexpr (!kRegs) {
+        for (int q = 0; q < nq; ++q) {  // candidates' keys, in place of their block ids
+          const uint32_t j = lane + 32u * q;
+          if (j < nc) sh.hist1[j] = orderable(keys.ld1(static_cast<int32_t>(sh.hist1[j])));
+        }
+        __syncwarp();
       }
-      __syncwarp();
       uint32_t prefix = lo1, mask = ~((1u << kShift1) - 1u);
       int32_t rm = rem;
 #pragma unroll 1
@@ -363,9 +404,15 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
       const uint32_t dmask = (1u << width) - 1u;
       for (int k = tid; k < 256; k += T) sh.hist2[k] = 0u;
       __syncthreads();
-      for_each_key<T>(keys, n_vis, [&](uint32_t key) {
-        if ((key & mask) == prefix) atomicAdd(&sh.hist2[(key >> shift) & dmask], 1u);
-      });
+      if constexpr (kRegs) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (g0 + e < n_vis && (kr[e] & mask) == prefix) atomicAdd(&sh.hist2[(kr[e] >> shift) & dmask], 1u);
+      } else {
+        for_each_key<T>(keys, n_vis, [&](uint32_t key) {
+          if ((key & mask) == prefix) atomicAdd(&sh.hist2[(key >> shift) & dmask], 1u);
+        });
+      }
       __syncthreads();
       if (warp == 0) {
         const Threshold th = find_digit256(sh.hist2, static_cast<uint32_t>(rem));
@@ -383,15 +430,25 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
       if (sh.thr_count == static_cast<uint32_t>(rem)) break;
     }
     const uint32_t lo = prefix, hi = prefix | ~mask;
+    if constexpr (kRegs) {
 #pragma unroll
-    for (int w = 0; w < MW; ++w) {
-      uint32_t m = cm[w];
-      while (m) {
-        const int bit = __ffs(m) - 1;
-        m &= m - 1u;
-        const uint32_t key = orderable(keys.ld1(g0 + 32 * w + bit));
-        if (key > hi) gtm[w] |= 1u << bit;
-        if (key > hi || key < lo) cm[w] &= ~(1u << bit);
+      for (int e = 0; e < 32; ++e) {
+        if ((cm[0] >> e) & 1u) {
+          if (kr[e] > hi) gtm[0] |= 1u << e;
+          if (kr[e] > hi || kr[e] < lo) cm[0] &= ~(1u << e);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int w = 0; w < MW; ++w) {
+        uint32_t m = cm[w];
+        while (m) {
+          const int bit = __ffs(m) - 1;
+          m &= m - 1u;
+          const uint32_t key = orderable(keys.ld1(g0 + 32 * w + bit));
+          if (key > hi) gtm[w] |= 1u << bit;
+          if (key > hi || key < lo) cm[w] &= ~(1u << bit);
+        }
       }
     }
   }
