@@ -110,7 +110,7 @@ topk_kernel(int32_t* __restrict__ out_idx, const float* __restrict__ logits, con
   const float* row = logits + static_cast<int64_t>(i) * num_blocks;
   const GlobalKeys keys{row, (reinterpret_cast<uintptr_t>(row) & 15u) == 0};
   select_row<T, MW, DECODE && MW == 1>(keys, ri.n_vis, sh);
-  write_selected<T>(out, sh.win, ri.tail, ri.n_vis);
+  write_selected<T>(out, sh.win(), ri.tail, ri.n_vis);
 }
 
 #ifndef QSA_SEL_THREADS

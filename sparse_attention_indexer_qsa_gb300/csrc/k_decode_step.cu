@@ -141,7 +141,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
   sel::SelShared<kDecThreads>& sh = *reinterpret_cast<sel::SelShared<kDecThreads>*>(en.ptr + dtc::kOffA);
   const sel::L2Keys keys{lrow, (reinterpret_cast<uintptr_t>(lrow) & 15u) == 0};
   sel::select_row<kDecThreads, MW, MW == 1>(keys, n_vis, sh);
-  sel::write_selected<kDecThreads>(out, sh.win, tail, n_vis);
+  sel::write_selected<kDecThreads>(out, sh.win(), tail, n_vis);
 }
 
 }  // namespace dec

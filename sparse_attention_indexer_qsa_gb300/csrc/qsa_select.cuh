@@ -38,13 +38,13 @@ __device__ __forceinline__ uint32_t orderable(float f) {
 //     position of its first winner; winners are written in ascending order and the
 //     row is expanded.
 // Keys are read from global memory (L1/L2 after the first pass).  Small CTAs (64
-// threads, up to 20 a SM) keep many rows in flight: the warp-0 steps between the
-// passes are serial and would otherwise leave the SM idle.
+// threads, 8.2 KB of shared memory, 24 a SM) keep many rows in flight: the warp-0
+// steps between the passes are serial and would otherwise leave the SM idle.
 #ifndef QSA_SEL_D1_BITS
 #define QSA_SEL_D1_BITS 11
 #endif
 #ifndef QSA_SEL_WARPS_PER_SM
-#define QSA_SEL_WARPS_PER_SM 40
+#define QSA_SEL_WARPS_PER_SM 48
 #endif
 constexpr int kD1 = QSA_SEL_D1_BITS;
 constexpr int kBins1 = 1 << kD1;
@@ -55,15 +55,26 @@ constexpr int kWarpCap = 32 * kCpl;
 constexpr int kMaxBlocks = 65536;
 static_assert(kWarpCap <= kBins1, "the candidate list reuses the histogram's storage");
 
+// Shared state of one row's selection.  After the threshold search the first-digit
+// histogram is dead, and its storage holds the later steps' data: the candidate list
+// (words [0, kWarpCap)), the radix counts (words [kHist2Word, +256)), the candidates'
+// classes (bytes from word kClsWord) and, last, the winners (words [0, kTopK)).  Each
+// reuse is separated from the previous use by CTA barriers.
+constexpr int kHist2Word = 1024;
+constexpr int kClsWord = 1536;
+static_assert(kWarpCap <= kHist2Word && kTopK <= kHist2Word && kHist2Word + 256 <= kClsWord &&
+                  kClsWord + kWarpCap / 4 <= kBins1,
+              "selection shared-memory layout");
+
 template <int T>
 struct SelShared {
-  uint32_t hist1[kBins1];  // pass-1 histogram, then the candidate list
-  uint32_t hist2[256];
-  int32_t win[kTopK];
-  uint8_t cls[kWarpCap];   // per listed candidate: 2 above T, 1 tied, 0 below
+  uint32_t hist1[kBins1];
   uint32_t warp_tot[T / 32];
   uint32_t thr_bin, thr_above, thr_count, ncand;
   int32_t rem;
+  __device__ __forceinline__ uint32_t* hist2() { return hist1 + kHist2Word; }
+  __device__ __forceinline__ uint8_t* cls() { return reinterpret_cast<uint8_t*>(hist1 + kClsWord); }
+  __device__ __forceinline__ int32_t* win() { return reinterpret_cast<int32_t*>(hist1); }
 };
 
 // The visible keys of one row.
@@ -212,7 +223,7 @@ __device__ __forceinline__ void for_each_key(const K& keys, int32_t n, F&& f) {
 }
 
 // The selection of one visible row (n_vis > 512 keys): winners' block ids, ascending,
-// in sh.win[0, 512).  Ends with a CTA barrier.  kRegs (MW == 1 only): each thread loads
+// in sh.win()[0, 512).  Ends with a CTA barrier.  kRegs (MW == 1 only): each thread loads
 // its 32 contiguous keys once and keeps them in registers, so the ordered pass and the
 // candidate resolution read no key from memory again.
 template <int T, int MW, bool kRegs = false, class K>
@@ -350,18 +361,18 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
         const int width = min(8, top);
         const int shift = top - width;
         const uint32_t dmask = (1u << width) - 1u;
-        reinterpret_cast<uint4*>(sh.hist2)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
-        reinterpret_cast<uint4*>(sh.hist2)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(sh.hist2())[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(sh.hist2())[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
         for (int q = 0; q < nq; ++q) {
           const uint32_t j = lane + 32u * q;
           if (j < nc) {
             const uint32_t key = sh.hist1[j];
-            if ((key & mask) == prefix) atomicAdd(&sh.hist2[(key >> shift) & dmask], 1u);
+            if ((key & mask) == prefix) atomicAdd(&sh.hist2()[(key >> shift) & dmask], 1u);
           }
         }
         __syncwarp();
-        const Threshold th = find_digit256(sh.hist2, static_cast<uint32_t>(rm));
+        const Threshold th = find_digit256(sh.hist2(), static_cast<uint32_t>(rm));
         rm -= static_cast<int32_t>(th.above);
         prefix |= th.bin << shift;
         mask |= dmask << shift;
@@ -374,7 +385,7 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
         const uint32_t j = lane + 32u * q;
         if (j < nc) {
           const uint32_t key = sh.hist1[j];
-          sh.cls[j] = key > hi ? 2 : (key >= lo ? 1 : 0);
+          sh.cls()[j] = key > hi ? 2 : (key >= lo ? 1 : 0);
         }
       }
       if (lane == 0) sh.rem = rm;
@@ -389,7 +400,7 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
         while (m) {
           const uint32_t bit = m & (0u - m);
           m &= m - 1u;
-          const uint8_t k = sh.cls[j++];
+          const uint8_t k = sh.cls()[j++];
           if (k == 2) gtm[w] |= bit;
           if (k != 1) cm[w] &= ~bit;
         }
@@ -402,20 +413,20 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
       const int width = min(8, top);
       const int shift = top - width;
       const uint32_t dmask = (1u << width) - 1u;
-      for (int k = tid; k < 256; k += T) sh.hist2[k] = 0u;
+      for (int k = tid; k < 256; k += T) sh.hist2()[k] = 0u;
       __syncthreads();
       if constexpr (kRegs) {
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          if (g0 + e < n_vis && (kr[e] & mask) == prefix) atomicAdd(&sh.hist2[(kr[e] >> shift) & dmask], 1u);
+          if (g0 + e < n_vis && (kr[e] & mask) == prefix) atomicAdd(&sh.hist2()[(kr[e] >> shift) & dmask], 1u);
       } else {
         for_each_key<T>(keys, n_vis, [&](uint32_t key) {
-          if ((key & mask) == prefix) atomicAdd(&sh.hist2[(key >> shift) & dmask], 1u);
+          if ((key & mask) == prefix) atomicAdd(&sh.hist2()[(key >> shift) & dmask], 1u);
         });
       }
       __syncthreads();
       if (warp == 0) {
-        const Threshold th = find_digit256(sh.hist2, static_cast<uint32_t>(rem));
+        const Threshold th = find_digit256(sh.hist2(), static_cast<uint32_t>(rem));
         if (lane == 0) {
           sh.thr_bin = th.bin;
           sh.thr_above = th.above;
@@ -482,7 +493,7 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
     }
     uint32_t wm = gtm[w] | keep;
     while (wm) {
-      sh.win[pos++] = g0 + 32 * w + __ffs(wm) - 1;
+      sh.win()[pos++] = g0 + 32 * w + __ffs(wm) - 1;
       wm &= wm - 1u;
     }
   }
