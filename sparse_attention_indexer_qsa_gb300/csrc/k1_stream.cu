@@ -2,8 +2,8 @@
 // launchQsaIndexQPrep and launchQsaIndexKCompress with blockBegin = 0,
 // blockEnd = ceilDiv(S, 4), pastLen = 0, as the prefill pipeline calls them).
 //
-// One CTA (4 warps) per work unit of 32 consecutive token rows of one sequence
-// (8 compressed blocks); several CTAs per SM keep units in flight, and the hardware
+// One CTA (4 warps) per work unit of 16 consecutive token rows of one sequence
+// (4 compressed blocks); six CTAs per SM keep units in flight, and the hardware
 // hands out CTAs in address order (on GB300, persistent CTAs on a static schedule
 // drift apart and stream noticeably slower).  Thread 0 copies the unit's valid rows
 // (a prefix of the sequence, so contiguous) and their cos/sin rows into shared
@@ -31,10 +31,10 @@ namespace k1s {
 
 constexpr int kModeQK = 3;  // the one mode built: q heads and compressed k together
 #ifndef QSA_K1S_ROWS
-#define QSA_K1S_ROWS 32
+#define QSA_K1S_ROWS 16
 #endif
 #ifndef QSA_K1S_CTAS
-#define QSA_K1S_CTAS 4
+#define QSA_K1S_CTAS 6
 #endif
 constexpr int kRows = QSA_K1S_ROWS;       // token rows per unit (one CTA)
 constexpr int kWarps = 4;
@@ -67,7 +67,7 @@ struct Params {
   const uint16_t* w_k;           // mode QK only
   float eps;
   int32_t batch, seq_len, num_blocks;
-  int32_t units_per_seq;         // ceilDiv(seq_len, 32)
+  int32_t units_per_seq;         // ceilDiv(seq_len, kRows)
 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k1_stream_kernel(const P
   const int ca = chunk_a(j);
   const int cb = chunk_b(j);
   if (ok) {
-    // K1a: warp w owns rows w, w+4, ..., w+28 of the unit
+    // K1a: warp w owns rows w, w+4, w+8, ... of the unit
 #pragma unroll 1
     for (int r = warp; r < kRows; r += kWarps) {
       if (t0 + r >= p.seq_len) break;  // warp-uniform
