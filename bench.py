@@ -767,19 +767,24 @@ def run_ours(args, rank: int, world: int) -> None:
         if K_e2e:
             e2e_step(-2)
             torch.cuda.synchronize()
-        ev_out.clear()
-        ev_k1 = None
-        barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for n in range(K_e2e):
-            e2e_step(n)
-        stream.wait_stream(s_out)
-        e1.record(stream)
-        e1.synchronize()
-        barrier()
-        ms_e2e = e0.elapsed_time(e1) / K_e2e if K_e2e else float("nan")
+        # three timed blocks of K_e2e steps; the median block is reported (the host link is
+        # shared with the rest of the machine, and one disturbed block should not decide)
+        e2e_blocks = []
+        for _ in range(3 if K_e2e else 0):
+            ev_out.clear()
+            ev_k1 = None
+            barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for n in range(K_e2e):
+                e2e_step(n)
+            stream.wait_stream(s_out)
+            e1.record(stream)
+            e1.synchronize()
+            barrier()
+            e2e_blocks.append(e0.elapsed_time(e1) / K_e2e)
+        ms_e2e = sorted(e2e_blocks)[1] if K_e2e else float("nan")
     torch.cuda.synchronize()
     # the separate K1a and K1b entry points, each back to back over the same workload
     # K1b alone touches 42 MB (the K slices and kbar), which L2 would keep across
@@ -874,8 +879,9 @@ def run_ours(args, rank: int, world: int) -> None:
         "kernels": kernels,
         "e2e": {"value": whole_job_rows_per_s(rows, ms_e2e, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": K_e2e,
+                "block_ms_per_step": [round(x, 4) for x in e2e_blocks],
                 "how": "Python API, pinned host buffers; copies overlap compute across streams; "
-                       "K2 in per-sequence row chunks"},
+                       "K2 in per-sequence row chunks; the median of three timed blocks of `steps` steps"},
         "gpu_launches": 2 * K,
         "clocks": clk.summary(),
         "device_fault_flags": faults,
