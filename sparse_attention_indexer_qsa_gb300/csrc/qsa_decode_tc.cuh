@@ -14,8 +14,9 @@
 // in the prefill scoring kernel: the same operand layouts, the same MMA shape along
 // K and the same K order.
 //
-// Roles (warps of the CTA): 0 TMA producer (lane 0), 1 MMA issuer (lane 0), 2-5
-// epilogue.  Warp 1 allocates and frees TMEM.  Every mbarrier wait is bounded; a wait
+// Roles (warps of the CTA): 0 TMA producer (lane 0; engine_start issues the first
+// tiles' copies before the CTA's setup barrier, engine_run the rest), 1 MMA issuer
+// (lane 0), 2-5 epilogue.  Warp 1 allocates and frees TMEM.  Every mbarrier wait is bounded; a wait
 // that runs out sets a fault bit and the CTA's abort flag, after which the CTA waits
 // (bounded) for its own copies and MMAs and returns; that launch's logits are undefined.
 #pragma once
