@@ -10,9 +10,9 @@
 // memory with bulk asynchronous copies (cp.async.bulk, completion counted on an
 // mbarrier); the warps then run the same norm_rope_group device routine as the
 // register-streaming kernels on data read from shared memory, so outputs are
-// bit-identical to them.  Mode QK reads each 1280-byte row exactly once: reading
-// only the 256-byte K slice of every row (as a standalone K1b must) runs at well
-// under half of the bandwidth of whole-row reads on GB300.
+// bit-identical to them.  Mode QK reads each 1280-byte row once, as one contiguous
+// copy, where the two separate kernels read its 1024-byte q part and its 256-byte K
+// slice; the bytes are the same, and the pass saves one launch and its ramp.
 //
 // Padding rows (t >= contextLengths[b]) and invalid blocks are written as exact
 // zeros and are never copied.  The one mbarrier wait is bounded; a wait that runs
