@@ -388,6 +388,52 @@ def test_fused_decode_step_long_rows(dtype):
     assert qsa.qsa_device_fault_flags() == 0
 
 
+def test_fused_decode_step_at_the_batch_limit():
+    """4096 sequences (the largest batch of the one-launch step: its arrival-counter set)
+    with contexts from 1 to 2400 tokens, every input drawn on the device: the one launch
+    and the three separate calls give the same bits on every output and in the pool."""
+    qsa = _qsa()
+    B, max_ctx = 4096, 2400
+    pages = (max_ctx + 127) // 128
+    num_pages = B * pages
+    gen = torch.Generator(device="cuda").manual_seed(17)
+    pool0 = torch.randn((2 * num_pages, 128, 1, 128), device="cuda", generator=gen).to(torch.bfloat16)
+    perm = torch.randperm(num_pages, device="cuda", generator=gen).to(torch.int32).view(B, pages)
+    table = torch.stack([perm, torch.roll(perm, 1, 0) + num_pages], dim=1).contiguous()   # [B, 2, pages]
+    ctx = torch.randint(1, max_ctx + 1, (B,), device="cuda", generator=gen, dtype=torch.int32)
+    rows = torch.randn((B, 640), device="cuda", generator=gen).to(torch.bfloat16)
+    cs = torch.randn((max_ctx, 64), device="cuda", generator=gen)
+    wq = (torch.randn(128, device="cuda", generator=gen) * 0.1).to(torch.bfloat16)
+    wk = (torch.randn(128, device="cuda", generator=gen) * 0.1).to(torch.bfloat16)
+    maxb = (max_ctx + 3) // 4
+    pools = [pool0.clone(), pool0.clone()]
+    states = [qsa.pool_state(p_, table, num_pages, numKVHeads=1, poolHeadDim=128, headSize=0) for p_ in pools]
+
+    def bufs():
+        return dict(q=torch.empty((B, 1, 4, 128), dtype=torch.bfloat16, device="cuda"),
+                    logits=torch.full((B, maxb), float("nan"), device="cuda"),
+                    out=torch.empty((B, 2051), dtype=torch.int32, device="cuda"),
+                    split=torch.full((B, 4), 3, dtype=torch.int32, device="cuda"))
+    three, fused = bufs(), bufs()
+    qsa.qsa_indexer_pre_decode(three["q"], rows, cs, ctx, wq, wk, 1e-6, states[0], B)
+    qsa.qsa_index_scores_decode(three["logits"], three["q"], ctx, states[0], B, maxb)
+    qsa.qsa_topk_expand_decode(three["out"], three["logits"], ctx, three["split"], 4, B, maxb)
+    for _ in range(2):   # twice: the counters must be back at zero after the first launch
+        fused["logits"].fill_(float("nan"))
+        qsa.qsa_indexer_decode_step(fused["out"], fused["logits"], fused["q"], rows, cs, ctx, wq, wk, 1e-6,
+                                    states[1], fused["split"], 4, B, maxb)
+        torch.cuda.synchronize()
+        for name in ("q", "out", "split"):
+            assert torch.equal(three[name], fused[name]), name
+        nv = (ctx // 4).cpu().numpy()
+        lt, lf = three["logits"].cpu().numpy(), fused["logits"].cpu().numpy()
+        for b in range(B):
+            assert np.array_equal(lt[b, :nv[b]].view(np.uint32), lf[b, :nv[b]].view(np.uint32)), b
+            assert np.all(np.isnan(lf[b, nv[b]:])), b
+        assert torch.equal(pools[0], pools[1])
+    assert qsa.qsa_device_fault_flags() == 0
+
+
 def test_fused_decode_step_validation():
     qsa = _qsa()
     P = 0x1000
