@@ -231,7 +231,10 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
   static_assert(!kRegs || MW == 1, "keys in registers: one 32-key word a thread");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t k_sel = kTopK;
-  const int32_t g0 = tid * (32 * MW);
+  // 32-key words a thread owns in this row: as few as the row needs, so that short rows
+  // spread over every warp of the CTA (words past wpt stay empty)
+  const int wpt = kRegs ? 1 : min(MW, static_cast<int>((n_vis + 32 * T - 1) / (32 * T)));
+  const int32_t g0 = tid * (32 * wpt);
 
   // ---- 1. first-digit histogram and its threshold bin
   uint32_t kr[kRegs ? 32 : 1];  // kRegs: keys of blocks g0 .. g0 + 31 (those >= n_vis unused)
@@ -284,7 +287,9 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
     gtm[w] = 0u;
     cm[w] = 0u;
     const int32_t gb = g0 + 32 * w;
-    if constexpr (kRegs) {
+    if (w >= wpt) {
+      // not this row's word
+    } else if constexpr (kRegs) {
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         if (gb + e < n_vis) {
