@@ -80,7 +80,7 @@ __device__ __forceinline__ bool compress_block(const PoolDev& pool, int32_t b, i
 constexpr int kDecThreads = 256;                              // threads of the one-launch decode step
 constexpr int kDecBlocksPerCta = 128;                         // the unit a CTA's run is made of
 constexpr int kPageWindow = 128;                              // V pages a run may span
-constexpr int kDecRunMax = kPageWindow * (128 / kRatio);      // blocks a run may hold (2048)
+constexpr int kDecRunMax = kPageWindow * (128 / kRatio);      // blocks a run may hold (4096)
 constexpr int kScoresCtasPerSm = 2;                           // resident CTAs the run length assumes
 
 // Blocks per CTA (a multiple of kDecBlocksPerCta, at most kDecRunMax) so that a grid of
