@@ -434,6 +434,65 @@ def test_fused_decode_step_at_the_batch_limit():
     assert qsa.qsa_device_fault_flags() == 0
 
 
+def test_fused_decode_steps_in_flight_on_two_streams():
+    """Launches of the one-launch step overlap on two streams (each launch takes its own
+    arrival-counter set): 24 launches, alternating streams, on two independent problems,
+    each equal bit for bit to its three-call reference."""
+    qsa = _qsa()
+    B, max_ctx = 48, 3000
+    pages = (max_ctx + 1 + 127) // 128     # contexts up to max_ctx + 1
+    num_pages = B * pages
+    gen = torch.Generator(device="cuda").manual_seed(23)
+    probs = []
+    for _ in range(2):
+        pool = torch.randn((2 * num_pages, 128, 1, 128), device="cuda", generator=gen).to(torch.bfloat16)
+        perm = torch.randperm(num_pages, device="cuda", generator=gen).to(torch.int32).view(B, pages)
+        table = torch.stack([perm, perm + num_pages], dim=1).contiguous()
+        ctx = torch.randint(1, max_ctx + 1, (B,), device="cuda", generator=gen, dtype=torch.int32)
+        ctx[ctx % 4 == 0] += 1            # no block completes: the pool is only read, so launches repeat
+        rows = torch.randn((B, 640), device="cuda", generator=gen).to(torch.bfloat16)
+        st = qsa.pool_state(pool, table, num_pages, numKVHeads=1, poolHeadDim=128, headSize=0)
+        probs.append(dict(pool=pool, table=table, ctx=ctx, rows=rows, st=st))
+    cs = torch.randn((max_ctx + 8, 64), device="cuda", generator=gen)   # positions up to max_ctx
+    wq = (torch.randn(128, device="cuda", generator=gen) * 0.1).to(torch.bfloat16)
+    wk = (torch.randn(128, device="cuda", generator=gen) * 0.1).to(torch.bfloat16)
+    maxb = (max_ctx + 4) // 4
+
+    def bufs():
+        return dict(q=torch.empty((B, 1, 4, 128), dtype=torch.bfloat16, device="cuda"),
+                    logits=torch.full((B, maxb), float("nan"), device="cuda"),
+                    out=torch.empty((B, 2051), dtype=torch.int32, device="cuda"),
+                    split=torch.full((B, 2), 3, dtype=torch.int32, device="cuda"))
+    refs = []
+    for p_ in probs:
+        r = bufs()
+        qsa.qsa_indexer_pre_decode(r["q"], p_["rows"], cs, p_["ctx"], wq, wk, 1e-6, p_["st"], B)
+        qsa.qsa_index_scores_decode(r["logits"], r["q"], p_["ctx"], p_["st"], B, maxb)
+        qsa.qsa_topk_expand_decode(r["out"], r["logits"], p_["ctx"], r["split"], 2, B, maxb)
+        refs.append(r)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [[bufs() for _ in range(12)] for _ in range(2)]
+    for i in range(12):
+        for k in range(2):
+            with torch.cuda.stream(streams[k]):
+                o, p_ = outs[k][i], probs[k]
+                qsa.qsa_indexer_decode_step(o["out"], o["logits"], o["q"], p_["rows"], cs, p_["ctx"], wq, wk, 1e-6,
+                                            p_["st"], o["split"], 2, B, maxb)
+    torch.cuda.synchronize()
+    for k in range(2):
+        nv = (probs[k]["ctx"] // 4).cpu().numpy()
+        lr = refs[k]["logits"].cpu().numpy()
+        for i in range(12):
+            o = outs[k][i]
+            for name in ("q", "out", "split"):
+                assert torch.equal(refs[k][name], o[name]), (k, i, name)
+            lo = o["logits"].cpu().numpy()
+            for b in range(B):
+                assert np.array_equal(lr[b, :nv[b]].view(np.uint32), lo[b, :nv[b]].view(np.uint32)), (k, i, b)
+    assert qsa.qsa_device_fault_flags() == 0
+
+
 def test_fused_decode_step_validation():
     qsa = _qsa()
     P = 0x1000
