@@ -227,6 +227,42 @@ def test_paged_scores_layouts_and_unusable_slots(dtype, nkv, phd, hs, B, max_tok
     assert qsa.qsa_device_fault_flags() == 0
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_paged_scores_ignore_tails_past_nvis(dtype):
+    """The paged scores copy a visible block's whole page: V-tails of blocks past nVis on
+    that page (and every page after it) set to NaN change no visible score's bits."""
+    qsa, g_ = _qsa(), _gu()
+    B = 4
+    ctx = np.array([1000, 517, 4 * 96 + 3, 130], np.int32)    # nVis 250, 129, 96, 32
+    maxb = 260
+    rng = np.random.default_rng(33)
+    hp = pool_util.make_pool(B, 1100, seed=34)
+    hp.pool[...] = workloads.round_to_t(rng.standard_normal(hp.pool.shape, dtype=np.float32),
+                                        dtype).reshape(hp.pool.shape)
+    q = workloads.round_to_t(rng.standard_normal((B, 1, 4, 128)), dtype).reshape(B, 1, 4, 128)
+
+    def run(pool_h):
+        logits = torch.full((B, maxb), float("nan"), dtype=torch.float32, device="cuda")
+        qsa.qsa_index_scores_decode(logits, g_.dev(q), g_.dev(ctx), DevPool(pool_h).state, B, maxb, dtype=dtype)
+        torch.cuda.synchronize()
+        return logits.cpu().numpy()
+    clean = run(hp)
+    poisoned = oracle.Pool(hp.pool.copy(), hp.page_table, hp.num_pages)
+    nan_bits = workloads.NAN_BITS[dtype]
+    for b in range(B):
+        for g in range(int(ctx[b]) // 4, (1100 + 3) // 4):
+            tail = pool_util.v_tail(poisoned, b, g)
+            if tail is not None:
+                tail[:] = nan_bits
+    dirty = run(poisoned)
+    for b in range(B):
+        nv = int(ctx[b]) // 4
+        assert np.array_equal(clean[b, :nv].view(np.uint32), dirty[b, :nv].view(np.uint32)), b
+        assert not np.isnan(dirty[b, :nv]).any(), b
+        assert np.all(np.isnan(dirty[b, nv:])), b
+    assert qsa.qsa_device_fault_flags() == 0
+
+
 def test_bounded_wait_runs_out_reports_and_leaves_the_context_usable():
     """The decode engine's bounded wait, on an mbarrier nothing arrives on, gives up after
     its limit, sets its fault bit (read on the host, then cleared), and the next launches
