@@ -242,3 +242,24 @@ def test_topk_expand_never_reads_masked_cells():
     poisoned[poisoned == np.float32(NEG_MAX)] = np.nan
     assert np.isnan(poisoned).any()
     assert np.array_equal(_run_topk(poisoned, ctx, B, S, NB, 0), ref)
+
+
+def test_two_identical_runs_give_identical_out_idx():
+    """Two identical runs of the prefill and decode selections give bitwise-identical
+    outIdx ("Qsa Indexer Kernels", launchQsaTopKExpandDecode: determinism), with heavy
+    ties, so that tie order is part of the check."""
+    qsa, g_ = _qsa(), _gu()
+    B, S, NB = 2, 3000, 760
+    ctx = [3000, 2222]
+    lg = _logits_like_k2(B, S, NB, ctx, seed=71, levels=[0.0, 0.25, 1.0, 3.0])
+    a = _run_topk(lg, ctx, B, S, NB, 0)
+    b = _run_topk(lg, ctx, B, S, NB, 0)
+    assert np.array_equal(a, b)
+    dl = torch.from_numpy(lg[S - 8:S + 8].copy()).cuda()           # 16 rows as a decode batch
+    dctx = torch.full((16,), 4 * NB - 1, dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(2):
+        o = torch.empty((16, W), dtype=torch.int32, device="cuda")
+        qsa.qsa_topk_expand_decode(o, dl, dctx, None, 2, 16, NB)
+        outs.append(o.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
