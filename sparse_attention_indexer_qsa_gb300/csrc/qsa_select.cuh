@@ -508,34 +508,31 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
 __device__ __forceinline__ void st_s32x4(int32_t* p, int32_t a, int32_t b, int32_t c, int32_t d) {
   asm volatile("st.global.v4.s32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
-__device__ __forceinline__ void st_s32x2(int32_t* p, int32_t a, int32_t b) {
-  asm volatile("st.global.v2.s32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
-}
 
 // A selected row's 2051 token ids: win[p] expands to out[4p + j] = 4*win[p] + j
-// (16-, 8- or 4-byte stores by the row's alignment), then the causal tail tokens
-// 4*nVis + j for j < tail, then -1.
+// (16-byte stores from the row's first aligned address on), then the causal tail
+// tokens 4*nVis + j for j < tail, then -1.
 template <int T>
 __device__ __forceinline__ void write_selected(int32_t* out, const int32_t* win, int32_t tail, int32_t n_vis) {
-  const uint32_t a = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(out) >> 2) & 3u;  // out's offset in 16 B
-  for (int p = threadIdx.x; p < kTopK; p += T) {
-    const int32_t v = win[p] * kRatio;
-    int32_t* o = out + kRatio * p;
-    if (a == 0u) {
-      st_s32x4(o, v, v + 1, v + 2, v + 3);
-    } else if (a == 2u) {
-      st_s32x2(o, v, v + 1);
-      st_s32x2(o + 2, v + 2, v + 3);
-    } else {
-      o[0] = v;
-      st_s32x2(o + 1, v + 1, v + 2);
-      o[3] = v + 3;
-    }
+  // every 16-byte-aligned group of four ids with one vector store; the few ids before the
+  // row's first aligned address and after its last are written one by one
+  const int k0 = static_cast<int>((4u - (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(out) >> 2) & 3u)) & 3u);
+  const int nchunks = (kRatio * kTopK - k0) / 4;
+  for (int c = threadIdx.x; c < nchunks; c += T) {
+    const int i = k0 + 4 * c;
+    int32_t v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = win[(i + j) >> 2] * kRatio + ((i + j) & 3);
+    st_s32x4(out + i, v[0], v[1], v[2], v[3]);
   }
-  if (threadIdx.x < kRatio - 1) {
-    const int j = threadIdx.x;
-    out[kRatio * kTopK + j] = j < tail ? kRatio * n_vis + j : -1;
+  const int tail_lo = k0 + 4 * nchunks;  // ids [tail_lo, 4 * kTopK): at most 3
+  const int t = threadIdx.x;
+  if (t < k0) out[t] = win[t >> 2] * kRatio + (t & 3);
+  if (t >= k0 && t < k0 + (kRatio * kTopK - tail_lo)) {
+    const int i = tail_lo + (t - k0);
+    out[i] = win[i >> 2] * kRatio + (i & 3);
   }
+  if (t < kRatio - 1) out[kRatio * kTopK + t] = t < tail ? kRatio * n_vis + t : -1;
 }
 
 // Rows whose selection needs no logits: padded rows (all -1) and rows with at most
