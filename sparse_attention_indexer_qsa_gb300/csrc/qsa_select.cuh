@@ -203,13 +203,18 @@ __device__ __forceinline__ Threshold find_digit256(const uint32_t* hist, uint32_
   return walk_and_share(b8, 8u * static_cast<uint32_t>(31 - lane) + 7u, excl, k, excl < k && k <= incl);
 }
 
+#ifndef QSA_SEL_P1_UNROLL
+#define QSA_SEL_P1_UNROLL 1
+#endif
+constexpr int kP1Unroll = QSA_SEL_P1_UNROLL;
+
 // f(key) for every visible block, T-strided (coalesced / conflict-free).
 template <int T, class K, class F>
 __device__ __forceinline__ void for_each_key(const K& keys, int32_t n, F&& f) {
   int32_t g = threadIdx.x;
   if (keys.vec) {
     const int32_t nv = n >> 2;
-#pragma unroll 4
+#pragma unroll kP1Unroll
     for (int32_t v = threadIdx.x; v < nv; v += T) {
       const float4 x = keys.ld4(4 * v);
       f(orderable(x.x));
