@@ -207,6 +207,10 @@ __device__ __forceinline__ Threshold find_digit256(const uint32_t* hist, uint32_
 #define QSA_SEL_P1_UNROLL 1
 #endif
 constexpr int kP1Unroll = QSA_SEL_P1_UNROLL;
+#ifndef QSA_SEL_GATHER
+#define QSA_SEL_GATHER 4
+#endif
+constexpr int kGather = QSA_SEL_GATHER;  // candidate-key loads a lane keeps in flight
 
 // f(key) for every visible block, T-strided (coalesced / conflict-free).
 template <int T, class K, class F>
@@ -358,9 +362,20 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
       const uint32_t nc = c1;
       const int nq = static_cast<int>((nc + 31u) >> 5);
       if constexpr (!kRegs) {
-        for (int q = 0; q < nq; ++q) {  // candidates' keys, in place of their block ids
-          const uint32_t j = lane + 32u * q;
-          if (j < nc) sh.hist1[j] = orderable(keys.ld1(static_cast<int32_t>(sh.hist1[j])));
+        // candidates' keys, in place of their block ids: kGather loads in flight a lane
+        // before their stores, so the L2 round trips overlap
+        for (int q0 = 0; q0 < nq; q0 += kGather) {
+          float x[kGather];
+#pragma unroll
+          for (int u = 0; u < kGather; ++u) {
+            const uint32_t j = lane + 32u * (q0 + u);
+            x[u] = q0 + u < nq && j < nc ? keys.ld1(static_cast<int32_t>(sh.hist1[j])) : 0.0f;
+          }
+#pragma unroll
+          for (int u = 0; u < kGather; ++u) {
+            const uint32_t j = lane + 32u * (q0 + u);
+            if (q0 + u < nq && j < nc) sh.hist1[j] = orderable(x[u]);
+          }
         }
         __syncwarp();
       }
