@@ -108,6 +108,19 @@ __device__ __forceinline__ RopeCS lds_rope(uint32_t cs_row, int j) {
   return r;
 }
 
+// Chunks chunk_a(j) and chunk_b(j) of a staged 128-dim vector (2-byte elements at `row`).
+// Within one 16-byte load, lanes j < 4 and j >= 4 of a group would read their chunk A
+// from the same banks (bytes 16j and 128 + 16(j - 4)); lanes j >= 4 load chunk B first,
+// so each load's eight lanes of a group cover 32 distinct banks.
+template <class T>
+__device__ __forceinline__ void lds_pair(uint32_t row, int ca, int cb, int j, float (&a)[8], float (&b)[8]) {
+  const bool swap = j >= 4;
+  const uint4 first = lds_v4(row + 2 * (swap ? cb : ca));
+  const uint4 second = lds_v4(row + 2 * (swap ? ca : cb));
+  unpack8<T>(swap ? second : first, a);
+  unpack8<T>(swap ? first : second, b);
+}
+
 // valid (copied) rows of unit u: the prefix [t0, t0 + nq)
 __device__ __forceinline__ void unit_rows(const Params& p, int32_t u, int32_t& b, int32_t& t0, int32_t& nq) {
   b = u / p.units_per_seq;
@@ -160,8 +173,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k1_stream_kernel(const P
       if (r < nq) {  // warp-uniform
         const uint32_t row = base + L::kRowsOff + r * L::kRowBytes + h * (kHeadDim * 2);
         float a[8], bv[8];
-        unpack8<T>(lds_v4(row + 2 * ca), a);
-        unpack8<T>(lds_v4(row + 2 * cb), bv);
+        lds_pair<T>(row, ca, cb, j, a, bv);
         RopeCS cs{};
         if (j < 4) cs = lds_rope(base + L::kCsOff + r * kCsBytes, j);
         norm_rope_group<T>(a, bv, g1q, p.eps, cs, j, oa, ob);
@@ -183,8 +195,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k1_stream_kernel(const P
 #pragma unroll
         for (int q = 0; q < kRatio; ++q) {
           const uint32_t row = base + L::kRowsOff + (kRatio * jb + q) * L::kRowBytes + kKCol * 2;
-          unpack8<T>(lds_v4(row + 2 * ca), fa[q]);
-          unpack8<T>(lds_v4(row + 2 * cb), fb[q]);
+          lds_pair<T>(row, ca, cb, j, fa[q], fb[q]);
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
