@@ -155,7 +155,11 @@ __device__ __forceinline__ void norm_rope_group(const float (&a)[8], const float
   const float r = rsqrtf(__fadd_rn(mean_sq, eps));
   const float4* ga4 = reinterpret_cast<const float4*>(g1 + chunk_a(j));
   const float4* gb4 = reinterpret_cast<const float4*>(g1 + chunk_b(j));
-  const float4 ga0 = ga4[0], ga1 = ga4[1], gb0 = gb4[0], gb1 = gb4[1];
+  // every chunk starts on a bank that is a multiple of 8: lanes j >= 4 read each chunk's
+  // second half first, so a 16-byte load's eight lanes of a group cover 32 banks
+  const int h0 = j >= 4 ? 1 : 0;
+  const float4 pa = ga4[h0], qa = ga4[h0 ^ 1], pb = gb4[h0], qb = gb4[h0 ^ 1];
+  const float4 ga0 = h0 ? qa : pa, ga1 = h0 ? pa : qa, gb0 = h0 ? qb : pb, gb1 = h0 ? pb : qb;
   const float ga[8] = {ga0.x, ga0.y, ga0.z, ga0.w, ga1.x, ga1.y, ga1.z, ga1.w};
   const float gb[8] = {gb0.x, gb0.y, gb0.z, gb0.w, gb1.x, gb1.y, gb1.z, gb1.w};
   float ya[8], yb[8];
