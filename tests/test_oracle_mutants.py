@@ -73,6 +73,23 @@ MUTANTS = [
      "k[j] = pool_tail(ps, b, 0, QSA_COMPRESS_RATIO * g + j + 1);", 0),
     ("decode scores: unusable slot scores 0",
      "if (!k) { *out = -FLT_MAX; continue; }", "if (!k) { *out = 0.0f; continue; }", 0),
+    ("q prep: the first padding row computed",
+     "if (t >= contextLengths[b]) {", "if (t > contextLengths[b]) {", 0),
+    ("q prep: rope at position t - 1",
+     "cosSin + (int64_t)t * 64,", "cosSin + (int64_t)(t > 0 ? t - 1 : 0) * 64,", 0),
+    ("block validity: a block starting at pastLen counted as cached",
+     "return last < ctx && first >= pastLen", "return last < ctx && first > pastLen", 0),
+    ("scores: the first padded row scored",
+     "if (ctx <= 0 || t >= ctx) {", "if (ctx <= 0 || t > ctx) {", 0),
+    ("scores: relu after the head sum",
+     "float rel = fmaxf(0.0f, dot);\n      sum = sum + rel;\n    }\n    out[g] = scale * sum;",
+     "float rel = dot;\n      sum = sum + rel;\n    }\n    out[g] = scale * fmaxf(0.0f, sum);", 0),
+    ("scores: block g scored against kbar row g + 1",
+     "const uint16_t* k = kb + (int64_t)g * QSA_HEAD_DIM;",
+     "const uint16_t* k = kb + (int64_t)(g + 1 < nVis ? g + 1 : g) * QSA_HEAD_DIM;", 0),
+    ("expand: 511 blocks kept when 512 or more are visible",
+     "int32_t kSel = nVis < QSA_TOPK_BLOCKS ? nVis : QSA_TOPK_BLOCKS;",
+     "int32_t kSel = nVis < QSA_TOPK_BLOCKS ? nVis : QSA_TOPK_BLOCKS - 1;", 0),
 ]
 
 
