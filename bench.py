@@ -882,6 +882,12 @@ def run_ours(args, rank: int, world: int) -> None:
         "gbs": ab["k2"] / (ms_k2_chunked * 1e-3) / 1e9,
         "frac_of_measured_hbm": ab["k2"] / (ms_k2_chunked * 1e-3) / 1e9 / hbm_peak,
         "timed": "K2 over the same rows as consecutive 8192-row calls, back to back after the step loop"}
+    step_bytes = ab["k1_fused"] + ab["k2"]
+    step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
+    kernels["step"] = {
+        "ms": ms_step, "alg_bytes": step_bytes, "gbs": step_gbs, "frac_of_measured_hbm": step_gbs / hbm_peak,
+        "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
+        "timed": "the whole step (fused K1, then K2): ms_per_step of this line"}
 
     traffic = k2_profiled_traffic(B)
     k2_gbs = kernels["k2"]["gbs"]
