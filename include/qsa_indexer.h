@@ -269,6 +269,10 @@ int qsa_index_k_compress_paged(qsa_dtype_t dtype, void* kbar, const void* indexQ
  * [ctx - ctx % 4, ctx) (the trailing incomplete block) copy indexQk row (b, t)
  * columns [512, 640) BIT-UNMODIFIED to their K-tails.  Nothing else in the pool is
  * touched.  0 <= contextLengths[b] <= seqLen.
+ * Errors: QSA_E_NULL (indexQk, contextLengths, the pool state or its pointers),
+ *         QSA_E_DTYPE, QSA_E_SHAPE (batchSize < 1, seqLen < 1, the pool sizes),
+ *         QSA_E_ALIGN (indexQk 16-byte, contextLengths 4-byte, the pool tails),
+ *         QSA_E_CUDA.
  */
 int qsa_raw_k_tail_write_prefill(qsa_dtype_t dtype, const void* indexQk, const int32_t* contextLengths,
                                  const qsa_pool_state_t* pool, int32_t batchSize, int32_t seqLen,
@@ -286,6 +290,9 @@ int qsa_raw_k_tail_write_prefill(qsa_dtype_t dtype, const void* indexQk, const i
  *           (bit-identical to prefill); the kbar row goes to the V-tail of 4g.  If
  *           any of those page slots is unusable the block is not written.
  *  cosSin   FP32 [maxPositions, 64], maxPositions >= max ctx.
+ * Errors: QSA_E_NULL (any array, the pool state or its pointers), QSA_E_DTYPE,
+ *         QSA_E_SHAPE (batchSize < 1, the pool sizes), QSA_E_ALIGN (T and FP32
+ *         arrays 16-byte, contextLengths 4-byte, the pool tails), QSA_E_CUDA.
  */
 int qsa_indexer_pre_decode(qsa_dtype_t dtype, void* qNormed, const void* indexQk, const float* cosSin,
                            const int32_t* contextLengths, const void* wQ, const void* wK, float rmsEps,
@@ -300,6 +307,11 @@ int qsa_indexer_pre_decode(qsa_dtype_t dtype, void* qNormed, const void* indexQk
  * bit for bit, qsa_index_scores' logit of the same token given the same q and kbar.
  *  logits   [out] FP32 [batchSize, maxBlocks]; maxBlocks >= ceilDiv(max ctx, 4)
  *  qNormed  [in]  T [batchSize, 1, 4, 128] (qsa_indexer_pre_decode's output)
+ * Limit: maxBlocks <= 16776960 (65535 * 256).
+ * Errors: QSA_E_NULL (logits, qNormed, contextLengths, the pool state or its
+ *         pointers), QSA_E_DTYPE, QSA_E_SHAPE (batchSize < 1, maxBlocks outside
+ *         [1, 16776960], the pool sizes), QSA_E_ALIGN (qNormed 16-byte, logits and
+ *         contextLengths 4-byte, the pool tails), QSA_E_CUDA.
  */
 int qsa_index_scores_decode(qsa_dtype_t dtype, float* logits, const void* qNormed,
                             const int32_t* contextLengths, const qsa_pool_state_t* pool,
@@ -317,6 +329,10 @@ int qsa_index_scores_decode(qsa_dtype_t dtype, float* logits, const void* qNorme
  *  Deterministic: identical inputs give identical bits.
  *  outIdx  [out] INT32 [batchSize, 1, 2051];  logits [in] FP32 [batchSize, maxBlocks]
  *  (only [0, nVis) read).
+ * Limit: maxBlocks <= 65536.
+ * Errors: QSA_E_NULL (outIdx, logits, contextLengths; splitCounters may be NULL),
+ *         QSA_E_SHAPE (batchSize < 1, maxBlocks outside [1, 65536], numKVHeads < 0
+ *         with split counters), QSA_E_ALIGN (4-byte), QSA_E_CUDA.
  */
 int qsa_topk_expand_decode(int32_t* outIdx, const float* logits, const int32_t* contextLengths,
                            int32_t* splitCounters, int32_t numKVHeads, int32_t batchSize, int32_t maxBlocks,
