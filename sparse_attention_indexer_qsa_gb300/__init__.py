@@ -134,10 +134,19 @@ def qsa_last_error() -> str:
 
 
 def _addr(x) -> int | None:
+    """Device address of a tensor argument.  The C ABI takes dense row-major device
+    arrays, so a host tensor (whose address a kernel would dereference as a device
+    address) or a non-contiguous view (whose strides the kernels would ignore) is
+    rejected here, before anything is enqueued.  Plain ints pass through as raw
+    device addresses."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if getattr(x, "is_cuda", True) is False:
+        raise ValueError(f"expected a CUDA tensor (a device array), got one on {x.device}")
+    if hasattr(x, "is_contiguous") and not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor: the C ABI takes dense row-major arrays")
     return x.data_ptr()
 
 

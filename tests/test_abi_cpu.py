@@ -122,3 +122,24 @@ def test_product_package_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "qsa_oracle" not in text, f
+
+
+def test_binding_rejects_host_and_strided_tensors(qsa):
+    """A host tensor's address is not a device address, and the kernels ignore strides:
+    the binding refuses both before calling the library."""
+    import torch
+    host = torch.zeros((1, 8, 640), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        qsa.qsa_index_q_prep(host, host, host, host, host, 1e-6, 1, 8, stream=0)
+
+    class StridedDeviceView:  # stands in for a non-contiguous CUDA tensor
+        is_cuda = True
+
+        def is_contiguous(self):
+            return False
+
+        def data_ptr(self):
+            return P
+    with pytest.raises(ValueError, match="contiguous"):
+        qsa._addr(StridedDeviceView())
+    assert qsa._addr(None) is None and qsa._addr(P) == P
