@@ -151,17 +151,21 @@ def _addr(x) -> int | None:
 
 
 def _dtype(dtype, *tensors) -> int:
-    if dtype is not None:
-        if isinstance(dtype, str):
-            return {"bf16": QSA_BF16, "fp16": QSA_F16}[dtype]
-        return int(dtype)
+    """The T code of a call: ``dtype`` if given, else the type of its bf16/fp16 tensors.
+    Every bf16/fp16 tensor of a call must have that one type (bit-pattern tensors of
+    other dtypes, and raw addresses, are taken as given)."""
     import torch
-    for t in tensors:
-        if isinstance(t, torch.Tensor):
-            if t.dtype == torch.bfloat16:
-                return QSA_BF16
-            if t.dtype == torch.float16:
-                return QSA_F16
+    seen = {QSA_BF16 if t.dtype == torch.bfloat16 else QSA_F16 for t in tensors
+            if isinstance(t, torch.Tensor) and t.dtype in (torch.bfloat16, torch.float16)}
+    if dtype is not None:
+        code = {"bf16": QSA_BF16, "fp16": QSA_F16}[dtype] if isinstance(dtype, str) else int(dtype)
+        if seen and seen != {code}:
+            raise ValueError(f"dtype {dtype!r} does not match the tensors' element type")
+        return code
+    if len(seen) == 1:
+        return seen.pop()
+    if len(seen) > 1:
+        raise ValueError("the tensors mix bf16 and fp16: every T array of a call has one type")
     raise ValueError("dtype not given and not inferable from the tensors")
 
 
@@ -182,7 +186,7 @@ def _check(status: int):
 def qsa_index_q_prep(qNormed, indexQk, cosSin, contextLengths, wQ, rmsEps, batchSize, seqLen,
                      stream=None, dtype=None):
     """K1a: indexQk [B, S, 640] -> qNormed [B, S, 4, 128] (see include/qsa_indexer.h)."""
-    _check(load().qsa_index_q_prep(_dtype(dtype, indexQk, qNormed), _addr(qNormed), _addr(indexQk),
+    _check(load().qsa_index_q_prep(_dtype(dtype, indexQk, qNormed, wQ), _addr(qNormed), _addr(indexQk),
                                 _addr(cosSin), _addr(contextLengths), _addr(wQ), float(rmsEps),
                                 int(batchSize), int(seqLen), _stream(stream)))
 
@@ -190,7 +194,7 @@ def qsa_index_q_prep(qNormed, indexQk, cosSin, contextLengths, wQ, rmsEps, batch
 def qsa_index_k_compress(kbar, indexQk, cosSin, contextLengths, wK, rmsEps, batchSize, seqLen,
                          numBlocks, blockBegin, blockEnd, pastLen, stream=None, dtype=None):
     """K1b: rows [blockBegin, blockEnd) of kbar [B, numBlocks, 128] (see include/qsa_indexer.h)."""
-    _check(load().qsa_index_k_compress(_dtype(dtype, indexQk, kbar), _addr(kbar), _addr(indexQk),
+    _check(load().qsa_index_k_compress(_dtype(dtype, indexQk, kbar, wK), _addr(kbar), _addr(indexQk),
                                     _addr(cosSin), _addr(contextLengths), _addr(wK), float(rmsEps),
                                     int(batchSize), int(seqLen), int(numBlocks), int(blockBegin),
                                     int(blockEnd), int(pastLen), _stream(stream)))
@@ -199,7 +203,7 @@ def qsa_index_k_compress(kbar, indexQk, cosSin, contextLengths, wK, rmsEps, batc
 def qsa_index_qk_prep(qNormed, kbar, indexQk, cosSin, contextLengths, wQ, wK, rmsEps, batchSize,
                       seqLen, numBlocks, stream=None, dtype=None):
     """K1a + prefill K1b in one pass over indexQk (see include/qsa_indexer.h)."""
-    _check(load().qsa_index_qk_prep(_dtype(dtype, indexQk, qNormed, kbar), _addr(qNormed), _addr(kbar),
+    _check(load().qsa_index_qk_prep(_dtype(dtype, indexQk, qNormed, kbar, wQ, wK), _addr(qNormed), _addr(kbar),
                                  _addr(indexQk), _addr(cosSin), _addr(contextLengths), _addr(wQ),
                                  _addr(wK), float(rmsEps), int(batchSize), int(seqLen), int(numBlocks),
                                  _stream(stream)))
@@ -235,7 +239,7 @@ def qsa_index_topk_expand(outIdx, logits, contextLengths, batchSize, seqLen, num
 def qsa_index_k_compress_paged(kbar, indexQk, cosSin, contextLengths, wK, rmsEps, pool: PoolState, batchSize,
                                seqLen, numBlocks, blockBegin, blockEnd, pastLen, stream=None, dtype=None):
     """K1b that also persists valid kbar rows to the pool V-tails (see include/qsa_indexer.h)."""
-    _check(load().qsa_index_k_compress_paged(_dtype(dtype, indexQk, kbar), _addr(kbar), _addr(indexQk),
+    _check(load().qsa_index_k_compress_paged(_dtype(dtype, indexQk, kbar, wK), _addr(kbar), _addr(indexQk),
                                           _addr(cosSin), _addr(contextLengths), _addr(wK), float(rmsEps),
                                           ctypes.byref(pool), int(batchSize), int(seqLen), int(numBlocks),
                                           int(blockBegin), int(blockEnd), int(pastLen), _stream(stream)))
@@ -251,7 +255,7 @@ def qsa_raw_k_tail_write_prefill(indexQk, contextLengths, pool: PoolState, batch
 def qsa_indexer_pre_decode(qNormed, indexQk, cosSin, contextLengths, wQ, wK, rmsEps, pool: PoolState, batchSize,
                            stream=None, dtype=None):
     """Decode pre-pass: q-prep of the new token + K-tail write or block compress."""
-    _check(load().qsa_indexer_pre_decode(_dtype(dtype, indexQk, qNormed), _addr(qNormed), _addr(indexQk),
+    _check(load().qsa_indexer_pre_decode(_dtype(dtype, indexQk, qNormed, wQ, wK), _addr(qNormed), _addr(indexQk),
                                       _addr(cosSin), _addr(contextLengths), _addr(wQ), _addr(wK), float(rmsEps),
                                       ctypes.byref(pool), int(batchSize), _stream(stream)))
 
@@ -275,7 +279,7 @@ def qsa_indexer_decode_step(outIdx, logits, qNormed, indexQk, cosSin, contextLen
                             pool: PoolState, splitCounters, numKVHeads, batchSize, maxBlocks, stream=None,
                             dtype=None):
     """The decode step in one launch: pre-decode, paged scores, top-512 + expand."""
-    _check(load().qsa_indexer_decode_step(_dtype(dtype, indexQk, qNormed), _addr(outIdx), _addr(logits),
+    _check(load().qsa_indexer_decode_step(_dtype(dtype, indexQk, qNormed, wQ, wK), _addr(outIdx), _addr(logits),
                                        _addr(qNormed), _addr(indexQk), _addr(cosSin), _addr(contextLengths),
                                        _addr(wQ), _addr(wK), float(rmsEps), ctypes.byref(pool),
                                        _addr(splitCounters), int(numKVHeads), int(batchSize), int(maxBlocks),

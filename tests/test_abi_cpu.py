@@ -143,3 +143,20 @@ def test_binding_rejects_host_and_strided_tensors(qsa):
     with pytest.raises(ValueError, match="contiguous"):
         qsa._addr(StridedDeviceView())
     assert qsa._addr(None) is None and qsa._addr(P) == P
+
+
+def test_binding_dtype_must_match_the_tensors(qsa):
+    """One T per call: bf16 and fp16 tensors are not mixed, and an explicit dtype agrees
+    with them (checked before any address is taken)."""
+    import torch
+    bf = torch.zeros((1, 8, 640), dtype=torch.bfloat16)
+    fp = torch.zeros((1, 8, 4, 128), dtype=torch.float16)
+    bits = torch.zeros((128,), dtype=torch.int16)
+    with pytest.raises(ValueError, match="mix"):
+        qsa.qsa_index_q_prep(fp, bf, P, P, bits, 1e-6, 1, 8, stream=0)
+    with pytest.raises(ValueError, match="does not match"):
+        qsa.qsa_index_q_prep(P, bf, P, P, bits, 1e-6, 1, 8, stream=0, dtype="fp16")
+    with pytest.raises(ValueError, match="inferable"):
+        qsa.qsa_index_q_prep(P, P, P, P, bits, 1e-6, 1, 8, stream=0)
+    assert qsa._dtype("fp16", bits, P) == qsa.QSA_F16      # bit-pattern tensors: dtype as given
+    assert qsa._dtype(None, bits, bf) == qsa.QSA_BF16
