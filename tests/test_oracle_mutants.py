@@ -87,6 +87,26 @@ MUTANTS = [
     ("scores: block g scored against kbar row g + 1",
      "const uint16_t* k = kb + (int64_t)g * QSA_HEAD_DIM;",
      "const uint16_t* k = kb + (int64_t)(g + 1 < nVis ? g + 1 : g) * QSA_HEAD_DIM;", 0),
+    ("pre-decode: q rotated one position early",
+     "qsa_oracle_norm_rope(dtype, x, wQ, eps, cosSin + (int64_t)pos * 64, q + h * QSA_HEAD_DIM);",
+     "qsa_oracle_norm_rope(dtype, x, wQ, eps, cosSin + (int64_t)(pos > 0 ? pos - 1 : 0) * 64, q + h * QSA_HEAD_DIM);",
+     0),
+    ("pre-decode: the new row's raw K written to the K-tail of the previous token",
+     "uint16_t* dst = pool_tail(ps, b, 0, pos);", "uint16_t* dst = pool_tail(ps, b, 0, pos - 1);", 0),
+    ("pre-decode: the new row averaged first",
+     "qsa_oracle_block_mean(dtype, k[0], k[1], k[2], k[3], m);",
+     "qsa_oracle_block_mean(dtype, k[3], k[0], k[1], k[2], m);", 0),
+    ("raw K-tail write: the last token of the incomplete block skipped",
+     "t < c && t < S; ++t) {", "t < c - 1 && t < S; ++t) {", 0),
+    ("decode top-k: causal tail shifted one token",
+     "for (int32_t j = 0; j < tail; ++j) out[n++] = QSA_COMPRESS_RATIO * nVis + j;",
+     "for (int32_t j = 0; j < tail; ++j) out[n++] = QSA_COMPRESS_RATIO * nVis + j + 1;", 0),
+    ("decode top-k: split counters left as they were",
+     "splitCounters[(int64_t)b * numKVHeads + h] = 0;",
+     "splitCounters[(int64_t)b * numKVHeads + h] = splitCounters[(int64_t)b * numKVHeads + h];", 0),
+    ("decode scores: an incomplete block counted as visible",
+     "int32_t nVis = c > 0 ? c / QSA_COMPRESS_RATIO : 0;",
+     "int32_t nVis = c > 0 ? (c + 3) / QSA_COMPRESS_RATIO : 0;", 0),
     ("expand: 511 blocks kept when 512 or more are visible",
      "int32_t kSel = nVis < QSA_TOPK_BLOCKS ? nVis : QSA_TOPK_BLOCKS;",
      "int32_t kSel = nVis < QSA_TOPK_BLOCKS ? nVis : QSA_TOPK_BLOCKS - 1;", 0),
