@@ -7,8 +7,8 @@ separate K1a and K1b entry points are timed too.  Prints ONE JSON line on rank 0
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
---impl reference times the CPU oracle (the plain C restatement, single thread)
-on a bounded sample of the same workload and reports the same metric.
+--impl reference times the CPU oracle (the plain C restatement, on every host
+core) over whole steps of the same workload and reports the same metric.
 With N > 1 (torchrun) every rank runs its own replica of the workload: the rows
 are independent, there is no exchange step (weak scaling); rank 0 prints
 rows of all ranks / max-over-ranks time.
@@ -591,167 +591,259 @@ def whole_job_rows_per_s(rows_per_rank: int, ms_max: float, world: int) -> float
     return world * rows_per_rank / (ms_max * 1e-3)
 
 
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own replica of the scoring workload: seed 4 on rank 0."""
+    return 4 + rank
+
+
+def rank_workload(batch: int, rank: int):
+    import workloads
+    return workloads.scoring("bf16", seed=rank_seed(rank), B=batch, full_context=True)
+
+
+L2_NOTE = ("inputs larger than L2 (indexQk 168 MB, qNormed 134 MB) and each step writes "
+           "2.15 GB of logits, which evicts L2 between steps")
+
+
+def step_config(B: int, S: int, NB: int) -> dict:
+    """The workload both arms run, printed identically by both."""
+    return {"workload": WORKLOAD.format(B=B), "B": B, "S": S, "num_blocks": NB, "rows_per_step": B * S,
+            "k2_row_chunk": B * S, "l2": L2_NOTE}
+
+
+def base_line(args, world: int, wl, ms_step: float) -> dict:
+    rows = wl.B * wl.S
+    return {"metric": METRIC, "value": whole_job_rows_per_s(rows, ms_step, world), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": step_config(wl.B, wl.S, wl.num_blocks)}
+
+
+def run_steps(args, rank: int, world: int, make_impl):
+    """One rank of a bench run: this rank's seeded workload, W warm-up steps, K timed
+    steps between barriers on the impl's own clock, the slowest rank's time, and ONE
+    JSON line printed by rank 0 (returned there; None on the other ranks).
+
+    make_impl(args, wl, rank, world) supplies the step: PrefillStepGpu for the GPU
+    arm.  It provides step(), sync(), check(), sampler() (a context whose value has
+    summary()), time_steps(K) -> ms for K steps, after_timed(args, world) (work that
+    runs inside the clock sampling) and report(...) -> the line's other keys."""
+    wl = rank_workload(args.batch, rank)
+    impl = make_impl(args, wl, rank, world)
+    for _ in range(args.warmup):
+        impl.step()
+    impl.sync()
+    impl.check()
+    with impl.sampler() as clk:
+        rank_barrier(world)
+        impl.sync()
+        ms_total = impl.time_steps(args.steps)
+        impl.sync()
+        rank_barrier(world)
+        after = impl.after_timed(args, world)
+    ms_step = max_over_ranks_of(ms_total / args.steps, world)
+    extra = impl.report(args, world, ms_step, after, clk.summary())
+    if rank != 0:
+        return None
+    line = base_line(args, world, wl, ms_step)
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def oracle_full_step(wl, pool, threads: int, logits: np.ndarray, piece: int = 256) -> None:
+    """One whole step of the CPU oracle on `threads` host threads: K1a over every row,
+    K1b over every block (both in 512-row slabs of each sequence), then K2 over every
+    row in `piece`-row pieces into `logits` [B*S, NB].  Its C calls release the GIL."""
+    import oracle
+    B, S, NB = wl.B, wl.S, wl.num_blocks
+    dtype = wl.dtype
+    qn = np.empty((B, S, 4, 128), np.uint16)
+    kb = np.zeros((B, NB, 128), np.uint16)
+    slab = 512
+
+    def k1(job):
+        b, lo = job
+        hi = min(S, lo + slab)
+        c = np.array([min(max(int(wl.context_lengths[b]) - lo, 0), hi - lo)], np.int32)
+        iq = wl.index_qk[b:b + 1, lo:hi]
+        qn[b, lo:hi] = oracle.q_prep(dtype, iq, wl.cos_sin[lo:], c, wl.w_q, wl.eps)[0]
+        nb = (hi - lo) // 4
+        kb[b, lo // 4:lo // 4 + nb] = oracle.k_compress(dtype, iq, wl.cos_sin[lo:], c, wl.w_k, wl.eps,
+                                                        nb, 0, nb, 0)[0]
+
+    list(pool.map(k1, [(b, lo) for b in range(B) for lo in range(0, S, slab)]))
+    rows = B * S
+
+    def k2(r0):
+        n = min(piece, rows - r0)
+        logits[r0:r0 + n] = oracle.scores(dtype, qn, kb, wl.context_lengths, r0, n)
+
+    list(pool.map(k2, range(0, rows, piece)))
+
+
 def run_reference(args, rank: int) -> None:
+    """The reference arm: the CPU oracle as it stands, on all host cores, timed over
+    whole steps of the workload when W + K of them fit the time budget, otherwise on a
+    bounded sample of each step scaled to a full step (the line then says so)."""
     if rank != 0:
         return
-    import workloads
-    wl = workloads.scoring("bf16", full_context=True)
-    budget = max(1.0, 100.0 / max(1, args.steps + args.warmup))
-    for i in range(args.warmup):
-        oracle_sample(wl, budget_s=budget, seed=i)
-    vals, t_total = [], 0.0
+    import concurrent.futures as cf
+    wl = rank_workload(args.batch, 0)
+    B, S, NB = wl.B, wl.S, wl.num_blocks
+    rows = B * S
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    budget_s = 300.0
+    probe = oracle_sample(wl, budget_s=2.0, seed=0, threads=threads)
+    whole = probe["est_step_s"] * (args.steps + args.warmup) <= budget_s
+    vals = []
     res = None
-    for i in range(args.steps):
-        a = time.perf_counter()
-        res = oracle_sample(wl, budget_s=budget, seed=1000 + i)
-        t_total += time.perf_counter() - a
-        vals.append(res["value"])
+    if whole:
+        pool = cf.ThreadPoolExecutor(max_workers=threads)
+        logits = np.empty((rows, NB), np.float32)
+        for _ in range(args.warmup):
+            oracle_full_step(wl, pool, threads, logits)
+        for _ in range(args.steps):
+            a = time.perf_counter()
+            oracle_full_step(wl, pool, threads, logits)
+            vals.append(rows / (time.perf_counter() - a))
+        pool.shutdown()
+        sample = (f"whole steps: K1a over all {rows} rows, K1b over all {B * NB} blocks and K2 over all "
+                  f"{rows} rows, on {threads} host threads (disjoint rows); the median of {args.steps} "
+                  f"timed steps after {args.warmup} warm-up steps")
+    else:
+        budget = max(1.0, budget_s / max(1, args.steps + args.warmup))
+        for i in range(args.warmup):
+            oracle_sample(wl, budget_s=budget, seed=i, threads=threads)
+        for i in range(args.steps):
+            res = oracle_sample(wl, budget_s=budget, seed=1000 + i, threads=threads)
+            vals.append(res["value"])
+        sample = res["sample"]
     value = statistics.median(vals)
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1000.0 * wl.B * wl.S / value, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD.format(B=wl.B), "B": wl.B, "S": wl.S, "num_blocks": wl.num_blocks},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": res["cores"], "kind": "oracle",
-                         "sample": res["sample"]},
+    line = base_line(args, 1, wl, 1000.0 * rows / value)
+    line.update({
+        "impl": "reference", "n_gpus": args.gpus, "dtype": "f32",
+        "extrapolated": not whole,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
-    }
+    })
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank: int, world: int) -> None:
-    import torch
-    import sparse_attention_indexer_qsa_gb300 as qsa
-    import workloads
+class PrefillStepGpu:
+    """The GPU arm's step for run_steps: fused K1 (qsa_index_qk_prep), then K2 over every
+    row, on this rank's workload resident in HBM; plus the legs reported beside it."""
 
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    wl = workloads.scoring("bf16", seed=4 + rank, B=args.batch, full_context=True)
-    B, S, NB = wl.B, wl.S, wl.num_blocks
-    rows = B * S
+    def __init__(self, args, wl, rank: int, world: int):
+        import torch
+        import sparse_attention_indexer_qsa_gb300 as qsa
+        self.torch, self.qsa, self.wl, self.rank = torch, qsa, wl, rank
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(self.local)
+        B, S, NB = wl.B, wl.S, wl.num_blocks
+        self.B, self.S, self.NB, self.rows = B, S, NB, B * S
+        dev = lambda a: self.host(a).cuda()
+        self.iq = dev(wl.index_qk).view(torch.bfloat16)
+        self.cs, self.ctx = dev(wl.cos_sin), dev(wl.context_lengths)
+        self.wq, self.wk = dev(wl.w_q).view(torch.bfloat16), dev(wl.w_k).view(torch.bfloat16)
+        self.qn = torch.empty((B, S, 4, 128), dtype=torch.bfloat16, device="cuda")
+        self.kb = torch.empty((B, NB, 128), dtype=torch.bfloat16, device="cuda")
+        self.logits = torch.empty((self.rows, NB), dtype=torch.float32, device="cuda")
+        self.stream = torch.cuda.current_stream()
+        self.sp = self.stream.cuda_stream
+        self.lib = qsa.load()
+        self.eps = wl.eps
+        self.evs = []
+
+    @staticmethod
     def host(a):
+        import torch
         a = np.ascontiguousarray(a)
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
 
-    dev = lambda a: host(a).cuda()
-    iq = dev(wl.index_qk).view(torch.bfloat16)
-    cs, ctx = dev(wl.cos_sin), dev(wl.context_lengths)
-    wq, wk = dev(wl.w_q).view(torch.bfloat16), dev(wl.w_k).view(torch.bfloat16)
-    qn = torch.empty((B, S, 4, 128), dtype=torch.bfloat16, device="cuda")
-    kb = torch.empty((B, NB, 128), dtype=torch.bfloat16, device="cuda")
-    logits = torch.empty((rows, NB), dtype=torch.float32, device="cuda")
-    stream = torch.cuda.current_stream()
-    sp = stream.cuda_stream
-    lib = qsa.load()
-    eps = wl.eps
-
-    def step(ev=None):
+    def step(self, ev=None):
         # K1a + K1b (prefill range) in one pass over indexQk, then K2 over every row
+        lib, qsa, stream = self.lib, self.qsa, self.stream
         if ev is not None:
             ev[0].record(stream)
-        st = lib.qsa_index_qk_prep(qsa.QSA_BF16, qn.data_ptr(), kb.data_ptr(), iq.data_ptr(), cs.data_ptr(),
-                                   ctx.data_ptr(), wq.data_ptr(), wk.data_ptr(), eps, B, S, NB, sp)
+        st = lib.qsa_index_qk_prep(qsa.QSA_BF16, self.qn.data_ptr(), self.kb.data_ptr(), self.iq.data_ptr(),
+                                   self.cs.data_ptr(), self.ctx.data_ptr(), self.wq.data_ptr(), self.wk.data_ptr(),
+                                   self.eps, self.B, self.S, self.NB, self.sp)
         if ev is not None:
             ev[1].record(stream)
-        st |= lib.qsa_index_scores(qsa.QSA_BF16, logits.data_ptr(), qn.data_ptr(), kb.data_ptr(), ctx.data_ptr(),
-                                   B, S, NB, 0, rows, sp)
+        st |= lib.qsa_index_scores(qsa.QSA_BF16, self.logits.data_ptr(), self.qn.data_ptr(), self.kb.data_ptr(),
+                                   self.ctx.data_ptr(), self.B, self.S, self.NB, 0, self.rows, self.sp)
         if ev is not None:
             ev[2].record(stream)
         if st != 0:
             raise RuntimeError(qsa.qsa_last_error())
 
-    def k1a_only():
-        if lib.qsa_index_q_prep(qsa.QSA_BF16, qn.data_ptr(), iq.data_ptr(), cs.data_ptr(), ctx.data_ptr(),
-                                wq.data_ptr(), eps, B, S, sp) != 0:
-            raise RuntimeError(qsa.qsa_last_error())
+    def sync(self):
+        self.torch.cuda.synchronize()
 
-    def k1b_only():
-        if lib.qsa_index_k_compress(qsa.QSA_BF16, kb.data_ptr(), iq.data_ptr(), cs.data_ptr(), ctx.data_ptr(),
-                                    wk.data_ptr(), eps, B, S, NB, 0, NB, 0, sp) != 0:
-            raise RuntimeError(qsa.qsa_last_error())
+    def check(self):
+        assert self.qsa.qsa_device_fault_flags() == 0
 
-    def loop_ms(fn, n):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        for _ in range(3):
-            fn()
-        e0.record(stream)
-        for _ in range(n):
-            fn()
-        e1.record(stream)
-        e1.synchronize()
-        return e0.elapsed_time(e1) / n
+    def sampler(self):
+        return ClockSampler(smi_device_id(self.local))
 
-    def barrier():
-        rank_barrier(world)
-
-    def max_over_ranks(x: float) -> float:
-        return max_over_ranks_of(x, world)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    assert qsa.qsa_device_fault_flags() == 0
-
-    dev_id = smi_device_id(local)
-
-    K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    with ClockSampler(dev_id) as clk:
-        # ---- device-timed region: inputs resident in HBM
-        barrier()
-        torch.cuda.synchronize()
+    def time_steps(self, K: int) -> float:
+        """K steps on the device clock (CUDA events on the launching stream), with
+        per-kernel events inside each step."""
+        torch = self.torch
+        self.evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
+        start.record(self.stream)
         for i in range(K):
-            step(evs[i])
-        end.record(stream)
+            self.step(self.evs[i])
+        end.record(self.stream)
         end.synchronize()
-        torch.cuda.synchronize()
-        barrier()
-        ms_total = start.elapsed_time(end)
+        return start.elapsed_time(end)
 
-        # ---- end-to-end through the public API with host buffers: every step copies
-        # its inputs in from pinned memory and its logits out to pinned memory.  The
-        # copies run on their own streams and overlap compute: step n+1's inputs go in
-        # while step n's logits come out, and K2 runs in row chunks whose logits are
-        # copied out as soon as each chunk is done (logits double-buffered).
-        K_e2e = 0 if args.no_e2e else max(3, min(K, 20))
+    def after_timed(self, args, world: int) -> dict:
+        """End-to-end through the public API with host buffers: every step copies its
+        inputs in from pinned memory and its logits out to pinned memory.  The copies
+        run on their own streams and overlap compute: step n+1's inputs go in while
+        step n's logits come out, and K2 runs in row chunks whose logits are copied out
+        as soon as each chunk is done (logits double-buffered)."""
+        torch, qsa, wl = self.torch, self.qsa, self.wl
+        B, S, NB, rows, stream, sp, eps = self.B, self.S, self.NB, self.rows, self.stream, self.sp, self.eps
+        qn, kb = self.qn, self.kb
+        K_e2e = 0 if args.no_e2e else max(3, min(args.steps, 20))
+        host = self.host
         h_in = [host(wl.index_qk).pin_memory(), host(wl.cos_sin).pin_memory(),
                 host(wl.context_lengths).pin_memory(), host(wl.w_q).pin_memory(), host(wl.w_k).pin_memory()]
         d_in = [torch.empty_like(h, device="cuda") for h in h_in]
         h2d = sum(t.numel() * t.element_size() for t in h_in)
         n_chunks = B
         chunk = rows // n_chunks
-        h_logits = [torch.empty((rows, NB), dtype=torch.float32).pin_memory() for _ in range(2)]
-        d_logits = [logits, torch.empty_like(logits)] if K_e2e else [logits]
+        h_logits = [torch.empty((rows, NB), dtype=torch.float32).pin_memory() for _ in range(2)] if K_e2e else []
+        d_logits = [self.logits, torch.empty_like(self.logits)] if K_e2e else [self.logits]
         d2h = rows * NB * 4
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-        ev_k1 = None
+        state = {"ev_k1": None}
         ev_out = {}
 
         def e2e_step(n):
-            nonlocal ev_k1
             d_iq, d_cs, d_ctx, d_wq, d_wk = d_in
             with torch.cuda.stream(s_in):
-                if ev_k1 is not None:
-                    s_in.wait_event(ev_k1)           # the previous step has consumed the inputs
+                if state["ev_k1"] is not None:
+                    s_in.wait_event(state["ev_k1"])   # the previous step has consumed the inputs
                 for h, d in zip(h_in, d_in):
                     d.copy_(h, non_blocking=True)
                 ev_in = torch.cuda.Event()
                 ev_in.record(s_in)
             stream.wait_event(ev_in)
             qsa.qsa_index_qk_prep(qn, kb, d_iq, d_cs, d_ctx, d_wq, d_wk, eps, B, S, NB, stream=sp, dtype="bf16")
-            ev_k1 = torch.cuda.Event()
-            ev_k1.record(stream)
+            state["ev_k1"] = torch.cuda.Event()
+            state["ev_k1"].record(stream)
             buf = d_logits[n % 2]
             for c in range(n_chunks):
                 prev = ev_out.get((n - 2, c))
                 if prev is not None:
-                    stream.wait_event(prev)         # this logits chunk has been copied out
+                    stream.wait_event(prev)           # this logits chunk has been copied out
                 qsa.qsa_index_scores(buf[c * chunk:(c + 1) * chunk], qn, kb, d_ctx, B, S, NB, c * chunk, chunk,
                                      stream=sp, dtype="bf16")
                 ev_c = torch.cuda.Event()
@@ -769,11 +861,11 @@ def run_ours(args, rank: int, world: int) -> None:
             torch.cuda.synchronize()
         # three timed blocks of K_e2e steps; the median block is reported (the host link is
         # shared with the rest of the machine, and one disturbed block should not decide)
-        e2e_blocks = []
+        blocks = []
         for _ in range(3 if K_e2e else 0):
             ev_out.clear()
-            ev_k1 = None
-            barrier()
+            state["ev_k1"] = None
+            rank_barrier(world)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -782,152 +874,172 @@ def run_ours(args, rank: int, world: int) -> None:
             stream.wait_stream(s_out)
             e1.record(stream)
             e1.synchronize()
-            barrier()
-            e2e_blocks.append(e0.elapsed_time(e1) / K_e2e)
-        ms_e2e = sorted(e2e_blocks)[1] if K_e2e else float("nan")
-    torch.cuda.synchronize()
-    # the separate K1a and K1b entry points, each back to back over the same workload
-    # K1b alone touches 42 MB (the K slices and kbar), which L2 would keep across
-    # back-to-back launches: each standalone launch runs after an L2 flush instead
-    l2_flush = torch.empty(2 * torch.cuda.get_device_properties(local).L2_cache_size, dtype=torch.uint8,
-                           device="cuda")
+            rank_barrier(world)
+            blocks.append(e0.elapsed_time(e1) / K_e2e)
+        ms_e2e = sorted(blocks)[1] if K_e2e else float("nan")
+        return {"ms_e2e": ms_e2e, "K_e2e": K_e2e, "blocks": blocks, "h2d": h2d, "d2h": d2h}
 
-    def cold_ms(fn, n):
-        for _ in range(3):
-            fn()
-        ts = []
-        for _ in range(n):
-            l2_flush.fill_(1)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-            e1.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        return statistics.median(ts)
+    def report(self, args, world: int, ms_step: float, after: dict, clocks: dict) -> dict:
+        torch, qsa, lib, wl = self.torch, self.qsa, self.lib, self.wl
+        B, S, NB, rows, stream, sp, eps = self.B, self.S, self.NB, self.rows, self.stream, self.sp, self.eps
+        qn, kb, iq, cs, ctx, wq, wk, logits = (self.qn, self.kb, self.iq, self.cs, self.ctx, self.wq, self.wk,
+                                               self.logits)
+        K = args.steps
+        torch.cuda.synchronize()
 
-    ms_k1a = cold_ms(k1a_only, max(K // 4, 20))
-    ms_k1b = cold_ms(k1b_only, max(K // 4, 20))
-    # prefill selection on the step's logits (top-512 blocks per row -> 2051 token ids)
-    out_idx = torch.empty((rows, 2051), dtype=torch.int32, device="cuda")
-
-    def select_only():
-        if lib.qsa_index_topk_expand(out_idx.data_ptr(), logits.data_ptr(), ctx.data_ptr(), B, S, NB, 0, rows,
-                                     sp) != 0:
-            raise RuntimeError(qsa.qsa_last_error())
-
-    ms_sel = loop_ms(select_only, max(10, K // 10))
-
-    # K2 over the same rows in 8192-row chunks (rowStart, numRows), as a caller that bounds
-    # its logits buffer would call it: all chunks back to back, per step
-    chunk_rows = 8192
-
-    def k2_chunked():
-        for r0 in range(0, rows, chunk_rows):
-            n = min(chunk_rows, rows - r0)
-            if lib.qsa_index_scores(qsa.QSA_BF16, logits.data_ptr() + r0 * NB * 4, qn.data_ptr(), kb.data_ptr(),
-                                    ctx.data_ptr(), B, S, NB, r0, n, sp) != 0:
+        def k1a_only():
+            if lib.qsa_index_q_prep(qsa.QSA_BF16, qn.data_ptr(), iq.data_ptr(), cs.data_ptr(), ctx.data_ptr(),
+                                    wq.data_ptr(), eps, B, S, sp) != 0:
                 raise RuntimeError(qsa.qsa_last_error())
 
-    ms_k2_chunked = loop_ms(k2_chunked, max(10, K // 10))
+        def k1b_only():
+            if lib.qsa_index_k_compress(qsa.QSA_BF16, kb.data_ptr(), iq.data_ptr(), cs.data_ptr(), ctx.data_ptr(),
+                                        wk.data_ptr(), eps, B, S, NB, 0, NB, 0, sp) != 0:
+                raise RuntimeError(qsa.qsa_last_error())
 
-    # the whole prefill indexer pipeline a caller runs: K1 (one pass), K2, then the top-512
-    # selection with expand, back to back on the stream
-    def pipeline():
-        step()
-        select_only()
+        def loop_ms(fn, n):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            for _ in range(3):
+                fn()
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1) / n
 
-    ms_pipeline = loop_ms(pipeline, max(10, K // 10))
-    decode = None if args.no_decode else decode_leg(qsa, lib, stream, K, B=args.decode_batch)
-    k1_small = None if args.no_sweep or rank != 0 else k1_configs_leg(qsa, lib, load_peaks()[0])
-    torch.cuda.synchronize()
-    faults = qsa.qsa_device_fault_flags()
+        # the separate K1a and K1b entry points, each back to back over the same workload.
+        # K1b alone touches 42 MB (the K slices and kbar), which L2 would keep across
+        # back-to-back launches: each standalone launch runs after an L2 flush instead
+        l2_flush = torch.empty(2 * torch.cuda.get_device_properties(self.local).L2_cache_size, dtype=torch.uint8,
+                               device="cuda")
 
-    ms_step = max_over_ranks(ms_total / K)
-    ms_e2e = max_over_ranks(ms_e2e)
-    per_kernel = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
-                  for j, n in enumerate(("k1_fused", "k2"))}
-    per_kernel["k1a"] = ms_k1a
-    per_kernel["k1b"] = ms_k1b
-    per_kernel["select"] = ms_sel
-    if rank != 0:
-        return
+        def cold_ms(fn, n):
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(n):
+                l2_flush.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            return statistics.median(ts)
 
-    hbm_peak, tf_peak, peak_src = load_peaks()
-    ab = algorithmic_bytes(wl.context_lengths, B, S, NB)
-    ab["k1_fused"] = ab["k1a"] + ab["k1b"]
-    kernels = {}
-    for n in ("k1_fused", "k2", "k1a", "k1b", "select"):
-        gbs = ab[n] / (per_kernel[n] * 1e-3) / 1e9
-        kernels[n] = {"ms": per_kernel[n], "alg_bytes": ab[n], "gbs": gbs,
-                      "frac_of_measured_hbm": gbs / hbm_peak, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS}
-    kernels["k1_fused"]["rows_per_s"] = rows / (per_kernel["k1_fused"] * 1e-3)
-    kernels["k1_fused"]["timed"] = "inside the step (CUDA events around the launch)"
-    for n in ("k1a", "k1b"):
-        kernels[n]["timed"] = "separate entry point after the step loop; each launch after an L2 flush, median"
-    kernels["select"]["timed"] = "separate entry point, back-to-back launches after the step loop (1 GB of logits)"
-    kernels["select"]["rows_per_s"] = rows / (per_kernel["select"] * 1e-3)
-    kernels["k1a"]["rows_per_s"] = rows / (per_kernel["k1a"] * 1e-3)
-    kernels["k1b"]["blocks_per_s"] = B * NB / (per_kernel["k1b"] * 1e-3)
-    kernels["k1b"]["token_rows_per_s"] = 4 * B * NB / (per_kernel["k1b"] * 1e-3)
-    kernels["k2"]["rows_per_s"] = rows / (per_kernel["k2"] * 1e-3)
-    kernels["k2"]["causal_tflops"] = ab["k2_causal_flops"] / (per_kernel["k2"] * 1e-3) / 1e12
-    kernels["k2"]["frac_of_measured_bf16_peak"] = kernels["k2"]["causal_tflops"] / tf_peak
-    kernels["prefill_pipeline"] = {
-        "ms": ms_pipeline, "rows_per_s": rows / (ms_pipeline * 1e-3),
-        "timed": "qsa_index_qk_prep, qsa_index_scores and qsa_index_topk_expand back to back, per step"}
-    kernels["k2_chunked_8192"] = {
-        "ms": ms_k2_chunked, "chunks": (rows + chunk_rows - 1) // chunk_rows,
-        "gbs": ab["k2"] / (ms_k2_chunked * 1e-3) / 1e9,
-        "frac_of_measured_hbm": ab["k2"] / (ms_k2_chunked * 1e-3) / 1e9 / hbm_peak,
-        "timed": "K2 over the same rows as consecutive 8192-row calls, back to back after the step loop"}
-    step_bytes = ab["k1_fused"] + ab["k2"]
-    step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
-    kernels["step"] = {
-        "ms": ms_step, "alg_bytes": step_bytes, "gbs": step_gbs, "frac_of_measured_hbm": step_gbs / hbm_peak,
-        "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
-        "timed": "the whole step (fused K1, then K2): ms_per_step of this line"}
+        ms_k1a = cold_ms(k1a_only, max(K // 4, 20))
+        ms_k1b = cold_ms(k1b_only, max(K // 4, 20))
+        # prefill selection on the step's logits (top-512 blocks per row -> 2051 token ids)
+        out_idx = torch.empty((rows, 2051), dtype=torch.int32, device="cuda")
 
-    traffic = k2_profiled_traffic(B)
-    k2_gbs = kernels["k2"]["gbs"]
-    line = {
-        "metric": METRIC,
-        "value": whole_job_rows_per_s(rows, ms_step, world),
-        "unit": UNIT,
-        "n_gpus": world,
-        "steps": K,
-        "warmup": args.warmup,
-        "ms_per_step": ms_step,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD.format(B=B), "B": B, "S": S, "num_blocks": NB, "rows_per_step": rows,
-                   "k2_row_chunk": rows,
-                   "l2": "inputs larger than L2 (indexQk 168 MB, qNormed 134 MB) and each step writes "
-                         "2.15 GB of logits, which evicts L2 between steps"},
-        "roofline": {"bound": "hbm", "kernel": "k2_scores_tc", "achieved": k2_gbs, "peak": hbm_peak,
-                     "unit": "GB/s", "frac": k2_gbs / hbm_peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} hbm_gbs"},
-        "kernels": kernels,
-        "e2e": {"value": whole_job_rows_per_s(rows, ms_e2e, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": K_e2e,
-                "block_ms_per_step": [round(x, 4) for x in e2e_blocks],
-                "how": "Python API, pinned host buffers; copies overlap compute across streams; "
-                       "K2 in per-sequence row chunks; the median of three timed blocks of `steps` steps"},
-        "gpu_launches": 2 * K,
-        "clocks": clk.summary(),
-        "device_fault_flags": faults,
-    }
-    if decode is not None:
-        line["decode"] = decode
-    if k1_small is not None:
-        line["k1_small_configs"] = k1_small
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_sample(wl)
-    print(json.dumps(line), flush=True)
+        def select_only():
+            if lib.qsa_index_topk_expand(out_idx.data_ptr(), logits.data_ptr(), ctx.data_ptr(), B, S, NB, 0, rows,
+                                         sp) != 0:
+                raise RuntimeError(qsa.qsa_last_error())
+
+        ms_sel = loop_ms(select_only, max(10, K // 10))
+
+        # K2 over the same rows in 8192-row chunks (rowStart, numRows), as a caller that bounds
+        # its logits buffer would call it: all chunks back to back, per step
+        chunk_rows = 8192
+
+        def k2_chunked():
+            for r0 in range(0, rows, chunk_rows):
+                n = min(chunk_rows, rows - r0)
+                if lib.qsa_index_scores(qsa.QSA_BF16, logits.data_ptr() + r0 * NB * 4, qn.data_ptr(), kb.data_ptr(),
+                                        ctx.data_ptr(), B, S, NB, r0, n, sp) != 0:
+                    raise RuntimeError(qsa.qsa_last_error())
+
+        ms_k2_chunked = loop_ms(k2_chunked, max(10, K // 10))
+
+        # the whole prefill indexer pipeline a caller runs: K1 (one pass), K2, then the top-512
+        # selection with expand, back to back on the stream
+        def pipeline():
+            self.step()
+            select_only()
+
+        ms_pipeline = loop_ms(pipeline, max(10, K // 10))
+        decode = None if args.no_decode else decode_leg(qsa, lib, stream, K, B=args.decode_batch)
+        k1_small = None if args.no_sweep or self.rank != 0 else k1_configs_leg(qsa, lib, load_peaks()[0])
+        torch.cuda.synchronize()
+        faults = qsa.qsa_device_fault_flags()
+
+        ms_e2e = max_over_ranks_of(after["ms_e2e"], world)
+        evs = self.evs
+        per_kernel = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+                      for j, n in enumerate(("k1_fused", "k2"))}
+        per_kernel["k1a"] = ms_k1a
+        per_kernel["k1b"] = ms_k1b
+        per_kernel["select"] = ms_sel
+        if self.rank != 0:
+            return {}
+
+        hbm_peak, tf_peak, peak_src = load_peaks()
+        ab = algorithmic_bytes(wl.context_lengths, B, S, NB)
+        ab["k1_fused"] = ab["k1a"] + ab["k1b"]
+        kernels = {}
+        for n in ("k1_fused", "k2", "k1a", "k1b", "select"):
+            gbs = ab[n] / (per_kernel[n] * 1e-3) / 1e9
+            kernels[n] = {"ms": per_kernel[n], "alg_bytes": ab[n], "gbs": gbs,
+                          "frac_of_measured_hbm": gbs / hbm_peak, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS}
+        kernels["k1_fused"]["rows_per_s"] = rows / (per_kernel["k1_fused"] * 1e-3)
+        kernels["k1_fused"]["timed"] = "inside the step (CUDA events around the launch)"
+        for n in ("k1a", "k1b"):
+            kernels[n]["timed"] = "separate entry point after the step loop; each launch after an L2 flush, median"
+        kernels["select"]["timed"] = ("separate entry point, back-to-back launches after the step loop "
+                                      "(1 GB of logits)")
+        kernels["select"]["rows_per_s"] = rows / (per_kernel["select"] * 1e-3)
+        kernels["k1a"]["rows_per_s"] = rows / (per_kernel["k1a"] * 1e-3)
+        kernels["k1b"]["blocks_per_s"] = B * NB / (per_kernel["k1b"] * 1e-3)
+        kernels["k1b"]["token_rows_per_s"] = 4 * B * NB / (per_kernel["k1b"] * 1e-3)
+        kernels["k2"]["rows_per_s"] = rows / (per_kernel["k2"] * 1e-3)
+        kernels["k2"]["causal_tflops"] = ab["k2_causal_flops"] / (per_kernel["k2"] * 1e-3) / 1e12
+        kernels["k2"]["frac_of_measured_bf16_peak"] = kernels["k2"]["causal_tflops"] / tf_peak
+        kernels["prefill_pipeline"] = {
+            "ms": ms_pipeline, "rows_per_s": rows / (ms_pipeline * 1e-3),
+            "timed": "qsa_index_qk_prep, qsa_index_scores and qsa_index_topk_expand back to back, per step"}
+        kernels["k2_chunked_8192"] = {
+            "ms": ms_k2_chunked, "chunks": (rows + chunk_rows - 1) // chunk_rows,
+            "gbs": ab["k2"] / (ms_k2_chunked * 1e-3) / 1e9,
+            "frac_of_measured_hbm": ab["k2"] / (ms_k2_chunked * 1e-3) / 1e9 / hbm_peak,
+            "timed": "K2 over the same rows as consecutive 8192-row calls, back to back after the step loop"}
+        step_bytes = ab["k1_fused"] + ab["k2"]
+        step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
+        kernels["step"] = {
+            "ms": ms_step, "alg_bytes": step_bytes, "gbs": step_gbs, "frac_of_measured_hbm": step_gbs / hbm_peak,
+            "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
+            "timed": "the whole step (fused K1, then K2): ms_per_step of this line"}
+
+        traffic = k2_profiled_traffic(B)
+        k2_gbs = kernels["k2"]["gbs"]
+        extra = {
+            "roofline": {"bound": "hbm", "kernel": "k2_scores_tc", "achieved": k2_gbs, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": k2_gbs / hbm_peak, "traffic": traffic,
+                         "peak_source": f"{peak_src} hbm_gbs"},
+            "kernels": kernels,
+            "e2e": {"value": whole_job_rows_per_s(rows, ms_e2e, world), "unit": UNIT,
+                    "h2d_bytes_per_step": after["h2d"], "d2h_bytes_per_step": after["d2h"], "ms_per_step": ms_e2e,
+                    "steps": after["K_e2e"], "block_ms_per_step": [round(x, 4) for x in after["blocks"]],
+                    "how": "Python API, pinned host buffers; copies overlap compute across streams; "
+                           "K2 in per-sequence row chunks; the median of three timed blocks of `steps` steps"},
+            "gpu_launches": 2 * K,
+            "clocks": clocks,
+            "device_fault_flags": faults,
+        }
+        if decode is not None:
+            extra["decode"] = decode
+        if k1_small is not None:
+            extra["k1_small_configs"] = k1_small
+        if world == 1 and not args.no_cpu_baseline:
+            extra["cpu_baseline"] = oracle_sample(wl)
+        return extra
+
+
+def run_ours(args, rank: int, world: int) -> None:
+    run_steps(args, rank, world, PrefillStepGpu)
 
 
 def main():

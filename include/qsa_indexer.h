@@ -145,8 +145,9 @@ int qsa_index_k_compress(qsa_dtype_t dtype, void* kbar, const void* indexQk,
  * Work is handed out by a device-side counter pair; calls take turns through 64
  * such pairs per device and each launch resets its pair when it ends, so at most
  * 64 launches may be in flight on one device at a time.  A CUDA graph that
- * captured a launch keeps that launch's pair on every replay (replays of one
- * graph must not overlap each other).
+ * captured a launch keeps that launch's pair on every replay, so one captured
+ * graph must not be replayed concurrently with itself (for example on two
+ * streams at once); replays in stream order are fine.
  *
  * Errors: QSA_E_NULL, QSA_E_DTYPE, QSA_E_SHAPE (batchSize < 1, seqLen < 1,
  *         numBlocks < ceilDiv(seqLen, 4)), QSA_E_RANGE (row range), QSA_E_ALIGN,
@@ -352,7 +353,8 @@ int qsa_topk_expand_decode(int32_t* outIdx, const float* logits, const int32_t* 
  * for another.  Sequences report completion
  * through a device-side counter set, one of 16 taken in turn by each launch: at most
  * 16 launches may be in flight on one device at a time, and a CUDA graph that captured
- * a launch keeps its set on every replay (replays of one graph must not overlap).
+ * a launch keeps its set on every replay, so one captured graph must not be replayed
+ * concurrently with itself.
  * Limits: batchSize <= 4096, maxBlocks <= 65536.
  * Errors: QSA_E_NULL, QSA_E_DTYPE, QSA_E_SHAPE, QSA_E_ALIGN, QSA_E_CUDA.
  */

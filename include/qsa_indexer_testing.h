@@ -17,9 +17,9 @@ extern "C" {
  * The K2 scores of qsa_index_scores ("Qsa Indexer Kernels", launchQsaIndexScores)
  * computed by a plain CUDA-core kernel (FP32 FMA dot products in ascending d, one
  * CTA per row and 128 blocks) instead of the tensor cores.  Same arguments,
- * layouts, validation and error codes as qsa_index_scores.  Tests use it as a
- * second, independent device implementation to cross-check the tcgen05 kernel on
- * every element of workloads too large for the CPU oracle.
+ * layouts, validation and error codes as qsa_index_scores.  Tests hold it to the
+ * oracle under the same tolerance as the tensor-core kernel; it is a second,
+ * independent device implementation of the same formula.
  */
 int qsa_testing_index_scores_cuda_core(qsa_dtype_t dtype, float* logits, const void* qNormed,
                                        const void* kbar, const int32_t* contextLengths,

@@ -103,7 +103,7 @@ def ref_norm_rope64(x, w_bits, eps, cs_row, dtype):
 def test_norm_rope_matches_rms_norm_and_complex_rotation(dtype):
     rng = np.random.default_rng(21)
     table = workloads.cos_sin_table(4096)
-    worst = 0.0
+    floor_used, n = 0, 0
     for trial in range(300):
         scale = [1.0, 50.0, 1e-3][trial % 3]
         x = to_f64(t_bits(rng.standard_normal(128) * scale, dtype), dtype)
@@ -113,8 +113,11 @@ def test_norm_rope_matches_rms_norm_and_complex_rotation(dtype):
         ref = ref_norm_rope64(x, w, 1e-6, table[pos], dtype)
         ok, st = check_t(out, ref, dtype)
         assert ok, (trial, st)
-        worst = max(worst, st["max_ulp"])
-    assert worst <= 1.0 + 1e-9 or worst < 64  # floor cases aside, typical worst is <= 1 ulp
+        floor_used += st["floor_used"]
+        n += st["n"]
+    # every element is within one ulp of T except the rare ones where the rope's
+    # subtraction cancels to a tiny value (those pass by the head-relative floor)
+    assert floor_used <= n // 1000, (floor_used, n)
 
 
 @pytest.mark.parametrize("dtype", DTYPES)

@@ -110,3 +110,25 @@ def check_logits(x, ref, dtype: str, floor: np.ndarray):
         "bad": int(np.sum(vis & ~(diff <= tol))),
     }
     return mask_ok and ok_vals, stats
+
+
+def check_logits_torch(x, ref, dtype: str, floor):
+    """check_logits on torch tensors (any device), for outputs too large for numpy
+    float64 arrays: the same mask rule and the same value bound, evaluated in float64."""
+    import torch
+    neg = float(np.float32(-np.finfo(np.float32).max))
+    mx = x == neg
+    mr = ref == neg
+    mask_ok = bool(torch.equal(mx, mr))
+    vis = ~mr
+    xd = x.double()
+    rd = ref.double()
+    diff = (xd - rd).abs()
+    tol = (2.0 ** -MANT_BITS[dtype]) * rd.abs() + floor.double()
+    ok_elem = torch.isfinite(xd) & (diff <= tol)
+    bad = int((vis & ~ok_elem).sum())
+    nvis = int(vis.sum())
+    worst = float((diff[vis] / tol[vis].clamp(min=1e-300)).max()) if nvis else 0.0
+    stats = {"n": int(x.numel()), "visible": nvis, "mask_ok": mask_ok,
+             "max_err_over_tol": worst, "bad": bad}
+    return mask_ok and bad == 0, stats
