@@ -228,6 +228,31 @@ int qsa_index_topk_expand(int32_t* outIdx, const float* logits, const int32_t* c
                           int32_t numRows, qsa_stream_t stream);
 
 /*
+ * The prefill scores of qsa_index_scores and the selection of qsa_index_topk_expand
+ * in one kernel, which never writes the FP32 logits ("Qsa Indexer Kernels":
+ * launchQsaIndexScores, then launchQsaIndexIdsFill, the stable descending segmented
+ * sort and launchQsaIndexExpand; the fusion is an addition of this library).  For
+ * the same arguments outIdx equals, bit for bit, what qsa_index_scores into a
+ * logits buffer followed by qsa_index_topk_expand on that buffer writes: every
+ * logit is computed by the same tensor-core tile and epilogue arithmetic, and the
+ * same 512 blocks a row are selected (largest keys, equal keys by ascending block
+ * id), emitted in ascending block order and expanded to 2051 token ids.
+ * The kernel computes each 64-token tile's scores twice or more on the tensor cores
+ * and keeps per-row histograms and bit masks in shared memory instead of the logits.
+ *  outIdx  [out] INT32 [batchSize*seqLen, 2051]; only the rows [rowStart,
+ *               rowStart + numRows) are written
+ *  qNormed [in]  T [batchSize, seqLen, 4, 128], kbar [in] T [batchSize, numBlocks, 128]
+ *               (16-byte aligned), as for qsa_index_scores
+ * Limit: numBlocks <= 4096 (larger problems: the two calls).  Up to 64 launches may
+ * be in flight on one device (device-side scheduler counters taken in turn), and one
+ * captured graph must not be replayed concurrently with itself.
+ * Errors: QSA_E_NULL, QSA_E_DTYPE, QSA_E_SHAPE, QSA_E_RANGE, QSA_E_ALIGN, QSA_E_CUDA.
+ */
+int qsa_index_scores_topk_expand(qsa_dtype_t dtype, int32_t* outIdx, const void* qNormed, const void* kbar,
+                                 const int32_t* contextLengths, int32_t batchSize, int32_t seqLen,
+                                 int32_t numBlocks, int32_t rowStart, int32_t numRows, qsa_stream_t stream);
+
+/*
  * QsaIndexerPoolState ("Qsa Indexer Kernels"): where the decode state lives.
  *  poolPtr      [2*numPages, 128, numKVHeads, poolHeadDim] T, element (page, row, head,
  *               col) at ((page*128 + row)*numKVHeads + head)*poolHeadDim + col
@@ -400,7 +425,8 @@ int qsa_index_scores_no_alloc(qsa_dtype_t dtype, float* logits, const void* qNor
  * Device-side fault flags.  Kernels that wait on their own asynchronous copies
  * bound every wait (about two seconds); a wait that runs out sets a bit here
  * (bits 0-3: scoring kernel, bits 8-11: staged q-prep kernels, bits 16-19: paged
- * decode scores, bits 20-23: the one-launch decode step)
+ * decode scores, bits 20-23: the one-launch decode step, bits 24-27: the fused
+ * scores + selection)
  * instead of hanging, the kernel drains and returns, and the outputs of that
  * launch are undefined.  This call synchronises `stream`, copies the flags of
  * the current device into *flags (0 = no fault since the last clear) and clears

@@ -20,7 +20,7 @@ __all__ = [
     "QsaError", "QSA_BF16", "QSA_F16", "load", "lib", "qsa_abi_version", "qsa_last_error",
     "qsa_index_q_prep", "qsa_index_k_compress", "qsa_index_qk_prep", "qsa_index_scores",
     "qsa_index_scores_no_alloc", "qsa_index_ids_fill", "qsa_index_expand", "qsa_index_topk_expand",
-    "PoolState", "pool_state", "qsa_index_k_compress_paged", "qsa_raw_k_tail_write_prefill",
+    "qsa_index_scores_topk_expand", "PoolState", "pool_state", "qsa_index_k_compress_paged", "qsa_raw_k_tail_write_prefill",
     "qsa_indexer_pre_decode", "qsa_index_scores_decode", "qsa_topk_expand_decode",
     "qsa_indexer_decode_step", "qsa_device_fault_flags",
     "qsa_testing_index_scores_cuda_core", "qsa_testing_bounded_wait_probe", "LIB_PATH",
@@ -32,7 +32,7 @@ STATUS_NAMES = {0: "QSA_OK", -1: "QSA_E_NULL", -2: "QSA_E_SHAPE", -3: "QSA_E_RAN
                 -4: "QSA_E_DTYPE", -5: "QSA_E_ALIGN", -6: "QSA_E_CUDA", -7: "QSA_E_DEVICE"}
 EXPORTED = ["qsa_abi_version", "qsa_last_error", "qsa_index_q_prep", "qsa_index_k_compress",
             "qsa_index_qk_prep", "qsa_index_ids_fill", "qsa_index_expand", "qsa_index_topk_expand",
-            "qsa_index_k_compress_paged", "qsa_raw_k_tail_write_prefill", "qsa_indexer_pre_decode",
+            "qsa_index_scores_topk_expand", "qsa_index_k_compress_paged", "qsa_raw_k_tail_write_prefill", "qsa_indexer_pre_decode",
             "qsa_index_scores_decode", "qsa_topk_expand_decode", "qsa_indexer_decode_step",
             "qsa_index_scores", "qsa_index_scores_no_alloc", "qsa_device_fault_flags",
             "qsa_testing_index_scores_cuda_core", "qsa_testing_bounded_wait_probe"]
@@ -92,6 +92,8 @@ def load():
     L.qsa_index_expand.restype = ctypes.c_int
     L.qsa_index_topk_expand.argtypes = [p, p, p, i32, i32, i32, i32, i32, p]
     L.qsa_index_topk_expand.restype = ctypes.c_int
+    L.qsa_index_scores_topk_expand.argtypes = [ctypes.c_int, p, p, p, p, i32, i32, i32, i32, i32, p]
+    L.qsa_index_scores_topk_expand.restype = ctypes.c_int
     pp = ctypes.POINTER(PoolState)
     L.qsa_index_k_compress_paged.argtypes = [ctypes.c_int, p, p, p, p, p, f32, pp, i32, i32, i32, i32, i32, i32, p]
     L.qsa_index_k_compress_paged.restype = ctypes.c_int
@@ -234,6 +236,14 @@ def qsa_index_topk_expand(outIdx, logits, contextLengths, batchSize, seqLen, num
     """Prefill selection in one kernel: radix top-512 + order + expand (see include/qsa_indexer.h)."""
     _check(load().qsa_index_topk_expand(_addr(outIdx), _addr(logits), _addr(contextLengths), int(batchSize),
                                      int(seqLen), int(numBlocks), int(rowStart), int(numRows), _stream(stream)))
+
+
+def qsa_index_scores_topk_expand(outIdx, qNormed, kbar, contextLengths, batchSize, seqLen, numBlocks, rowStart,
+                                 numRows, stream=None, dtype=None):
+    """K2 fused with the top-512 selection + expand; no logits written (see include/qsa_indexer.h)."""
+    _check(load().qsa_index_scores_topk_expand(_dtype(dtype, qNormed, kbar), _addr(outIdx), _addr(qNormed),
+                                            _addr(kbar), _addr(contextLengths), int(batchSize), int(seqLen),
+                                            int(numBlocks), int(rowStart), int(numRows), _stream(stream)))
 
 
 def qsa_index_k_compress_paged(kbar, indexQk, cosSin, contextLengths, wK, rmsEps, pool: PoolState, batchSize,

@@ -285,6 +285,33 @@ QSA_API int qsa_index_topk_expand(int32_t* outIdx, const float* logits, const in
                                               d.num_sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+QSA_API int qsa_index_scores_topk_expand(qsa_dtype_t dtype, int32_t* outIdx, const void* qNormed,
+                                         const void* kbar, const int32_t* contextLengths, int32_t batchSize,
+                                         int32_t seqLen, int32_t numBlocks, int32_t rowStart, int32_t numRows,
+                                         qsa_stream_t stream) {
+  static const char* fn = "qsa_index_scores_topk_expand";
+  int st;
+  if ((st = check_dtype(fn, dtype)) != QSA_OK) return st;
+  if (!qNormed || !kbar) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  if ((st = validate_selection(fn, outIdx, qNormed, contextLengths, batchSize, seqLen, numBlocks, rowStart,
+                               numRows)) != QSA_OK)
+    return st;
+  if (numBlocks > qsa::scores_topk_max_blocks())
+    return fail(QSA_E_SHAPE, "%s: numBlocks=%d above %d (use qsa_index_scores + qsa_index_topk_expand)", fn,
+                numBlocks, qsa::scores_topk_max_blocks());
+  if (!aligned(qNormed, 16) || !aligned(kbar, 16))
+    return fail(QSA_E_ALIGN, "%s: qNormed/kbar must be 16-byte aligned", fn);
+  if (numRows == 0) {
+    g_last_error[0] = '\0';
+    return QSA_OK;
+  }
+  DeviceInfo d;
+  if ((st = current_device(fn, &d)) != QSA_OK) return st;
+  qsa::LaunchScoresTopk a{dtype == QSA_BF16, outIdx, qNormed, kbar, contextLengths, batchSize, seqLen, numBlocks,
+                          rowStart, numRows, score_scale(), d.num_sms, reinterpret_cast<cudaStream_t>(stream)};
+  return launched(fn, qsa::launch_scores_topk_fused(a));
+}
+
 namespace {
 int validate_pool(const char* fn, const qsa_pool_state_t* ps, qsa::PoolDev* out) {
   if (!ps || !ps->poolPtr || !ps->pageTable) return fail(QSA_E_NULL, "%s: null pool state or pool pointer", fn);
@@ -477,14 +504,15 @@ QSA_API int qsa_device_fault_flags(uint32_t* flags, int clear, qsa_stream_t stre
   DeviceInfo d;
   int st = current_device(fn, &d);
   if (st != QSA_OK) return st;
-  uint32_t k2 = 0, k1 = 0, dec = 0, step = 0;
+  uint32_t k2 = 0, k1 = 0, dec = 0, step = 0, fused = 0;
   const auto cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = qsa::read_fault_flags(&k2, clear != 0, cs);
   if (e == cudaSuccess) e = qsa::read_k1_fault_flags(&k1, clear != 0, cs);
   if (e == cudaSuccess) e = qsa::read_dec_fault_flags(&dec, clear != 0, cs);
   if (e == cudaSuccess) e = qsa::read_step_fault_flags(&step, clear != 0, cs);
+  if (e == cudaSuccess) e = qsa::read_fused_fault_flags(&fused, clear != 0, cs);
   if (e != cudaSuccess) return fail(QSA_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
-  *flags = k2 | (k1 << 8) | (dec << 16) | (step << 20);
+  *flags = k2 | (k1 << 8) | (dec << 16) | (step << 20) | (fused << 24);
   g_last_error[0] = '\0';
   return QSA_OK;
 }

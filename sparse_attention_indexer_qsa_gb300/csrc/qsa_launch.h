@@ -91,6 +91,20 @@ struct LaunchScores {
   cudaStream_t stream;
 };
 
+// K2 and the top-512 selection + expand in one kernel, no logits written
+// (k2_topk_fused.cu); num_blocks <= scores_topk_max_blocks().
+struct LaunchScoresTopk {
+  bool bf16;
+  int32_t* out_idx;
+  const void* q_normed;
+  const void* kbar;
+  const int32_t* context_lengths;
+  int32_t batch, seq_len, num_blocks, row_start, num_rows;
+  float scale;
+  int num_sms;
+  cudaStream_t stream;
+};
+
 cudaError_t launch_q_prep(const LaunchQPrep& a);         // K1a (k1a_qprep.cu)
 cudaError_t launch_qk_prep(const LaunchQKPrep& a);       // fused K1a + prefill K1b (k1_stream.cu)
 cudaError_t launch_k_compress(const LaunchKCompress& a);
@@ -141,6 +155,10 @@ cudaError_t read_dec_fault_flags(uint32_t* flags, bool clear, cudaStream_t strea
 // Test-only: one warp's bounded wait on an mbarrier nothing arrives on (k_decode.cu).
 cudaError_t launch_bounded_wait_probe(uint64_t limit_ns, cudaStream_t stream);
 cudaError_t read_step_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
+cudaError_t read_fused_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
+
+cudaError_t launch_scores_topk_fused(const LaunchScoresTopk& a);
+int32_t scores_topk_max_blocks();
 
 // TMA map (a CUtensorMap, 64-byte aligned) over the pool's V-tails for the tensor-core
 // decode scoring (k_decode.cu).
