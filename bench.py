@@ -55,12 +55,15 @@ def algorithmic_bytes(ctx: np.ndarray, B: int, S: int, NB: int) -> dict:
         t = np.arange(int(min(c, S)))
         vis_logits += int(np.minimum((t + 1) // 4, NB).sum())
     select = vis_logits * 4 + B * S * 2051 * 4
+    # scoring fused with selection: q and kbar read once, outIdx written; no logits
+    fused_select = valid_rows * 1024 + vis_blocks * 256 + B * S * 2051 * 4
     # causal MMA work: row t of a sequence scores floor((t+1)/4) blocks x 4 heads x 128 dims
     flops = 0
     for c in ctx:
         t = np.arange(int(min(c, S)))
         flops += int(((t + 1) // 4).sum()) * 4 * 128 * 2
-    return {"k1a": k1a, "k1b": k1b, "k2": k2, "select": select, "k2_causal_flops": flops}
+    return {"k1a": k1a, "k1b": k1b, "k2": k2, "select": select, "fused_select": fused_select,
+            "k2_causal_flops": flops}
 
 
 def load_peaks():
@@ -566,6 +569,52 @@ def k1_configs_leg(qsa, lib, hbm_peak: float, names=None, sweep: bool = True) ->
     return res
 
 
+def prefill_select_leg(qsa, lib, stream, K, B=8):
+    """The prefill selection of the scoring workload (B sequences of 16384 tokens, ctx = S)
+    both ways: qsa_index_scores + qsa_index_topk_expand, and the fused
+    qsa_index_scores_topk_expand; K launches of each after 3 warm-up launches."""
+    import torch
+    wl = rank_workload(B, 0)
+    S, NB = wl.S, wl.num_blocks
+    rows = B * S
+    host = PrefillStepGpu.host
+    iq = host(wl.index_qk).cuda().view(torch.bfloat16)
+    cs, ctx = host(wl.cos_sin).cuda(), host(wl.context_lengths).cuda()
+    wq, wk = host(wl.w_q).cuda().view(torch.bfloat16), host(wl.w_k).cuda().view(torch.bfloat16)
+    qn = torch.empty((B, S, 4, 128), dtype=torch.bfloat16, device="cuda")
+    kb = torch.empty((B, NB, 128), dtype=torch.bfloat16, device="cuda")
+    sp = stream.cuda_stream
+    qsa.qsa_index_qk_prep(qn, kb, iq, cs, ctx, wq, wk, wl.eps, B, S, NB, stream=sp)
+    logits = torch.empty((rows, NB), dtype=torch.float32, device="cuda")
+    out2 = torch.empty((rows, 2051), dtype=torch.int32, device="cuda")
+    out1 = torch.empty_like(out2)
+
+    def two():
+        qsa.qsa_index_scores(logits, qn, kb, ctx, B, S, NB, 0, rows, stream=sp)
+        qsa.qsa_index_topk_expand(out2, logits, ctx, B, S, NB, 0, rows, stream=sp)
+
+    def fused():
+        qsa.qsa_index_scores_topk_expand(out1, qn, kb, ctx, B, S, NB, 0, rows, stream=sp)
+
+    def ms(fn):
+        for _ in range(3):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    res = {"B": B, "S": S, "num_blocks": NB, "fused_ms": ms(fused), "two_calls_ms": ms(two)}
+    torch.cuda.synchronize()
+    res["outidx_equal"] = bool(torch.equal(out1, out2))
+    res["device_fault_flags"] = qsa.qsa_device_fault_flags()
+    return res
+
+
 # ----------------------------------------------------------------- ranks (N > 1)
 
 def rank_barrier(world: int) -> None:
@@ -962,6 +1011,27 @@ class PrefillStepGpu:
             select_only()
 
         ms_pipeline = loop_ms(pipeline, max(10, K // 10))
+
+        # K2 fused with the selection (no logits written): alone, and as the pipeline
+        # K1 (one pass) then the fused call; its outIdx must equal the two calls'
+        out_fused = torch.empty_like(out_idx)
+
+        def fused_only():
+            if lib.qsa_index_scores_topk_expand(qsa.QSA_BF16, out_fused.data_ptr(), qn.data_ptr(), kb.data_ptr(),
+                                                ctx.data_ptr(), B, S, NB, 0, rows, sp) != 0:
+                raise RuntimeError(qsa.qsa_last_error())
+
+        def pipeline_fused():
+            if lib.qsa_index_qk_prep(qsa.QSA_BF16, qn.data_ptr(), kb.data_ptr(), iq.data_ptr(), cs.data_ptr(),
+                                     ctx.data_ptr(), wq.data_ptr(), wk.data_ptr(), eps, B, S, NB, sp) != 0:
+                raise RuntimeError(qsa.qsa_last_error())
+            fused_only()
+
+        ms_fused = loop_ms(fused_only, max(10, K // 10))
+        ms_pipeline_fused = loop_ms(pipeline_fused, max(10, K // 10))
+        pipeline()
+        torch.cuda.synchronize()
+        fused_equal = bool(torch.equal(out_fused, out_idx))
         decode = None if args.no_decode else decode_leg(qsa, lib, stream, K, B=args.decode_batch)
         k1_small = None if args.no_sweep or self.rank != 0 else k1_configs_leg(qsa, lib, load_peaks()[0])
         torch.cuda.synchronize()
@@ -1001,6 +1071,14 @@ class PrefillStepGpu:
         kernels["prefill_pipeline"] = {
             "ms": ms_pipeline, "rows_per_s": rows / (ms_pipeline * 1e-3),
             "timed": "qsa_index_qk_prep, qsa_index_scores and qsa_index_topk_expand back to back, per step"}
+        kernels["fused_select"] = {
+            "ms": ms_fused, "alg_bytes": ab["fused_select"], "gbs": ab["fused_select"] / (ms_fused * 1e-3) / 1e9,
+            "frac_of_measured_hbm": ab["fused_select"] / (ms_fused * 1e-3) / 1e9 / hbm_peak,
+            "rows_per_s": rows / (ms_fused * 1e-3), "outidx_equals_two_calls": fused_equal,
+            "timed": "qsa_index_scores_topk_expand over every row, back to back after the step loop"}
+        kernels["prefill_pipeline_fused"] = {
+            "ms": ms_pipeline_fused, "rows_per_s": rows / (ms_pipeline_fused * 1e-3),
+            "timed": "qsa_index_qk_prep then qsa_index_scores_topk_expand, back to back, per step"}
         kernels["k2_chunked_8192"] = {
             "ms": ms_k2_chunked, "chunks": (rows + chunk_rows - 1) // chunk_rows,
             "gbs": ab["k2"] / (ms_k2_chunked * 1e-3) / 1e9,
@@ -1056,6 +1134,9 @@ def main():
     ap.add_argument("--decode-batch", type=int, default=64, help="sequences in the decode-step leg")
     ap.add_argument("--only-decode", action="store_true",
                     help="run only the decode-step leg (for profiler captures)")
+    ap.add_argument("--only-prefill-select", action="store_true",
+                    help="run only the prefill selection of --batch sequences, fused and as two calls "
+                         "(for profiler captures)")
     ap.add_argument("--only-k1-configs", nargs="?", const="all", default=None, metavar="NAMES",
                     help="run only K1 on the small configurations and the size sweep, or on the named "
                          "configurations (comma-separated) without the sweep; for profiler captures")
@@ -1077,6 +1158,13 @@ def main():
                 torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
                 leg = decode_leg(qsa, qsa.load(), torch.cuda.current_stream(), args.steps, B=args.decode_batch)
                 print(json.dumps({"decode": leg}), flush=True)
+        elif args.only_prefill_select:
+            if rank == 0:
+                import torch
+                import sparse_attention_indexer_qsa_gb300 as qsa
+                torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+                leg = prefill_select_leg(qsa, qsa.load(), torch.cuda.current_stream(), args.steps, B=args.batch)
+                print(json.dumps({"prefill_select": leg}), flush=True)
         elif args.only_k1_configs:
             if rank == 0:
                 import torch

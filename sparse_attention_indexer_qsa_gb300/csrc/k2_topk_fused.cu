@@ -66,7 +66,13 @@ constexpr int kWords = kMaxBlocks / 32;
 constexpr int kCap = 128;                      // candidates listed per row
 constexpr int kKStages = 2;
 constexpr int kAccStages = 2;
-constexpr int kEpiWarps = 8;
+#ifndef QSA_FUSED_EPI_WARPS
+#define QSA_FUSED_EPI_WARPS 16
+#endif
+constexpr int kEpiWarps = QSA_FUSED_EPI_WARPS;     // 8 or 16: two or four per TMEM sub-partition
+static_assert(kEpiWarps == 8 || kEpiWarps == 16, "epilogue warps");
+constexpr int kTokPerWarp = kTokTile / (kEpiWarps / 4);  // tokens of a tile per epilogue warp
+constexpr int kLdPerWarp = kTokPerWarp / 8;              // 32-column TMEM loads (8 tokens each)
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
@@ -104,8 +110,8 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
 constexpr uint32_t kOffA = kOffK + kKStages * kKBytes;          // per row: histogram, then selected mask
 constexpr uint32_t kOffB = kOffA + kTokTile * kWords * 4;        // per row: candidates or tie mask
-constexpr uint32_t kOffStage = kOffB + kTokTile * kWords * 4;    // per epilogue warp: 512 winners
-constexpr uint32_t kOffRows = kOffStage + kEpiWarps * sel::kTopK * 4;
+constexpr uint32_t kOffStage = kOffB + kTokTile * kWords * 4;    // per epilogue warp: 512 winners (u16)
+constexpr uint32_t kOffRows = kOffStage + kEpiWarps * sel::kTopK * 2;
 constexpr uint32_t kOffBar = kOffRows + kTokTile * sizeof(RowState);
 constexpr int kBarQFull = 0;
 constexpr int kBarQEmpty = 1;
@@ -221,12 +227,49 @@ __device__ __forceinline__ float logit_of(const uint32_t (&r)[32], int k, float 
   return __fmul_rn(v, scale);
 }
 
+// Two rounded binary32 operations per instruction (add.rn.f32x2, mul.rn.f32x2):
+// lane-wise identical to the scalar forms, as in K2's epilogue.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+  return v;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t c;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(c) : "l"(a), "l"(b));
+  return c;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t c;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(c) : "l"(a), "l"(b));
+  return c;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ float relu_bits(uint32_t x) { return fmaxf(0.0f, __uint_as_float(x)); }
+
+// Keys of tokens k and k+1 of an 8-token TMEM load r (4 heads a token): per token
+// ((h0 + h1) + h2) + h3 of the relus, then times scale, two tokens per instruction.
+__device__ __forceinline__ void keys2(const uint32_t (&r)[32], int k, uint64_t sc, uint32_t& k0, uint32_t& k1) {
+  uint64_t v = add2(pack2(relu_bits(r[4 * k + 0]), relu_bits(r[4 * k + 4])),
+                    pack2(relu_bits(r[4 * k + 1]), relu_bits(r[4 * k + 5])));
+  v = add2(v, pack2(relu_bits(r[4 * k + 2]), relu_bits(r[4 * k + 6])));
+  v = add2(v, pack2(relu_bits(r[4 * k + 3]), relu_bits(r[4 * k + 7])));
+  v = mul2(v, sc);
+  float a, b;
+  unpack2(v, a, b);
+  k0 = sel::orderable(a);
+  k1 = sel::orderable(b);
+}
+
 // first-pass bin of a key, and the key range of a first-pass bin
+// -0 (and anything ordered below +0): bin 0; +0: bin 1; positive keys: 64 bins an
+// octave from `base`, clamped to [2, 255].
 __device__ __forceinline__ uint32_t bin0_of(uint32_t key, int32_t base) {
-  if (key < 0x80000000u) return 0u;            // -0 (and anything ordered below +0)
-  if (key == 0x80000000u) return 1u;           // +0
   const int32_t d = static_cast<int32_t>(key >> 17) - base;
-  return static_cast<uint32_t>(min(max(d, 2), 255));
+  const uint32_t b = static_cast<uint32_t>(min(max(d, 2), 255));
+  return key <= 0x80000000u ? key >> 31 : b;
 }
 
 __device__ __forceinline__ void bin0_range(uint32_t b, int32_t base, uint32_t& lo, uint32_t& hi) {
@@ -263,7 +306,7 @@ __device__ __forceinline__ void st_s32x4(int32_t* p, int32_t a, int32_t b, int32
 
 // A row's 2051 ids from its 512 winners (ascending): id 4p + j = 4*win[p] + j, then the
 // causal tail, then -1; 16-byte stores from the row's first aligned address.
-__device__ __forceinline__ void warp_write_selected(int32_t* out, const uint32_t* win, int32_t tail,
+__device__ __forceinline__ void warp_write_selected(int32_t* out, const uint16_t* win, int32_t tail,
                                                     int32_t n_vis, int lane) {
   constexpr int kIds = sel::kRatio * sel::kTopK;
   const int k0 = static_cast<int>((4u - (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(out) >> 2) & 3u)) & 3u);
@@ -494,12 +537,12 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     }
   } else {
     // --------------------------------------------------------------- epilogue
-    const int ew = warp - 2;          // 0..7
-    const int sp = warp & 3;          // TMEM sub-partition: blocks 32*sp + lane of a g-tile
-    const int grp = ew >> 2;          // token slice [32*grp, 32*grp + 32) of the tile
+    const int ew = warp - 2;                      // 0 .. kEpiWarps-1
+    const int sp = warp & 3;                      // TMEM sub-partition: blocks 32*sp + lane of a g-tile
+    const int tok0 = kTokPerWarp * (ew >> 2);     // this warp's tokens [tok0, tok0 + kTokPerWarp) of the tile
     const int etid = threadIdx.x - 64;
-    const float scale = p.scale;
-    uint32_t* stage = reinterpret_cast<uint32_t*>(base_ptr + kOffStage) + ew * sel::kTopK;
+    const uint64_t sc2 = pack2(p.scale, p.scale);
+    uint16_t* stage = reinterpret_cast<uint16_t*>(base_ptr + kOffStage) + ew * sel::kTopK;
     int acnt = 0, scnt = 0, dcnt = 0;
     bool ok = true;
     while (ok) {
@@ -534,13 +577,21 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       epi_sync();
 
       if (x.n_gt > 0) {
-        int32_t base0 = *bin_base;
+        const int32_t base0 = *bin_base;
         bool final_pass = false;
         for (int pass = 0; ok; ++pass) {
-          // per-token facts of this warp's 32 tokens, read once a pass
-          const RowState my = rows[32 * grp + lane];
-          const uint32_t mode_mask_active = __ballot_sync(0xffffffffu, my.mode == kActive);
-          const uint32_t mode_mask_final = __ballot_sync(0xffffffffu, my.mode >= kTakeAll);
+          // this warp's tokens: lane j (< kTokPerWarp) holds token tok0 + j's row state
+          const RowState my = rows[tok0 + (lane % kTokPerWarp)];
+          const bool mine = lane < kTokPerWarp;
+          const uint32_t act = __ballot_sync(0xffffffffu, mine && (final_pass ? my.mode >= kTakeAll : my.mode == kActive));
+          const uint32_t ties = __ballot_sync(0xffffffffu, mine && my.mode == kTies);
+          const uint32_t cands = __ballot_sync(0xffffffffu, mine && my.mode == kCand);
+          const bool lvl0 = my.level0 != 0u;         // the same for every active row of a pass
+          const uint32_t lvl0_any = __ballot_sync(0xffffffffu, mine && my.mode == kActive && lvl0);
+          // final pass: key > sel_gt selects; lo <= key <= hi lists (lo = 1 > hi = 0: none)
+          const uint32_t my_sel_gt = my.mode == kTakeAll ? my.lo - 1u : my.hi;
+          const uint32_t my_in_lo = my.mode == kTakeAll ? 1u : my.lo;
+          const uint32_t my_in_hi = my.mode == kTakeAll ? 0u : my.hi;
           for (int i = 0; i < x.n_gt; ++i) {
             const int as = acnt % kAccStages;
             if (!wait_bounded(bar(kBarAccFull + as), (acnt / kAccStages) & 1, abort_flag, kFaultEpilogue)) {
@@ -549,59 +600,87 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             }
             ptx::tc_fence_after();
             const int32_t g = i * kGTile + 32 * sp + lane;
-            const int wi = i * 4 + sp;                       // mask word of this warp's 32 blocks
+            const int wi = i * 4 + sp;               // mask word of this warp's 32 blocks
+            // token tok0 + 8c + k sees block g iff 4g + 3 <= t, i.e. dv - 8c <= k
+            const int32_t dv = 4 * g + 3 - (x.t0 + tok0);
             const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * sp) << 16) +
-                                   static_cast<uint32_t>(as) * kAccCols + 4u * 32u * grp;
-            uint32_t r[32];
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              const uint32_t todo = (final_pass ? mode_mask_final : mode_mask_active) >> (8 * c);
-              if ((todo & 0xFFu) == 0u) continue;
-              ptx::tmem_ld_32x32b_x32(taddr + 32u * c, r);
-              ptx::tmem_ld_wait(r);
+                                   static_cast<uint32_t>(as) * kAccCols + 4u * static_cast<uint32_t>(tok0);
+            if (act != 0u) {
+              uint32_t ra[32], rb[32];
+              ptx::tmem_ld_32x32b_x32(taddr, ra);
+              ptx::tmem_ld_wait(ra);
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                if (!((todo >> k) & 1u)) continue;
-                const int tt = 32 * grp + 8 * c + k;          // row of the unit
-                const int src = 8 * c + k;                    // lane holding its state
-                const int32_t n_vis = __shfl_sync(0xffffffffu, my.n_vis, src);
-                const bool vis = g < n_vis;
-                const uint32_t key = sel::orderable(logit_of(r, k, scale));
-                if (!final_pass) {
-                  const uint32_t lvl0 = __shfl_sync(0xffffffffu, my.level0, src);
-                  uint32_t bin = 0xFFFFFFFFu;
-                  if (lvl0) {
-                    bin = bin0_of(key, base0);
+              for (int c = 0; c < kLdPerWarp; ++c) {
+                uint32_t (&r)[32] = (c & 1) ? rb : ra;
+                uint32_t (&nx)[32] = (c & 1) ? ra : rb;
+                if (c + 1 < kLdPerWarp) ptx::tmem_ld_32x32b_x32(taddr + 32u * (c + 1), nx);
+                const uint32_t a8 = (act >> (8 * c)) & 0xFFu;
+                const int32_t dvc = dv - 8 * c;
+                if (a8 != 0u) {
+                  if (final_pass) {
+#pragma unroll
+                    for (int k = 0; k < 8; k += 2) {
+                      uint32_t key[2];
+                      keys2(r, k, sc2, key[0], key[1]);
+#pragma unroll
+                      for (int h = 0; h < 2; ++h) {
+                        const int j = 8 * c + k + h;       // token of this warp's slice
+                        const uint32_t sel_gt = __shfl_sync(0xffffffffu, my_sel_gt, j);
+                        const uint32_t in_lo = __shfl_sync(0xffffffffu, my_in_lo, j);
+                        const uint32_t in_hi = __shfl_sync(0xffffffffu, my_in_hi, j);
+                        const bool vis = dvc <= k + h;
+                        const bool s = vis && key[h] > sel_gt;
+                        const bool in = vis && key[h] >= in_lo && key[h] <= in_hi;
+                        const uint32_t ws = __ballot_sync(0xffffffffu, s);
+                        const uint32_t wc = __ballot_sync(0xffffffffu, in);
+                        if ((act >> j) & 1u) {
+                          const int tt = tok0 + j;
+                          if (lane == 0) reg_a[tt * kWords + wi] = ws;
+                          if ((ties >> j) & 1u) {
+                            if (lane == 0) reg_b[tt * kWords + wi] = wc;
+                          } else if (((cands >> j) & 1u) && wc != 0u) {
+                            uint32_t at = 0u;
+                            if (lane == 0) at = atomicAdd(&rows[tt].cnt, static_cast<uint32_t>(__popc(wc)));
+                            at = __shfl_sync(0xffffffffu, at, 0);
+                            const uint32_t slot = at + static_cast<uint32_t>(__popc(wc & ((1u << lane) - 1u)));
+                            if (in && slot < static_cast<uint32_t>(kCap))
+                              reg_b[tt * kWords + slot] = ((key[h] - in_lo) << 12) | static_cast<uint32_t>(g);
+                          }
+                        }
+                      }
+                    }
+                  } else if (lvl0_any != 0u) {
+#pragma unroll
+                    for (int k = 0; k < 8; k += 2) {
+                      uint32_t key[2];
+                      keys2(r, k, sc2, key[0], key[1]);
+#pragma unroll
+                      for (int h = 0; h < 2; ++h) {
+                        const int j = 8 * c + k + h;
+                        const uint32_t b = bin0_of(key[h], base0);
+                        if (((a8 >> (k + h)) & 1u) && dvc <= k + h)
+                          atomicAdd(&reg_a[(tok0 + j) * kWords + (b >> 1)], 1u << ((b & 1u) << 4));
+                      }
+                    }
                   } else {
-                    const uint32_t lo = __shfl_sync(0xffffffffu, my.lo, src);
-                    const uint32_t hi = __shfl_sync(0xffffffffu, my.hi, src);
-                    const uint32_t sh = __shfl_sync(0xffffffffu, my.shift, src);
-                    if (key >= lo && key <= hi) bin = (key - lo) >> sh;
-                  }
-                  if (vis && bin != 0xFFFFFFFFu)
-                    atomicAdd(&reg_a[tt * kWords + (bin >> 1)], 1u << ((bin & 1u) * 16u));
-                } else {
-                  const uint32_t mode = __shfl_sync(0xffffffffu, my.mode, src);
-                  const uint32_t lo = __shfl_sync(0xffffffffu, my.lo, src);
-                  const uint32_t hi = __shfl_sync(0xffffffffu, my.hi, src);
-                  const bool s = vis && (mode == kTakeAll ? key >= lo : key > hi);
-                  const bool in = vis && mode != kTakeAll && key >= lo && key <= hi;
-                  const uint32_t ws = __ballot_sync(0xffffffffu, s);
-                  const uint32_t wc = __ballot_sync(0xffffffffu, in);
-                  if (lane == 0) reg_a[tt * kWords + wi] = ws;
-                  if (mode == kTies) {
-                    if (lane == 0) reg_b[tt * kWords + wi] = wc;
-                  } else if (mode == kCand && wc != 0u) {
-                    uint32_t at = 0u;
-                    if (lane == 0) at = atomicAdd(&rows[tt].cnt, static_cast<uint32_t>(__popc(wc)));
-                    at = __shfl_sync(0xffffffffu, at, 0);
-                    if (in) {
-                      const uint32_t slot = at + static_cast<uint32_t>(__popc(wc & ((1u << lane) - 1u)));
-                      if (slot < static_cast<uint32_t>(kCap))
-                        reg_b[tt * kWords + slot] = ((key - lo) << 12) | static_cast<uint32_t>(g);
+#pragma unroll
+                    for (int k = 0; k < 8; k += 2) {
+                      uint32_t key[2];
+                      keys2(r, k, sc2, key[0], key[1]);
+#pragma unroll
+                      for (int h = 0; h < 2; ++h) {
+                        const int j = 8 * c + k + h;
+                        const uint32_t lo = __shfl_sync(0xffffffffu, my.lo, j);
+                        const uint32_t hi = __shfl_sync(0xffffffffu, my.hi, j);
+                        const uint32_t sh = __shfl_sync(0xffffffffu, my.shift, j);
+                        const uint32_t b = (key[h] - lo) >> sh;
+                        if (((a8 >> (k + h)) & 1u) && dvc <= k + h && key[h] >= lo && key[h] <= hi)
+                          atomicAdd(&reg_a[(tok0 + j) * kWords + (b >> 1)], 1u << ((b & 1u) << 4));
+                      }
                     }
                   }
                 }
+                if (c + 1 < kLdPerWarp) ptx::tmem_ld_wait(nx);
               }
             }
             ptx::tc_fence_before();
@@ -621,11 +700,11 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             // this lane's 8 bins, highest first: bins 8*(31-lane) + 7 .. + 0
             const uint32_t b8[8] = {v.w >> 16, v.w & 0xFFFFu, v.z >> 16, v.z & 0xFFFFu,
                                     v.y >> 16, v.y & 0xFFFFu, v.x >> 16, v.x & 0xFFFFu};
-            uint32_t mine = 0;
+            uint32_t mine8 = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) mine += b8[j];
-            const uint32_t incl = warp_inclusive_sum(mine, lane);
-            const uint32_t excl = incl - mine;
+            for (int j = 0; j < 8; ++j) mine8 += b8[j];
+            const uint32_t incl = warp_inclusive_sum(mine8, lane);
+            const uint32_t excl = incl - mine8;
             const uint32_t want = static_cast<uint32_t>(rs.rem);
             const bool hit = excl < want && want <= incl;
             uint32_t fb = 0u, fabove = 0u, fcount = 0u;
@@ -733,29 +812,41 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           // sort key = offset, then 4095 - block, so all listed sort keys differ
           const int n = static_cast<int>(min(rs.cnt, static_cast<uint32_t>(kCap)));
           const uint32_t need = static_cast<uint32_t>(rs.rem);
-          uint32_t e[4], s[4];
-          bool valid[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int idx = lane + 32 * j;
-            valid[j] = idx < n;
-            e[j] = valid[j] ? reg_b[tt * kWords + idx] : 0u;
-            s[j] = (e[j] & 0xFFFFF000u) | (0xFFFu - (e[j] & 0xFFFu));
-          }
-          uint32_t thr = 0u;
-#pragma unroll 1
-          for (int bit = 31; bit >= 0; --bit) {
-            const uint32_t cand = thr | (1u << bit);
-            uint32_t c = 0u;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) c += __popc(__ballot_sync(0xffffffffu, valid[j] && s[j] >= cand));
-            if (c >= need) thr = cand;
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (valid[j] && s[j] >= thr) {
-              const uint32_t gb = e[j] & 0xFFFu;
+          if (n <= 32) {
+            const bool valid = lane < n;
+            const uint32_t e = valid ? reg_b[tt * kWords + lane] : 0u;
+            const uint32_t s = (e & 0xFFFFF000u) | (0xFFFu - (e & 0xFFFu));
+            uint32_t rank = 0u;
+            for (int j = 0; j < n; ++j) rank += __shfl_sync(0xffffffffu, s, j) > s ? 1u : 0u;
+            if (valid && rank < need) {
+              const uint32_t gb = e & 0xFFFu;
               atomicOr(&selm[gb >> 5], 1u << (gb & 31u));
+            }
+          } else {
+            uint32_t e[4], s[4];
+            bool valid[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int idx = lane + 32 * j;
+              valid[j] = idx < n;
+              e[j] = valid[j] ? reg_b[tt * kWords + idx] : 0u;
+              s[j] = (e[j] & 0xFFFFF000u) | (0xFFFu - (e[j] & 0xFFFu));
+            }
+            uint32_t thr = 0u;
+#pragma unroll 1
+            for (int bit = 31; bit >= 0; --bit) {
+              const uint32_t cand = thr | (1u << bit);
+              uint32_t c = 0u;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) c += __popc(__ballot_sync(0xffffffffu, valid[j] && s[j] >= cand));
+              if (c >= need) thr = cand;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (valid[j] && s[j] >= thr) {
+                const uint32_t gb = e[j] & 0xFFFu;
+                atomicOr(&selm[gb >> 5], 1u << (gb & 31u));
+              }
             }
           }
           __syncwarp();
@@ -802,7 +893,7 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           while (m != 0u) {
             const int bit = __ffs(m) - 1;
             m &= m - 1u;
-            if (pos < static_cast<uint32_t>(sel::kTopK)) stage[pos] = static_cast<uint32_t>(32 * (4 * lane + j) + bit);
+            if (pos < static_cast<uint32_t>(sel::kTopK)) stage[pos] = static_cast<uint16_t>(32 * (4 * lane + j) + bit);
             ++pos;
           }
         }
