@@ -218,15 +218,6 @@ __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 1, %0;" :: "n"(kEpiThreads) : "memory");
 }
 
-// relu per head, ascending-h sum, scale after the sum: r holds 8 tokens x 4 heads of
-// one block; the operations and their order are K2's, so the bits are K2's.
-__device__ __forceinline__ float logit_of(const uint32_t (&r)[32], int k, float scale) {
-  float v = __fadd_rn(fmaxf(0.0f, __uint_as_float(r[4 * k + 0])), fmaxf(0.0f, __uint_as_float(r[4 * k + 1])));
-  v = __fadd_rn(v, fmaxf(0.0f, __uint_as_float(r[4 * k + 2])));
-  v = __fadd_rn(v, fmaxf(0.0f, __uint_as_float(r[4 * k + 3])));
-  return __fmul_rn(v, scale);
-}
-
 // Two rounded binary32 operations per instruction (add.rn.f32x2, mul.rn.f32x2):
 // lane-wise identical to the scalar forms, as in K2's epilogue.
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
@@ -251,6 +242,7 @@ __device__ __forceinline__ float relu_bits(uint32_t x) { return fmaxf(0.0f, __ui
 
 // Keys of tokens k and k+1 of an 8-token TMEM load r (4 heads a token): per token
 // ((h0 + h1) + h2) + h3 of the relus, then times scale, two tokens per instruction.
+// The operations and their order are K2's, so every logit has K2's bits.
 __device__ __forceinline__ void keys2(const uint32_t (&r)[32], int k, uint64_t sc, uint32_t& k0, uint32_t& k1) {
   uint64_t v = add2(pack2(relu_bits(r[4 * k + 0]), relu_bits(r[4 * k + 4])),
                     pack2(relu_bits(r[4 * k + 1]), relu_bits(r[4 * k + 5])));
@@ -313,9 +305,12 @@ __device__ __forceinline__ void warp_write_selected(int32_t* out, const uint16_t
   const int nchunks = (kIds - k0) / 4;
   for (int c = lane; c < nchunks; c += 32) {
     const int i = k0 + 4 * c;
+    // ids i .. i+3 come from winners i/4 and (i+3)/4 (the same one when the row is aligned)
+    const int32_t wa = static_cast<int32_t>(win[i >> 2]) * sel::kRatio;
+    const int32_t wb = static_cast<int32_t>(win[(i + 3) >> 2]) * sel::kRatio;
     int32_t v[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = static_cast<int32_t>(win[(i + j) >> 2]) * sel::kRatio + ((i + j) & 3);
+    for (int j = 0; j < 4; ++j) v[j] = (((i + j) >> 2) == (i >> 2) ? wa : wb) + ((i + j) & 3);
     st_s32x4(out + i, v[0], v[1], v[2], v[3]);
   }
   const int tail_lo = k0 + 4 * nchunks;
@@ -571,8 +566,9 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         rows[etid] = rs;
       }
       if (x.n_gt > 0) {
+        // histograms (region A) and tie masks (region B) start at zero; A and B are adjacent
         uint4* a4 = reinterpret_cast<uint4*>(reg_a);
-        for (int k = etid; k < kTokTile * kWords / 4; k += kEpiThreads) a4[k] = make_uint4(0u, 0u, 0u, 0u);
+        for (int k = etid; k < 2 * kTokTile * kWords / 4; k += kEpiThreads) a4[k] = make_uint4(0u, 0u, 0u, 0u);
       }
       epi_sync();
 
@@ -588,10 +584,11 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           const uint32_t cands = __ballot_sync(0xffffffffu, mine && my.mode == kCand);
           const bool lvl0 = my.level0 != 0u;         // the same for every active row of a pass
           const uint32_t lvl0_any = __ballot_sync(0xffffffffu, mine && my.mode == kActive && lvl0);
-          // final pass: key > sel_gt selects; lo <= key <= hi lists (lo = 1 > hi = 0: none)
+          // final pass: key > sel_gt selects; in_lo <= key <= sel_gt is the threshold bin
+          // (take-all rows: in_lo = sel_gt + 1, an empty bin)
           const uint32_t my_sel_gt = my.mode == kTakeAll ? my.lo - 1u : my.hi;
-          const uint32_t my_in_lo = my.mode == kTakeAll ? 1u : my.lo;
-          const uint32_t my_in_hi = my.mode == kTakeAll ? 0u : my.hi;
+          // (a take-all row has lo > 0: all keys >= 0 taken would mean nVis = 512)
+          const uint32_t my_in_lo = my.lo;
           for (int i = 0; i < x.n_gt; ++i) {
             const int as = acnt % kAccStages;
             if (!wait_bounded(bar(kBarAccFull + as), (acnt / kAccStages) & 1, abort_flag, kFaultEpilogue)) {
@@ -618,35 +615,45 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 const int32_t dvc = dv - 8 * c;
                 if (a8 != 0u) {
                   if (final_pass) {
+                    // per token: its selected-bit word (kept by lane j, stored once for the 8
+                    // tokens) and, per lane, which tokens hold a key of their threshold bin
+                    uint32_t wsel = 0u, cbits = 0u, key8[8];
 #pragma unroll
                     for (int k = 0; k < 8; k += 2) {
-                      uint32_t key[2];
-                      keys2(r, k, sc2, key[0], key[1]);
+                      keys2(r, k, sc2, key8[k], key8[k + 1]);
 #pragma unroll
                       for (int h = 0; h < 2; ++h) {
                         const int j = 8 * c + k + h;       // token of this warp's slice
+                        const uint32_t key = key8[k + h];
                         const uint32_t sel_gt = __shfl_sync(0xffffffffu, my_sel_gt, j);
                         const uint32_t in_lo = __shfl_sync(0xffffffffu, my_in_lo, j);
-                        const uint32_t in_hi = __shfl_sync(0xffffffffu, my_in_hi, j);
                         const bool vis = dvc <= k + h;
-                        const bool s = vis && key[h] > sel_gt;
-                        const bool in = vis && key[h] >= in_lo && key[h] <= in_hi;
-                        const uint32_t ws = __ballot_sync(0xffffffffu, s);
-                        const uint32_t wc = __ballot_sync(0xffffffffu, in);
-                        if ((act >> j) & 1u) {
-                          const int tt = tok0 + j;
-                          if (lane == 0) reg_a[tt * kWords + wi] = ws;
-                          if ((ties >> j) & 1u) {
-                            if (lane == 0) reg_b[tt * kWords + wi] = wc;
-                          } else if (((cands >> j) & 1u) && wc != 0u) {
-                            uint32_t at = 0u;
-                            if (lane == 0) at = atomicAdd(&rows[tt].cnt, static_cast<uint32_t>(__popc(wc)));
-                            at = __shfl_sync(0xffffffffu, at, 0);
-                            const uint32_t slot = at + static_cast<uint32_t>(__popc(wc & ((1u << lane) - 1u)));
-                            if (in && slot < static_cast<uint32_t>(kCap))
-                              reg_b[tt * kWords + slot] = ((key[h] - in_lo) << 12) | static_cast<uint32_t>(g);
-                          }
-                        }
+                        const uint32_t ws = __ballot_sync(0xffffffffu, vis && key > sel_gt);
+                        wsel = lane == k + h ? ws : wsel;
+                        cbits |= (vis && key >= in_lo && key <= sel_gt) ? 1u << (k + h) : 0u;
+                      }
+                    }
+                    // a row that is not in its final pass never reads this word again
+                    if (lane < 8) reg_a[(tok0 + 8 * c + lane) * kWords + wi] = wsel;
+                    const uint32_t todo_c = __reduce_or_sync(0xffffffffu, cbits) & a8;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                      if (!((todo_c >> kk) & 1u)) continue;  // the same for every lane
+                      const int j = 8 * c + kk;
+                      const int tt = tok0 + j;
+                      const bool in = (cbits >> kk) & 1u;
+                      const uint32_t wc = __ballot_sync(0xffffffffu, in);
+                      if ((ties >> j) & 1u) {
+                        if (lane == 0) reg_b[tt * kWords + wi] = wc;
+                      } else if ((cands >> j) & 1u) {
+                        const uint32_t kv = key8[kk];
+                        const uint32_t in_lo = __shfl_sync(0xffffffffu, my_in_lo, j);
+                        uint32_t at = 0u;
+                        if (lane == 0) at = atomicAdd(&rows[tt].cnt, static_cast<uint32_t>(__popc(wc)));
+                        at = __shfl_sync(0xffffffffu, at, 0);
+                        const uint32_t slot = at + static_cast<uint32_t>(__popc(wc & ((1u << lane) - 1u)));
+                        if (in && slot < static_cast<uint32_t>(kCap))
+                          reg_b[tt * kWords + slot] = ((kv - in_lo) << 12) | static_cast<uint32_t>(g);
                       }
                     }
                   } else if (lvl0_any != 0u) {
@@ -658,8 +665,10 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                       for (int h = 0; h < 2; ++h) {
                         const int j = 8 * c + k + h;
                         const uint32_t b = bin0_of(key[h], base0);
-                        if (((a8 >> (k + h)) & 1u) && dvc <= k + h)
-                          atomicAdd(&reg_a[(tok0 + j) * kWords + (b >> 1)], 1u << ((b & 1u) << 4));
+                        // every lane adds: a key the row does not count adds 0 (no divergence);
+                        // rows outside this pass never read their histogram again
+                        const bool cnt = ((a8 >> (k + h)) & 1u) && dvc <= k + h;
+                        atomicAdd(&reg_a[(tok0 + j) * kWords + (b >> 1)], cnt ? 1u << ((b & 1u) << 4) : 0u);
                       }
                     }
                   } else {
@@ -673,9 +682,9 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                         const uint32_t lo = __shfl_sync(0xffffffffu, my.lo, j);
                         const uint32_t hi = __shfl_sync(0xffffffffu, my.hi, j);
                         const uint32_t sh = __shfl_sync(0xffffffffu, my.shift, j);
-                        const uint32_t b = (key[h] - lo) >> sh;
-                        if (((a8 >> (k + h)) & 1u) && dvc <= k + h && key[h] >= lo && key[h] <= hi)
-                          atomicAdd(&reg_a[(tok0 + j) * kWords + (b >> 1)], 1u << ((b & 1u) << 4));
+                        const bool cnt = ((a8 >> (k + h)) & 1u) && dvc <= k + h && key[h] >= lo && key[h] <= hi;
+                        const uint32_t b = cnt ? (key[h] - lo) >> sh : 0u;
+                        atomicAdd(&reg_a[(tok0 + j) * kWords + (b >> 1)], cnt ? 1u << ((b & 1u) << 4) : 0u);
                       }
                     }
                   }
