@@ -324,6 +324,10 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Everything above overlaps the previous kernel's tail when this launch is a
+  // programmatic dependent; nothing below may read its inputs (q, kbar, ctx) or
+  // overwrite the logits buffer before that kernel has completed.
+  ptx::grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -339,6 +343,8 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         } else {
           x = Unit{};
           x.b = -1;
+          // this CTA takes no more work: the next kernel may start launching
+          ptx::launch_dependents();
         }
         const int ss = scnt % kSchedStages;
         if (!wait_bounded(bar(kBarSchedEmpty + ss), ((scnt / kSchedStages) & 1) ^ 1, abort_flag, kFaultProducer)) break;
@@ -529,6 +535,7 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
   }
 
+  ptx::launch_dependents();
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -633,8 +640,20 @@ cudaError_t launch_scores_tc(const LaunchScores& a) {
   p.scale = a.scale;
   p.vec_fill = (a.num_blocks % 4 == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0) ? 1 : 0;
   const int grid = static_cast<int>(units < a.num_sms ? units : a.num_sms);
-  k2_scores_tc_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, p);
-  return cudaGetLastError();
+  // A programmatic dependent of the previous kernel in the stream: this launch's CTAs
+  // may become resident, and set up, while that kernel drains; they wait for it to
+  // complete before touching any input or output (griddepcontrol.wait above).
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k2_scores_tc_kernel, tq, tk, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -645,6 +664,9 @@ cudaError_t launch_scores_tc(const LaunchScores& a) {
 // {next unit, CTAs finished} counter pair; each call zeroes them on its stream
 // before the kernel runs, so calls that overlap on the GPU race on them.
 constexpr int kNoAllocScratchWords = 64;  // 256 bytes
+// The header states the no-alloc limit with 1024 blocks per work unit's g-tile group.
+static_assert(k2::kGTile * k2::kGTilesPerUnit == 1024,
+              "qsa_index_scores_no_alloc's documented work-unit count assumes 1024 blocks a group");
 static __device__ __align__(256) uint32_t g_k2_noalloc_scratch[kNoAllocScratchWords];
 
 namespace {

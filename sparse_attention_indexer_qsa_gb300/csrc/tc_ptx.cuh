@@ -154,6 +154,22 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
                :: "memory");
 }
 
+// ------------------------------------------------- programmatic dependent launch
+
+// Block until the grids this launch depends on (the previous kernel in the stream,
+// when this one was launched with programmatic stream serialization) have completed
+// and their memory is visible; returns at once for an ordinary launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream, if launched with programmatic stream
+// serialization, to start launching once every CTA of this grid has called this
+// or exited.  Changes nothing this grid computes.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA with
 // 128-byte swizzle: rows of 128 bytes (64 two-byte elements), 8-row swizzle atoms
 // of 1024 bytes stacked along M/N (stride-dimension offset 1024 B).  The leading
