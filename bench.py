@@ -499,6 +499,22 @@ def k1_configs_leg(qsa, lib, hbm_peak: float, names=None, sweep: bool = True) ->
                           B, S, NB)
         ab = algorithmic_bytes(ctx_np, B, S, NB)
         ab["k1_fused"] = ab["k1a"] + ab["k1b"]
+        # the same-size yardstick: a plain streaming kernel moving each K1 kernel's byte pattern
+        # (K1a: 1024 B in and out per row; K1b: 4 x 256 B in at a 1280 B pitch, 256 B out per
+        # block) over every row / block, through the same copies and the same graph harness
+        units_a, units_b = B * S, B * (S // 4)
+
+        def yard(kind):
+            def mk(i):
+                iq, qn, kb = bufs(i)
+                if kind == "k1a":
+                    return lambda st: lib.qsa_testing_stream_yardstick(qn, iq, units_a, 1, 1280, 1280, 0, 1024, st)
+                return lambda st: lib.qsa_testing_stream_yardstick(kb, iq, units_b, 4, 1280, 5120, 1024, 256, st)
+            return mk
+        L["yardstick_k1a"], L["yardstick_k1b"] = yard("k1a"), yard("k1b")
+        n_sets["yardstick_k1a"], n_sets["yardstick_k1b"] = n_sets["k1a"], n_sets["k1b"]
+        touched["yardstick_k1a"], touched["yardstick_k1b"] = touched["k1a"], touched["k1b"]
+        ab["yardstick_k1a"], ab["yardstick_k1b"] = units_a * 2048, units_b * (1024 + 256)
         out = {}
         for name, mk in L.items():
             launches = [mk(i) for i in range(n_sets[name])]
@@ -508,6 +524,8 @@ def k1_configs_leg(qsa, lib, hbm_peak: float, names=None, sweep: bool = True) ->
             gbs = ab[name] / (ms * 1e-3) / 1e9
             out[name] = {"us": ms * 1e3, "alg_bytes": ab[name], "gbs": gbs, "frac_of_measured_hbm": gbs / hbm_peak,
                          "copies": n_sets[name], "touched_bytes": touched[name]}
+        for name in ("k1a", "k1b"):
+            out[name]["frac_of_yardstick"] = out[name]["gbs"] / out["yardstick_" + name]["gbs"]
         del bufs
         return out
 
@@ -555,7 +573,7 @@ def k1_configs_leg(qsa, lib, hbm_peak: float, names=None, sweep: bool = True) ->
             return lambda i: (iq[i].data_ptr(), qn[i].data_ptr(), kb[i].data_ptr())
         r = measure(B, S, NB, qsa.QSA_BF16, np.full(B, S, np.int32), make, cs, wq, wk, 1e-6)
         row = {"rows": B * S, "B": B, "S": S}
-        for name in ("k1a", "k1b", "k1_fused"):
+        for name in ("k1a", "k1b", "k1_fused", "yardstick_k1a", "yardstick_k1b"):
             row[name + "_gbs"] = r[name]["gbs"]
             row[name + "_us"] = r[name]["us"]
             row[name + "_copies"] = r[name]["copies"]
@@ -564,7 +582,8 @@ def k1_configs_leg(qsa, lib, hbm_peak: float, names=None, sweep: bool = True) ->
     res["how"] = ("per-launch device time from a CUDA graph of back-to-back launches (median of 10 replays); each "
                   "kernel cycles through copies of its inputs and outputs whose footprint exceeds 2x L2 (at most "
                   f"{K1_MAX_COPIES} copies); the sweep's inputs are drawn on the device (torch generator, seed 5), "
-                  "S=16384, ctx=S, bf16")
+                  "S=16384, ctx=S, bf16; yardstick_k1a / yardstick_k1b: qsa_testing_stream_yardstick moving "
+                  "the K1a / K1b byte pattern over every row / block in the same harness")
     res["l2_bytes"] = l2
     return res
 

@@ -37,6 +37,22 @@ int qsa_testing_index_scores_cuda_core(qsa_dtype_t dtype, float* logits, const v
  */
 int qsa_testing_bounded_wait_probe(int32_t timeoutMs, qsa_stream_t stream);
 
+/*
+ * A plain streaming kernel for same-size bandwidth comparisons (no computation of
+ * the page).  Unit u < units reads `rows` slices of `bytes` bytes at
+ *   src + u*unitPitch + r*rowPitch + offset,  r < rows,
+ * XORs them and writes `bytes` bytes at dst + u*bytes, one 16-byte chunk per
+ * thread with every row's load issued first.  With rows = 4, rowPitch = 1280,
+ * unitPitch = 5120, offset = 1024, bytes = 256 it moves what qsa_index_k_compress
+ * moves for B*numBlocks valid blocks; with rows = 1, rowPitch = unitPitch = 1280,
+ * offset = 0, bytes = 1024, what qsa_index_q_prep moves for B*seqLen valid rows.
+ * Limits: 1 <= rows <= 8, bytes a multiple of 16 in [16, 1024], pitches and offset
+ * multiples of 16, src/dst 16-byte aligned.
+ * Errors: QSA_E_NULL, QSA_E_SHAPE, QSA_E_ALIGN, QSA_E_CUDA.
+ */
+int qsa_testing_stream_yardstick(void* dst, const void* src, int64_t units, int32_t rows, int64_t rowPitch,
+                                 int64_t unitPitch, int64_t offset, int32_t bytes, qsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

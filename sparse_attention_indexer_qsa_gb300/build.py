@@ -25,7 +25,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["qsa_abi.cpp", "k1a_qprep.cu", "k1b_compress.cu", "k1_stream.cu", "k2_scores_tc.cu",
-           "k2_scores_cc.cu", "k2_topk_fused.cu", "k34_select.cu", "k_decode.cu", "k_decode_step.cu"]
+           "k2_scores_cc.cu", "k2_topk_fused.cu", "k34_select.cu", "k_decode.cu", "k_decode_step.cu", "yardstick.cu"]
 
 
 def nvcc() -> str:

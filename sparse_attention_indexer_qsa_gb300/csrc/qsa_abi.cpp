@@ -498,6 +498,27 @@ QSA_API int qsa_testing_index_scores_cuda_core(qsa_dtype_t dtype, float* logits,
   return launched(fn, qsa::launch_scores_cc(a));
 }
 
+QSA_API int qsa_testing_stream_yardstick(void* dst, const void* src, int64_t units, int32_t rows, int64_t rowPitch,
+                                         int64_t unitPitch, int64_t offset, int32_t bytes, qsa_stream_t stream) {
+  static const char* fn = "qsa_testing_stream_yardstick";
+  if (!dst || !src) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  if (units < 0 || rows < 1 || rows > qsa::yardstick_max_rows() || bytes < 16 || bytes > 1024 || bytes % 16 != 0 ||
+      rowPitch < 0 || unitPitch < 0 || offset < 0)
+    return fail(QSA_E_SHAPE, "%s: need units >= 0, 1 <= rows <= %d, bytes a multiple of 16 in [16, 1024]", fn,
+                qsa::yardstick_max_rows());
+  if (!aligned(dst, 16) || !aligned(src, 16) || rowPitch % 16 != 0 || unitPitch % 16 != 0 || offset % 16 != 0)
+    return fail(QSA_E_ALIGN, "%s: pointers, pitches and offset must be 16-byte aligned", fn);
+  if (units == 0) {
+    g_last_error[0] = '\0';
+    return QSA_OK;
+  }
+  DeviceInfo d;
+  int st = current_device(fn, &d);
+  if (st != QSA_OK) return st;
+  return launched(fn, qsa::launch_stream_yardstick(dst, src, units, rows, rowPitch, unitPitch, offset, bytes,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 QSA_API int qsa_device_fault_flags(uint32_t* flags, int clear, qsa_stream_t stream) {
   static const char* fn = "qsa_device_fault_flags";
   if (!flags) return fail(QSA_E_NULL, "%s: null flags pointer", fn);

@@ -160,6 +160,11 @@ cudaError_t read_fused_fault_flags(uint32_t* flags, bool clear, cudaStream_t str
 cudaError_t launch_scores_topk_fused(const LaunchScoresTopk& a);
 int32_t scores_topk_max_blocks();
 
+// Test-only plain streaming kernel with a K1 kernel's byte pattern (yardstick.cu).
+cudaError_t launch_stream_yardstick(void* dst, const void* src, int64_t units, int rows, int64_t row_pitch,
+                                    int64_t unit_pitch, int64_t offset, int bytes, cudaStream_t stream);
+int yardstick_max_rows();
+
 // TMA map (a CUtensorMap, 64-byte aligned) over the pool's V-tails for the tensor-core
 // decode scoring (k_decode.cu).
 cudaError_t encode_vtail_map(void* map, const PoolDev& pool);

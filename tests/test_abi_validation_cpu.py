@@ -75,6 +75,44 @@ def test_selection_entries(qsa):
     assert "65536" in qsa.qsa_last_error()
 
 
+def test_fused_scores_topk_expand(qsa):
+    L = qsa.load()
+    ok = lambda **o: [o.get(k, v) for k, v in dict(dt=0, out=P, q=P, kb=P, ctx=P, B=2, S=16, NB=4, r0=0, n=32,
+                                                    st=None).items()]
+    f = L.qsa_index_scores_topk_expand
+    assert f(*ok(dt=2)) == E_DTYPE
+    for arg in ("out", "q", "kb", "ctx"):
+        assert f(*ok(**{arg: None})) == E_NULL
+    assert f(*ok(S=0)) == E_SHAPE
+    assert f(*ok(NB=3)) == E_SHAPE                        # < ceilDiv(16, 4)
+    assert f(*ok(r0=1)) == E_RANGE
+    assert f(*ok(n=-1)) == E_RANGE
+    assert f(*ok(q=P + 8)) == E_ALIGN
+    assert f(*ok(kb=P + 8)) == E_ALIGN
+    assert f(*ok(out=P + 2)) == E_ALIGN
+    assert f(*ok(n=0)) == 0
+    # a row's selection state lives in shared memory: rows of at most 4096 blocks
+    assert f(*ok(NB=4097)) == E_SHAPE
+    assert "4096" in qsa.qsa_last_error()
+
+
+def test_stream_yardstick(qsa):
+    L = qsa.load()
+    ok = lambda **o: [o.get(k, v) for k, v in dict(dst=P, src=P, units=8, rows=4, rp=1280, up=5120, off=1024,
+                                                    nb=256, st=None).items()]
+    f = L.qsa_testing_stream_yardstick
+    assert f(*ok(dst=None)) == E_NULL
+    assert f(*ok(rows=0)) == E_SHAPE
+    assert f(*ok(rows=9)) == E_SHAPE
+    assert f(*ok(nb=24)) == E_SHAPE
+    assert f(*ok(nb=2048)) == E_SHAPE
+    assert f(*ok(units=-1)) == E_SHAPE
+    assert f(*ok(off=8)) == E_ALIGN
+    assert f(*ok(src=P + 8)) == E_ALIGN
+    assert f(*ok(units=0)) == 0
+    assert f(*ok()) == E_CUDA
+
+
 def test_pool_state_is_checked_by_every_paged_entry(qsa):
     L = qsa.load()
     calls = {
@@ -161,6 +199,7 @@ def test_no_gpu_means_a_loud_cuda_error(qsa):
     assert L.qsa_index_q_prep(0, P, P, P, P, P, 1e-6, 1, 8, None) == E_CUDA
     assert L.qsa_index_scores(0, P, P, P, P, 1, 8, 2, 0, 8, None) == E_CUDA
     assert L.qsa_index_scores_no_alloc(0, P, P, P, P, 1, 8, 2, 0, 8, None) == E_CUDA
+    assert L.qsa_index_scores_topk_expand(0, P, P, P, P, 2, 16, 4, 0, 32, None) == E_CUDA
     assert "cudaGetDevice" in qsa.qsa_last_error()
     flags = ctypes.c_uint32(0)
     assert L.qsa_device_fault_flags(ctypes.byref(flags), 1, None) == E_CUDA
