@@ -41,6 +41,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "qsa_bins.cuh"
 #include "qsa_launch.h"
 #include "qsa_select.cuh"
 #include "tc_ptx.cuh"
@@ -145,9 +146,8 @@ enum : uint32_t {
   kFaultDrain = 8u,
 };
 
-// First-pass bins: 64 bins an octave of the positive keys from `base` (key >> 17).
-constexpr int kBaseMin = 0x3FFE;   // keeps bin 2 = (+0, first log bin) a proper range
-constexpr int kBaseMax = 0x7F00;   // keeps (base + 255) << 17 inside 32 bits
+constexpr int kBaseMin = bins::kBaseMin;
+constexpr int kBaseMax = bins::kBaseMax;
 
 struct Params {
   uint32_t* sched;
@@ -255,32 +255,9 @@ __device__ __forceinline__ void keys2(const uint32_t (&r)[32], int k, uint64_t s
   k1 = sel::orderable(b);
 }
 
-// first-pass bin of a key, and the key range of a first-pass bin
-// -0 (and anything ordered below +0): bin 0; +0: bin 1; positive keys: 64 bins an
-// octave from `base`, clamped to [2, 255].
-__device__ __forceinline__ uint32_t bin0_of(uint32_t key, int32_t base) {
-  const int32_t d = static_cast<int32_t>(key >> 17) - base;
-  const uint32_t b = static_cast<uint32_t>(min(max(d, 2), 255));
-  return key <= 0x80000000u ? key >> 31 : b;
-}
-
+__device__ __forceinline__ uint32_t bin0_of(uint32_t key, int32_t base) { return bins::bin_of(key, base); }
 __device__ __forceinline__ void bin0_range(uint32_t b, int32_t base, uint32_t& lo, uint32_t& hi) {
-  const uint32_t ub = static_cast<uint32_t>(base);
-  if (b == 0u) {
-    lo = 0u;
-    hi = 0x7FFFFFFFu;
-  } else if (b == 1u) {
-    lo = hi = 0x80000000u;
-  } else if (b == 2u) {
-    lo = 0x80000001u;
-    hi = ((ub + 3u) << 17) - 1u;
-  } else if (b == 255u) {
-    lo = (ub + 255u) << 17;
-    hi = 0xFFFFFFFFu;
-  } else {
-    lo = (ub + b) << 17;
-    hi = ((ub + b + 1u) << 17) - 1u;
-  }
+  bins::bin_range(b, base, lo, hi);
 }
 
 __device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t v, int lane) {
@@ -1013,10 +990,8 @@ cudaError_t launch_scores_topk_fused(const LaunchScoresTopk& a) {
   p.units = static_cast<int32_t>(units);
   p.idesc = ptx::idesc_f16(a.bf16, kGTile, kN);
   p.scale = a.scale;
-  // first-pass bins centred a little below key(1.0f) >> 17: thresholds of unit-RMS
-  // q and kbar rows fall in [0.35, 5.3); each CTA then adapts the base to the
-  // thresholds it has seen
-  p.base0 = static_cast<int32_t>(0xBF800000u >> 17) - 100;
+  // each CTA then adapts the base to the thresholds it has seen
+  p.base0 = bins::kDefaultBase;
   const int grid = static_cast<int>(units < a.num_sms ? units : a.num_sms);
   k2_topk_fused_kernel<<<grid, kThreads, kSmemBytes, a.stream>>>(tq, tk, p);
   return cudaGetLastError();
