@@ -32,7 +32,7 @@
 //
 // Roles (one persistent CTA per SM, units taken from a device-wide counter, heaviest
 // tiles first): warp 0 scheduler + TMA producer, warp 1 TMEM allocator + MMA issuer,
-// warps 2..9 the epilogue (two per TMEM sub-partition, 32 tokens each).  Producer and
+// warps 2..17 the epilogue (four per TMEM sub-partition, 16 tokens each).  Producer and
 // MMA issuer learn after each histogram pass whether another one follows from a
 // decision ring the epilogue fills.  Every mbarrier wait is bounded; a wait that runs
 // out sets a fault bit, the CTA drains its own copies and MMAs, frees TMEM and exits.
