@@ -23,7 +23,7 @@ __device__ __forceinline__ uint32_t orderable(float f) {
 // ---------------------------------------------------------------------------
 // topk: one CTA of T threads per row.
 //
-//  1. histogram of the top kD1 key bits over the visible blocks (coalesced); warp 0
+//  1. histogram of the first digit (digit1) over the visible blocks (coalesced); warp 0
 //     finds the bin b1 holding the kSel-th largest key, the count above it and c1,
 //     its own count;
 //  2. one ordered pass: thread k owns the 32*MW contiguous blocks from 32*MW*k and
@@ -49,6 +49,52 @@ __device__ __forceinline__ uint32_t orderable(float f) {
 constexpr int kD1 = QSA_SEL_D1_BITS;
 constexpr int kBins1 = 1 << kD1;
 constexpr int kShift1 = 32 - kD1;
+
+// The first digit of a key: a monotone map of the u32 keys onto at most kBins1 bins,
+// each an exact prefix range of keys.  QSA_SEL_FINE_DIGIT = 0: the top kD1 key bits.
+// QSA_SEL_FINE_DIGIT = 1: keys whose sign-and-exponent field e = key >> 23 lies below
+// kFineLo or from kFineHi on take one bin an exponent (2^23 keys); the positive values
+// of the twelve octaves [2^-6, 2^6) take 128 bins an octave (key >> 16, 2^16 keys), so
+// that the bin of the 512th key of a row of relu-summed logits holds a few keys
+// instead of hundreds.  Which keys are selected does not depend on the map.
+#ifndef QSA_SEL_FINE_DIGIT
+#define QSA_SEL_FINE_DIGIT 1
+#endif
+constexpr uint32_t kFineLo = 256u + 127u - 6u;   // e of +2^-6
+constexpr uint32_t kFineHi = 256u + 127u + 6u;   // e of +2^6
+constexpr uint32_t kFineBins = (kFineHi - kFineLo) << 7;
+static_assert(kFineLo + kFineBins + (511u - kFineHi) < static_cast<uint32_t>(kBins1) || !QSA_SEL_FINE_DIGIT,
+              "the fine first digit needs 2048 bins");
+
+__device__ __forceinline__ uint32_t digit1(uint32_t key) {
+#if QSA_SEL_FINE_DIGIT
+  const uint32_t e = key >> 23;
+  const uint32_t fine = (key >> 16) - (kFineLo << 7) + kFineLo;
+  const uint32_t high = e - kFineHi + kFineLo + kFineBins;
+  return e < kFineLo ? e : (e < kFineHi ? fine : high);
+#else
+  return key >> kShift1;
+#endif
+}
+
+// the key range [lo, lo + 2^top - 1] of first-digit bin b
+__device__ __forceinline__ void digit1_range(uint32_t b, uint32_t& lo, int& top) {
+#if QSA_SEL_FINE_DIGIT
+  if (b < kFineLo) {
+    lo = b << 23;
+    top = 23;
+  } else if (b < kFineLo + kFineBins) {
+    lo = (b - kFineLo + (kFineLo << 7)) << 16;
+    top = 16;
+  } else {
+    lo = (b - kFineLo - kFineBins + kFineHi) << 23;
+    top = 23;
+  }
+#else
+  lo = b << kShift1;
+  top = kShift1;
+#endif
+}
 constexpr int kSuper = kBins1 / 128;   // 128-bin super-bins for the two-level search
 constexpr int kCpl = 16;               // listed candidates a lane of warp 0 may hold
 constexpr int kWarpCap = 32 * kCpl;
@@ -268,9 +314,9 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
   if constexpr (kRegs) {
 #pragma unroll
     for (int e = 0; e < 32; ++e)
-      if (g0 + e < n_vis) atomicAdd(&sh.hist1[kr[e] >> kShift1], 1u);
+      if (g0 + e < n_vis) atomicAdd(&sh.hist1[digit1(kr[e])], 1u);
   } else {
-    for_each_key<T>(keys, n_vis, [&](uint32_t key) { atomicAdd(&sh.hist1[key >> kShift1], 1u); });
+    for_each_key<T>(keys, n_vis, [&](uint32_t key) { atomicAdd(&sh.hist1[digit1(key)], 1u); });
   }
   __syncthreads();
   if (warp == 0) {
@@ -287,7 +333,10 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
   int32_t rem = k_sel - static_cast<int32_t>(sh.thr_above);
   const bool exact1 = c1 == static_cast<uint32_t>(rem);
   const bool listed = !exact1 && c1 <= static_cast<uint32_t>(kWarpCap);
-  const uint32_t lo1 = b1 << kShift1, hi1 = lo1 | ((1u << kShift1) - 1u);
+  uint32_t lo1;
+  int top1;
+  digit1_range(b1, lo1, top1);
+  const uint32_t hi1 = lo1 | ((1u << top1) - 1u);
 
   // ---- 2. ordered pass over this thread's contiguous blocks
   uint32_t gtm[MW], cm[MW];
@@ -303,7 +352,7 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
       for (int e = 0; e < 32; ++e) {
         if (gb + e < n_vis) {
           if (kr[e] > hi1) gtm[w] |= 1u << e;
-          if ((kr[e] >> kShift1) == b1) cm[w] |= 1u << e;
+          if (kr[e] >= lo1 && kr[e] <= hi1) cm[w] |= 1u << e;
         }
       }
     } else if (keys.vec && gb + 32 <= n_vis) {
@@ -316,7 +365,7 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
           const uint32_t key = orderable(xs[j]);
           const uint32_t bit = 1u << (4 * e + j);
           if (key > hi1) gtm[w] |= bit;
-          if ((key >> kShift1) == b1) cm[w] |= bit;
+          if (key >= lo1 && key <= hi1) cm[w] |= bit;
         }
       }
     } else if (gb < n_vis) {
@@ -326,7 +375,7 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
         if (e < n) {
           const uint32_t key = orderable(keys.ld1(gb + e));
           if (key > hi1) gtm[w] |= 1u << e;
-          if ((key >> kShift1) == b1) cm[w] |= 1u << e;
+          if (key >= lo1 && key <= hi1) cm[w] |= 1u << e;
         }
       }
     }
@@ -379,10 +428,10 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
         }
         __syncwarp();
       }
-      uint32_t prefix = lo1, mask = ~((1u << kShift1) - 1u);
+      uint32_t prefix = lo1, mask = ~((1u << top1) - 1u);
       int32_t rm = rem;
 #pragma unroll 1
-      for (int top = kShift1; top > 0;) {
+      for (int top = top1; top > 0;) {
         const int width = min(8, top);
         const int shift = top - width;
         const uint32_t dmask = (1u << width) - 1u;
@@ -432,9 +481,9 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
       }
     }
   } else if (!exact1) {  // more candidates than warp 0 holds: passes over the row
-    uint32_t prefix = lo1, mask = ~((1u << kShift1) - 1u);
+    uint32_t prefix = lo1, mask = ~((1u << top1) - 1u);
 #pragma unroll 1
-    for (int top = kShift1; top > 0;) {
+    for (int top = top1; top > 0;) {
       const int width = min(8, top);
       const int shift = top - width;
       const uint32_t dmask = (1u << width) - 1u;
