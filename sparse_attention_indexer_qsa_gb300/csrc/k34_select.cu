@@ -5,7 +5,7 @@
 //   expand        K4: top kSel = min(512, nVis) sorted block ids -> token ids
 //                 4*id + j, then the causal tail, then -1 to width 2051
 //   topk          the whole selection of a row in one CTA, without a segmented
-//                 sort or its workspace: an MSB-first radix select (an 11-bit first
+//                 sort or its workspace: an MSB-first radix select (a 1024-bin first
 //                 digit, then 8-bit digits over the candidates it leaves) on the
 //                 order-preserving u32 map of the FP32 logits finds the kSel-th
 //                 largest key; keys above it, and keys equal to it in ascending

@@ -38,10 +38,10 @@ __device__ __forceinline__ uint32_t orderable(float f) {
 //     position of its first winner; winners are written in ascending order and the
 //     row is expanded.
 // Keys are read from global memory (L1/L2 after the first pass).  Small CTAs (64
-// threads, 8.2 KB of shared memory, 24 a SM) keep many rows in flight: the warp-0
+// threads, 4.1 KB of shared memory, 24 a SM) keep many rows in flight: the warp-0
 // steps between the passes are serial and would otherwise leave the SM idle.
 #ifndef QSA_SEL_D1_BITS
-#define QSA_SEL_D1_BITS 11
+#define QSA_SEL_D1_BITS 10
 #endif
 #ifndef QSA_SEL_WARPS_PER_SM
 #define QSA_SEL_WARPS_PER_SM 48
@@ -54,22 +54,25 @@ constexpr int kShift1 = 32 - kD1;
 // each an exact prefix range of keys.  QSA_SEL_FINE_DIGIT = 0: the top kD1 key bits.
 // QSA_SEL_FINE_DIGIT = 1: keys whose sign-and-exponent field e = key >> 23 lies below
 // kFineLo or from kFineHi on take one bin an exponent (2^23 keys); the positive values
-// of the twelve octaves [2^-6, 2^6) take 128 bins an octave (key >> 16, 2^16 keys), so
-// that the bin of the 512th key of a row of relu-summed logits holds a few keys
-// instead of hundreds.  Which keys are selected does not depend on the map.
+// of the octaves around 1.0 take finer bins (1024 bins: 64 an octave over [2^-4, 2^4),
+// key >> 17), so that the bin of the 512th key of a row of relu-summed logits holds
+// tens of keys instead of hundreds.  Which keys are selected does not depend on the map.
 #ifndef QSA_SEL_FINE_DIGIT
 #define QSA_SEL_FINE_DIGIT 1
 #endif
-constexpr uint32_t kFineLo = 256u + 127u - 6u;   // e of +2^-6
-constexpr uint32_t kFineHi = 256u + 127u + 6u;   // e of +2^6
-constexpr uint32_t kFineBins = (kFineHi - kFineLo) << 7;
+// 2048 bins: 128 bins an octave over [2^-6, 2^6); 1024 bins: 64 an octave over [2^-4, 2^4)
+constexpr int kFineShift = kD1 >= 11 ? 16 : 17;                  // fine bins: key >> kFineShift
+constexpr uint32_t kFineOctaves = kD1 >= 11 ? 6u : 4u;           // on each side of 1.0
+constexpr uint32_t kFineLo = 256u + 127u - kFineOctaves;         // e of +2^-kFineOctaves
+constexpr uint32_t kFineHi = 256u + 127u + kFineOctaves;
+constexpr uint32_t kFineBins = (kFineHi - kFineLo) << (23 - kFineShift);
 static_assert(kFineLo + kFineBins + (511u - kFineHi) < static_cast<uint32_t>(kBins1) || !QSA_SEL_FINE_DIGIT,
-              "the fine first digit needs 2048 bins");
+              "the fine first digit does not fit the bins");
 
 __device__ __forceinline__ uint32_t digit1(uint32_t key) {
 #if QSA_SEL_FINE_DIGIT
   const uint32_t e = key >> 23;
-  const uint32_t fine = (key >> 16) - (kFineLo << 7) + kFineLo;
+  const uint32_t fine = (key >> kFineShift) - (kFineLo << (23 - kFineShift)) + kFineLo;
   const uint32_t high = e - kFineHi + kFineLo + kFineBins;
   return e < kFineLo ? e : (e < kFineHi ? fine : high);
 #else
@@ -84,8 +87,8 @@ __device__ __forceinline__ void digit1_range(uint32_t b, uint32_t& lo, int& top)
     lo = b << 23;
     top = 23;
   } else if (b < kFineLo + kFineBins) {
-    lo = (b - kFineLo + (kFineLo << 7)) << 16;
-    top = 16;
+    lo = (b - kFineLo + (kFineLo << (23 - kFineShift))) << kFineShift;
+    top = kFineShift;
   } else {
     lo = (b - kFineLo - kFineBins + kFineHi) << 23;
     top = 23;
@@ -106,8 +109,8 @@ static_assert(kWarpCap <= kBins1, "the candidate list reuses the histogram's sto
 // (words [0, kWarpCap)), the radix counts (words [kHist2Word, +256)), the candidates'
 // classes (bytes from word kClsWord) and, last, the winners (words [0, kTopK)).  Each
 // reuse is separated from the previous use by CTA barriers.
-constexpr int kHist2Word = 1024;
-constexpr int kClsWord = 1536;
+constexpr int kHist2Word = kBins1 >= 2048 ? 1024 : kWarpCap;
+constexpr int kClsWord = kBins1 >= 2048 ? 1536 : kHist2Word + 256;
 static_assert(kWarpCap <= kHist2Word && kTopK <= kHist2Word && kHist2Word + 256 <= kClsWord &&
                   kClsWord + kWarpCap / 4 <= kBins1,
               "selection shared-memory layout");
