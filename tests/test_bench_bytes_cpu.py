@@ -15,7 +15,7 @@ T = 2  # bytes per element
 
 
 def enumerate_bytes(ctx, B, S, NB):
-    k1a = k1b = k2 = select = flops = 0
+    k1a = k1b = k2 = select = fused = flops = 0
     positions = set()
     k_positions = set()
     for b in range(B):
@@ -25,6 +25,7 @@ def enumerate_bytes(ctx, B, S, NB):
                 k1a += 4 * 128 * T + 4 * 128 * T  # read q heads, write qNormed
                 positions.add(t)
                 k2 += 4 * 128 * T  # q row read once
+                fused += 4 * 128 * T
                 vis = min((t + 1) // 4, NB)
                 select += vis * 4
                 flops += vis * 4 * 128 * 2
@@ -35,13 +36,16 @@ def enumerate_bytes(ctx, B, S, NB):
                 k1b += 4 * 128 * T + 128 * T  # four raw K rows read, kbar row written
                 k_positions.add(4 * g)
                 k2 += 128 * T  # each visible kbar row read once per sequence
+                fused += 128 * T
             else:
                 k1b += 128 * T
     k1a += len(positions) * 64 * 4  # one FP32 cos/sin row per distinct position
     k1b += len(k_positions) * 64 * 4
     k2 += B * S * NB * 4  # every logit written (masked cells too)
     select += B * S * 2051 * 4  # 2051 token ids per row
-    return {"k1a": k1a, "k1b": k1b, "k2": k2, "select": select, "k2_causal_flops": flops}
+    fused += B * S * 2051 * 4  # scoring fused with selection: no logits, the ids written
+    return {"k1a": k1a, "k1b": k1b, "k2": k2, "select": select, "fused_select": fused,
+            "k2_causal_flops": flops}
 
 
 @pytest.mark.parametrize("B,S,NB,ctx", [
