@@ -375,11 +375,15 @@ int qsa_topk_expand_decode(int32_t* outIdx, const float* logits, const int32_t* 
  * Each CTA computes its sequence's q heads once and scores a run of 128-block chunks
  * of that sequence (the run length sizes the grid to about one wave of resident
  * CTAs); the CTA that completes a sequence last runs its selection, so no CTA waits
- * for another.  Sequences report completion
- * through a device-side counter set, one of 16 taken in turn by each launch: at most
- * 16 launches may be in flight on one device at a time, and a CUDA graph that captured
- * a launch keeps its set on every replay, so one captured graph must not be replayed
- * concurrently with itself.
+ * for another.  For batches of up to 64 sequences, the scoring CTAs also count every
+ * logit they write into the row's first-digit histogram of the selection, which the
+ * last CTA copies instead of counting the row again (and leaves zeroed).  Sequences
+ * report completion through a device-side set of counters (and of histograms), one of
+ * 16 taken in turn by each launch: at most 16 launches may be in flight on one device
+ * at a time, and a CUDA graph that captured a launch keeps its set on every replay, so
+ * one captured graph must not be replayed concurrently with itself.  The sets are
+ * module memory of the library (256 KB of counters, 4 MB of histograms a device),
+ * zero at load; no call allocates.
  * Limits: batchSize <= 4096, maxBlocks <= 65536.
  * Errors: QSA_E_NULL, QSA_E_DTYPE, QSA_E_SHAPE, QSA_E_ALIGN, QSA_E_CUDA.
  */

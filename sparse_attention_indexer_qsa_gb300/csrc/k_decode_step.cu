@@ -15,9 +15,12 @@
 //   - the last CTA of sequence b to finish (a per-sequence arrival counter, no waiting)
 //     runs the top-512 selection of row b on the logits at L2, writes outIdx[b], zeroes
 //     b's split counters and puts the counter back to zero.  Its shared memory for the
-//     selection reuses the engine's operand stages.
+//     selection reuses the engine's operand stages.  For batches of up to kHistBatch
+//     sequences with more than 512 visible blocks, the scoring CTAs also count each
+//     logit they write into the row's first-digit histogram, so that the last CTA
+//     copies it instead of counting the row again, and zeroes it.
 // Every value equals the one the three separate kernels give: the same device routines
-// compute it.  Arrival counters: kStepSlots sets of kStepMaxBatch, one set a launch in
+// compute it.  Arrival counters and histograms: kStepSlots sets, one set a launch in
 // turn (so up to kStepSlots launches may run at once on a device), zero at module load
 // and left at zero by every launch.
 #include <algorithm>
@@ -33,8 +36,10 @@ namespace qsa {
 
 constexpr int kStepSlots = 16;
 constexpr int kStepMaxBatch = 4096;
+constexpr int kHistBatch = 64;     // batches up to this size count the rows' histograms while scoring
 constexpr int kStepCtasPerSm = 2;  // the resident CTAs of decode_step_kernel an SM is sized for
 __device__ __align__(256) uint32_t g_decode_step_arrivals[kStepSlots * kStepMaxBatch];
+__device__ __align__(256) uint32_t g_decode_step_hist[kStepSlots * kHistBatch * sel::kBins1];
 __device__ uint32_t g_step_fault_flags;
 
 namespace dec {
@@ -51,7 +56,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
                    const int32_t* __restrict__ ctx, const uint16_t* __restrict__ w_q,
                    const uint16_t* __restrict__ w_k, float eps, const PoolDev pool,
                    int32_t* __restrict__ split_counters, int32_t num_kv_heads, int32_t max_blocks, float scale,
-                   int32_t per_cta, uint32_t* __restrict__ arrivals) {
+                   int32_t per_cta, uint32_t* __restrict__ arrivals, uint32_t* __restrict__ hists) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(16) float g1q[kHeadDim];
   __shared__ __align__(16) float g1k[kHeadDim];
@@ -66,6 +71,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
   const int32_t n_vis = c > 0 ? min(c / kRatio, max_blocks) : 0;
   const int32_t g_begin = y * per_cta;
   const int32_t g_end = min(g_begin + per_cta, n_vis);
+  uint32_t* const hist = hists != nullptr && n_vis > sel::kTopK ? hists + static_cast<int64_t>(b) * sel::kBins1 : nullptr;
   // the CTA that compresses block g_new = c/4 - 1 (if this step completes one): the
   // one whose run holds it, or the last one if g_new lies past maxBlocks
   const int32_t g_new = c > 0 && c % kRatio == 0 ? c / kRatio - 1 : -1;
@@ -118,17 +124,15 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
   if (tid == 0) ptx::fence_proxy_async_global();
   float* lrow = logits + static_cast<int64_t>(b) * max_blocks;
   dtc::engine_run<T::kIsBf16>(en, tmem, &pool_map, vpages, pool.head_size, g_begin, g_end, lrow, scale,
-                              pre_limit);
+                              pre_limit, hist);
   dtc::engine_teardown(tmem);
 
-  // ---- the last CTA of sequence b selects its row
-  if (tid == 0) {
-    __threadfence();  // this CTA's logits, before its arrival
-    last = atomicAdd(arrivals + b, 1u) == gridDim.y - 1 ? 1 : 0;
-  }
+  // ---- the last CTA of sequence b selects its row.  The arrival releases this CTA's
+  // logits and histogram counts (ordered before it by the teardown's CTA barrier) and
+  // acquires those of the CTAs that arrived before.
+  if (tid == 0) last = ptx::atom_add_acq_rel_gpu(arrivals + b, 1u) == gridDim.y - 1 ? 1 : 0;
   __syncthreads();
   if (!last) return;
-  __threadfence();  // every CTA's logits of row b, before they are read
   if (tid == 0) arrivals[b] = 0u;
   if (split_counters != nullptr)
     for (int k = tid; k < num_kv_heads; k += kDecThreads) split_counters[static_cast<int64_t>(b) * num_kv_heads + k] = 0;
@@ -140,7 +144,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
   }
   sel::SelShared<kDecThreads>& sh = *reinterpret_cast<sel::SelShared<kDecThreads>*>(en.ptr + dtc::kOffA);
   const sel::L2Keys keys{lrow, (reinterpret_cast<uintptr_t>(lrow) & 15u) == 0};
-  sel::select_row<kDecThreads, MW, MW == 1>(keys, n_vis, sh);
+  sel::select_row<kDecThreads, MW, MW == 1>(keys, n_vis, sh, hist);
   sel::write_selected<kDecThreads>(out, sh.win(), tail, n_vis);
 }
 
@@ -149,6 +153,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
 namespace {
 std::mutex g_step_mu;
 uint32_t* g_step_base[64] = {};
+uint32_t* g_step_hist_base[64] = {};
 uint32_t g_step_seq[64] = {};
 }  // namespace
 
@@ -162,15 +167,21 @@ cudaError_t launch_decode_step(bool bf16, int32_t* out_idx, float* logits, void*
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   uint32_t* arrivals = nullptr;
+  uint32_t* hists = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_step_mu);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (g_step_base[dev] == nullptr) {  // the symbol's device address, once per device
+    if (g_step_base[dev] == nullptr) {  // the symbols' device addresses, once per device
       void* ptr = nullptr;
       if ((e = cudaGetSymbolAddress(&ptr, g_decode_step_arrivals)) != cudaSuccess) return e;
+      void* hptr = nullptr;
+      if ((e = cudaGetSymbolAddress(&hptr, g_decode_step_hist)) != cudaSuccess) return e;
       g_step_base[dev] = static_cast<uint32_t*>(ptr);
+      g_step_hist_base[dev] = static_cast<uint32_t*>(hptr);
     }
-    arrivals = g_step_base[dev] + static_cast<int64_t>(g_step_seq[dev]++ % kStepSlots) * kStepMaxBatch;
+    const int64_t slot = g_step_seq[dev]++ % kStepSlots;
+    arrivals = g_step_base[dev] + slot * kStepMaxBatch;
+    if (batch <= kHistBatch) hists = g_step_hist_base[dev] + slot * kHistBatch * sel::kBins1;
   }
   // Y CTAs a sequence, each over a run of per_cta blocks: about one wave of resident CTAs
   // over the batch, so that each CTA computes the q heads once
@@ -210,7 +221,7 @@ cudaError_t launch_decode_step(bool bf16, int32_t* out_idx, float* logits, void*
 #define QSA_STEP_LAUNCH(T, MW)                                                                             \
   dec::decode_step_kernel<T, MW><<<grid, dec::kDecThreads, dec::kStepSmem, stream>>>(                     \
       map, out_idx, logits, q, iq, cos_sin, ctx, wq, wk, eps, pool, split_counters, num_kv_heads, max_blocks,     \
-      scale, per_cta, arrivals)
+      scale, per_cta, arrivals, hists)
 #define QSA_STEP_DISPATCH(T)                 \
   do {                                       \
     if (words <= 1) QSA_STEP_LAUNCH(T, 1);   \

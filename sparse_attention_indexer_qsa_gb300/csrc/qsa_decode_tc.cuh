@@ -25,6 +25,7 @@
 
 #include "qsa_common.cuh"
 #include "qsa_launch.h"
+#include "qsa_select.cuh"
 #include "tc_ptx.cuh"
 
 namespace qsa {
@@ -208,12 +209,13 @@ __device__ __forceinline__ void engine_teardown(uint32_t tmem) {
 // The roles over the run's tiles, after engine_setup.  pages: stage_vpages of the run
 // (visible to every thread); out: the sequence's logits row; pool map: 3-D
 // {poolHeadDim, 4 x numKVHeads, 2 x numPages x 32} over the pool, box {64, 1, 32},
-// 128-byte swizzle; limit: the one given to engine_start.  Warps 6+ (if any) return
-// at once.
+// 128-byte swizzle; limit: the one given to engine_start; hist (optional): the row's
+// first-digit histogram of the selection (sel::digit1 bins), to which every logit the
+// run writes adds one.  Warps 6+ (if any) return at once.
 template <bool kBf16>
 __device__ __forceinline__ void engine_run(const Engine& en, uint32_t tmem, const CUtensorMap* map,
                                            const int32_t* pages, int32_t head_size, int32_t g_run, int32_t g_end,
-                                           float* out, float scale, int limit) {
+                                           float* out, float scale, int limit, uint32_t* hist = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = run_tiles(g_run, g_end);
   if (warp == 0) {
@@ -279,7 +281,9 @@ __device__ __forceinline__ void engine_run(const Engine& en, uint32_t tmem, cons
         float v = __fadd_rn(fmaxf(0.0f, __uint_as_float(r[0])), fmaxf(0.0f, __uint_as_float(r[1])));
         v = __fadd_rn(v, fmaxf(0.0f, __uint_as_float(r[2])));
         v = __fadd_rn(v, fmaxf(0.0f, __uint_as_float(r[3])));
-        out[g] = usable ? __fmul_rn(v, scale) : -FLT_MAX;
+        const float logit = usable ? __fmul_rn(v, scale) : -FLT_MAX;
+        out[g] = logit;
+        if (hist != nullptr) atomicAdd(hist + sel::digit1(sel::orderable(logit)), 1u);
       }
     }
   }

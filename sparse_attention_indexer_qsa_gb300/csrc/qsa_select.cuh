@@ -285,7 +285,8 @@ __device__ __forceinline__ void for_each_key(const K& keys, int32_t n, F&& f) {
 // its 32 contiguous keys once and keeps them in registers, so the ordered pass and the
 // candidate resolution read no key from memory again.
 template <int T, int MW, bool kRegs = false, class K>
-__device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShared<T>& sh) {
+__device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShared<T>& sh,
+                                           uint32_t* ghist = nullptr) {
   static_assert(!kRegs || MW == 1, "keys in registers: one 32-key word a thread");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t k_sel = kTopK;
@@ -294,7 +295,17 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
   const int wpt = kRegs ? 1 : min(MW, static_cast<int>((n_vis + 32 * T - 1) / (32 * T)));
   const int32_t g0 = tid * (32 * wpt);
 
-  // ---- 1. first-digit histogram and its threshold bin
+  // ---- 1. first-digit histogram and its threshold bin.  ghist (optional, 16-byte
+  // aligned): the row's kBins1 first-digit counts, added by the kernels that wrote the
+  // keys and made visible to this CTA; they are copied (loads issued before the keys')
+  // and ghist is left zeroed for the next row that counts into it.
+  constexpr int kHq = (kBins1 / 4 + T - 1) / T;  // 16-byte pieces of ghist a thread copies
+  uint4 gh[kHq];
+  if (ghist != nullptr) {
+#pragma unroll
+    for (int q = 0; q < kHq; ++q)
+      if (tid + q * T < kBins1 / 4) gh[q] = __ldcg(reinterpret_cast<const uint4*>(ghist) + tid + q * T);
+  }
   uint32_t kr[kRegs ? 32 : 1];  // kRegs: keys of blocks g0 .. g0 + 31 (those >= n_vis unused)
   if constexpr (kRegs) {
     if (keys.vec && g0 + 32 <= n_vis) {
@@ -311,17 +322,30 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
       for (int e = 0; e < 32; ++e) kr[e] = g0 + e < n_vis ? orderable(keys.ld1(g0 + e)) : 0u;
     }
   }
-  for (int k = tid; k < kBins1 / 4; k += T) reinterpret_cast<uint4*>(sh.hist1)[k] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int q = 0; q < kHq; ++q) {
+    const int k = tid + q * T;
+    if (k < kBins1 / 4) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (ghist != nullptr) {
+        v = gh[q];
+        __stcg(reinterpret_cast<uint4*>(ghist) + k, make_uint4(0u, 0u, 0u, 0u));
+      }
+      reinterpret_cast<uint4*>(sh.hist1)[k] = v;
+    }
+  }
   if (tid == 0) sh.ncand = 0;
   __syncthreads();
-  if constexpr (kRegs) {
+  if (ghist == nullptr) {
+    if constexpr (kRegs) {
 #pragma unroll
-    for (int e = 0; e < 32; ++e)
-      if (g0 + e < n_vis) atomicAdd(&sh.hist1[digit1(kr[e])], 1u);
-  } else {
-    for_each_key<T>(keys, n_vis, [&](uint32_t key) { atomicAdd(&sh.hist1[digit1(key)], 1u); });
+      for (int e = 0; e < 32; ++e)
+        if (g0 + e < n_vis) atomicAdd(&sh.hist1[digit1(kr[e])], 1u);
+    } else {
+      for_each_key<T>(keys, n_vis, [&](uint32_t key) { atomicAdd(&sh.hist1[digit1(key)], 1u); });
+    }
+    __syncthreads();
   }
-  __syncthreads();
   if (warp == 0) {
     const Threshold th = find_first_digit(sh.hist1, static_cast<uint32_t>(k_sel));
     if (lane == 0) {

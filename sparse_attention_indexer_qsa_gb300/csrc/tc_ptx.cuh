@@ -170,6 +170,16 @@ __device__ __forceinline__ void launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Device-scope atomic add with acquire-release semantics, returning the old value: the
+// writes that precede it (this thread's, and those ordered before it by a CTA barrier)
+// are visible to whoever acquires the new value, and the writes released before the
+// old value are visible after it.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA with
 // 128-byte swizzle: rows of 128 bytes (64 two-byte elements), 8-row swizzle atoms
 // of 1024 bytes stacked along M/N (stride-dimension offset 1024 B).  The leading

@@ -470,6 +470,57 @@ def test_fused_decode_step_at_the_batch_limit():
     assert qsa.qsa_device_fault_flags() == 0
 
 
+@pytest.mark.parametrize("B", [1, 64, 65])
+def test_fused_decode_step_histogram_batch_edge(B):
+    """Batches up to 64 sequences count each row's first-digit histogram while scoring
+    (the last CTA copies and zeroes it); larger ones count it in the selection.  On both
+    sides of that edge, with rows of 500 to 4096 visible blocks, two launches in a row
+    equal the three separate calls bit for bit, and the selection equals the oracle's
+    on the same logits."""
+    qsa = _qsa()
+    max_ctx = 16384
+    pages = (max_ctx + 127) // 128
+    num_pages = B * pages
+    gen = torch.Generator(device="cuda").manual_seed(29 + B)
+    pool0 = torch.randn((2 * num_pages, 128, 1, 128), device="cuda", generator=gen).to(torch.bfloat16)
+    perm = torch.randperm(num_pages, device="cuda", generator=gen).to(torch.int32).view(B, pages)
+    table = torch.stack([perm, perm + num_pages], dim=1).contiguous()
+    ctx = torch.randint(2000, max_ctx + 1, (B,), device="cuda", generator=gen, dtype=torch.int32)
+    ctx[0] = max_ctx
+    rows = torch.randn((B, 640), device="cuda", generator=gen).to(torch.bfloat16)
+    cs = torch.randn((max_ctx, 64), device="cuda", generator=gen)
+    wq = (torch.randn(128, device="cuda", generator=gen) * 0.1).to(torch.bfloat16)
+    wk = (torch.randn(128, device="cuda", generator=gen) * 0.1).to(torch.bfloat16)
+    maxb = max_ctx // 4
+    pools = [pool0.clone(), pool0.clone()]
+    states = [qsa.pool_state(p_, table, num_pages, numKVHeads=1, poolHeadDim=128, headSize=0) for p_ in pools]
+
+    def bufs():
+        return dict(q=torch.empty((B, 1, 4, 128), dtype=torch.bfloat16, device="cuda"),
+                    logits=torch.full((B, maxb), float("nan"), device="cuda"),
+                    out=torch.empty((B, 2051), dtype=torch.int32, device="cuda"),
+                    split=torch.full((B, 2), 3, dtype=torch.int32, device="cuda"))
+    three, fused = bufs(), bufs()
+    qsa.qsa_indexer_pre_decode(three["q"], rows, cs, ctx, wq, wk, 1e-6, states[0], B)
+    qsa.qsa_index_scores_decode(three["logits"], three["q"], ctx, states[0], B, maxb)
+    qsa.qsa_topk_expand_decode(three["out"], three["logits"], ctx, three["split"], 2, B, maxb)
+    for _ in range(2):   # twice: the histograms and counters must be back at zero after the first
+        fused["logits"].fill_(float("nan"))
+        qsa.qsa_indexer_decode_step(fused["out"], fused["logits"], fused["q"], rows, cs, ctx, wq, wk, 1e-6,
+                                    states[1], fused["split"], 2, B, maxb)
+        torch.cuda.synchronize()
+        for name in ("q", "out", "split"):
+            assert torch.equal(three[name], fused[name]), name
+        assert torch.equal(pools[0], pools[1])
+    nv = (ctx // 4).cpu().numpy()
+    lf = fused["logits"].cpu().numpy()
+    for b in range(B):
+        assert np.array_equal(three["logits"][b, :nv[b]].cpu().numpy().view(np.uint32), lf[b, :nv[b]].view(np.uint32)), b
+    want = oracle.topk_expand_decode(np.where(np.isnan(lf), np.float32(-np.finfo(np.float32).max), lf), ctx.cpu().numpy())
+    assert np.array_equal(fused["out"].cpu().numpy(), want)
+    assert qsa.qsa_device_fault_flags() == 0
+
+
 def test_fused_decode_steps_in_flight_on_two_streams():
     """Launches of the one-launch step overlap on two streams (each launch takes its own
     arrival-counter set): 24 launches, alternating streams, on two independent problems,
