@@ -104,14 +104,15 @@ __global__ void __launch_bounds__(kScoresThreads, kScoresCtasPerSm)
   const int32_t c = __ldg(ctx + b);
   const int32_t n_vis = c > 0 ? min(c / kRatio, max_blocks) : 0;
   const int32_t g_begin = blockIdx.y * run;
-  if (g_begin >= n_vis) return;  // only the valid prefix is written (the whole CTA leaves)
   const int32_t g_end = min(g_begin + run, n_vis);
   const int tid = threadIdx.x, warp = tid >> 5;
-  if (warp == 0) {  // the page entries, then the first tiles' copies, before the CTA barrier
-    stage_vpages(vpages, pool, b, g_begin, g_end, tid, 32);
+  if (warp == 0) {
+    // the page entries of the whole run (their loads need not wait for the context
+    // length), then the first tiles' copies, before the CTA barrier
+    stage_vpages(vpages, pool, b, g_begin, min(g_begin + run, max_blocks), tid, 32);
     __syncwarp();
-    dtc::engine_start(en, &pool_map, vpages, pool.head_size, g_begin, g_end, dtc::kStages);
-  } else {
+    if (g_begin < n_vis) dtc::engine_start(en, &pool_map, vpages, pool.head_size, g_begin, g_end, dtc::kStages);
+  } else if (g_begin < n_vis) {
     const int k = tid - 32;
     if (k < kNumQHeads * 16) {
       const int h = k >> 4, ch = k & 15;
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kScoresThreads, kScoresCtasPerSm)
     dtc::zero_b_padding(en, k, kScoresThreads - 32);
     ptx::fence_proxy_async_shared();
   }
+  if (g_begin >= n_vis) return;  // only the valid prefix is written (the whole CTA leaves)
   const uint32_t tmem = dtc::engine_setup(en);
   dtc::engine_run<kBf16>(en, tmem, &pool_map, vpages, pool.head_size, g_begin, g_end,
                          logits + static_cast<int64_t>(b) * max_blocks, scale, dtc::kStages);

@@ -79,22 +79,27 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
   // tiles copied before the CTA barrier: in the owning CTA, none from g_new's tile on
   // (its V-tail is written below)
   const int pre_limit = owner && g_new < g_end ? (g_new - g_begin) / dtc::kTile : dtc::kStages;
+  const uint16_t* row = index_qk + static_cast<int64_t>(b) * kRowWidth;
+  QHeadsIn qin{};
+  CompressIn cin{};
   if (warp == 0) {
-    stage_vpages(vpages, pool, b, g_begin, g_end, tid, 32);
+    stage_vpages(vpages, pool, b, g_begin, min(g_begin + per_cta, max_blocks), tid, 32);
     __syncwarp();
     dtc::engine_start(en, &pool_map, vpages, pool.head_size, g_begin, g_end, pre_limit);
   } else {
+    // the q heads' and the block compress's loads, in flight across the barrier
+    if (warp == 2) qin = q_heads_load(row, cos_sin, c, lane);
+    if (warp == 3 && owner) cin = compress_load(pool, b, c, row, cos_sin, lane);
     stage_gamma<T>(w_q, g1q, tid - 32, kDecThreads - 32);
     stage_gamma<T>(w_k, g1k, tid - 32, kDecThreads - 32);
     dtc::zero_b_padding(en, tid - 32, kDecThreads - 32);
   }
   __syncthreads();
-  const uint16_t* row = index_qk + static_cast<int64_t>(b) * kRowWidth;
   const int h = lane >> 3, j = lane & 7;
   const int ca = chunk_a(j), cb = chunk_b(j);
   if (warp == 2) {
     uint4 oa, ob;
-    q_heads<T>(row, cos_sin, c, g1q, eps, lane, oa, ob);
+    q_heads_finish<T>(qin, c, g1q, eps, lane, oa, ob);
     dtc::put_q_chunk(en, h, ca / 8, oa);
     dtc::put_q_chunk(en, h, cb / 8, ob);
     if (y == 0) {
@@ -110,11 +115,10 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
       }
     } else if (owner) {
       uint4 oa, ob;
-      uint16_t* vtail = nullptr;
-      const bool ok = compress_block<T>(pool, b, c, row, cos_sin, g1k, eps, lane, oa, ob, &vtail);
-      if (ok && h == 0) {
-        st_v4(vtail + ca, oa);
-        st_v4(vtail + cb, ob);
+      compress_finish<T>(cin, g1k, eps, lane, oa, ob);
+      if (cin.ok && h == 0) {
+        st_v4(cin.vtail + ca, oa);
+        st_v4(cin.vtail + cb, ob);
       }
       ptx::fence_proxy_async_global();  // the V-tail, before this CTA's TMA copies read it
     }
