@@ -365,7 +365,10 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
   digit1_range(b1, lo1, top1);
   const uint32_t hi1 = lo1 | ((1u << top1) - 1u);
 
-  // ---- 2. ordered pass over this thread's contiguous blocks
+  // ---- 2. ordered pass over this thread's contiguous blocks (keys in registers:
+  // branch-free bit masks, key in [lo1, hi1] as one unsigned compare, the word's keys
+  // past n_vis masked off)
+  const uint32_t span1 = hi1 - lo1;
   uint32_t gtm[MW], cm[MW];
 #pragma unroll
   for (int w = 0; w < MW; ++w) {
@@ -375,13 +378,16 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
     if (w >= wpt) {
       // not this row's word
     } else if constexpr (kRegs) {
+      uint32_t gt = 0u, in = 0u;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        if (gb + e < n_vis) {
-          if (kr[e] > hi1) gtm[w] |= 1u << e;
-          if (kr[e] >= lo1 && kr[e] <= hi1) cm[w] |= 1u << e;
-        }
+        gt |= static_cast<uint32_t>(kr[e] > hi1) << e;
+        in |= static_cast<uint32_t>(kr[e] - lo1 <= span1) << e;
       }
+      const int32_t nk = n_vis - gb;  // keys of this word that exist
+      const uint32_t valid = nk >= 32 ? 0xFFFFFFFFu : (nk > 0 ? (1u << nk) - 1u : 0u);
+      gtm[w] = gt & valid;
+      cm[w] = in & valid;
     } else if (keys.vec && gb + 32 <= n_vis) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
