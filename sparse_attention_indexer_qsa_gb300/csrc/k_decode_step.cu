@@ -76,9 +76,13 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
   // one whose run holds it, or the last one if g_new lies past maxBlocks
   const int32_t g_new = c > 0 && c % kRatio == 0 ? c / kRatio - 1 : -1;
   const bool owner = g_new >= 0 && min(g_new / per_cta, static_cast<int32_t>(gridDim.y) - 1) == y;
-  // tiles copied before the CTA barrier: in the owning CTA, none from g_new's tile on
-  // (its V-tail is written below)
-  const int pre_limit = owner && g_new < g_end ? (g_new - g_begin) / dtc::kTile : dtc::kStages;
+  // The owning CTA scores g_new itself when g_new < g_end.  If g_new's tile is one of the
+  // first kStages (copied before the CTA barrier, with g_new's stale V-tail row), the
+  // compressed row is written into that tile's A stage once the copy has landed; a later
+  // tile is copied after the V-tail is written and fenced, and reads it from L2.
+  const int t_patch = owner && g_new < g_end ? (g_new - g_begin) / dtc::kTile : dtc::kStages;
+  const bool patch = t_patch < dtc::kStages;
+  constexpr int pre_limit = dtc::kStages;
   const uint16_t* row = index_qk + static_cast<int64_t>(b) * kRowWidth;
   QHeadsIn qin{};
   CompressIn cin{};
@@ -120,7 +124,9 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
         st_v4(cin.vtail + ca, oa);
         st_v4(cin.vtail + cb, ob);
       }
-      ptx::fence_proxy_async_global();  // the V-tail, before this CTA's TMA copies read it
+      ptx::fence_proxy_async_global();  // the V-tail, before a TMA copy issued later reads it
+      if (patch && cin.ok)  // warp-uniform
+        dtc::patch_a_row(en, t_patch, g_new - g_begin - dtc::kTile * t_patch, lane, ca, cb, oa, ob);
     }
   }
   ptx::fence_proxy_async_shared();  // the B operand, before the MMAs read it

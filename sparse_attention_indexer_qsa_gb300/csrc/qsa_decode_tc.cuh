@@ -181,6 +181,32 @@ __device__ __forceinline__ void engine_start(const Engine& en, const CUtensorMap
   for (int t = 0; t < np; ++t) issue_tile(en, map, pages, head_size, g_run, g_end, t, t);
 }
 
+// One warp, after the CTA barrier that follows engine_start, before engine_setup: once
+// the copies of tile t (one engine_start issued) have landed, lanes 0-7 overwrite the A
+// operand row of the tile's block rr (0 <= rr < kTile) with the 128 T values whose
+// chunks at element offsets ca and cb they hold (chunk_a / chunk_b of the lane), in the
+// 128-byte-swizzled layout the copies wrote, and fence them for the MMAs.  Returns false
+// if the wait ran out (the abort flag is then set).
+__device__ __forceinline__ bool patch_a_row(const Engine& en, int t, int rr, int lane, int ca, int cb, uint4 va,
+                                            uint4 vb) {
+  const int s = t % kStages;
+  if (!wait_bounded(en, en.bar(kBarFull + s), (t / kStages) & 1, kFaultEpilogue)) return false;
+  if (lane < 8) {
+    const int r = rr & 31;  // row of the 32-row page box, which starts 1024-byte aligned
+    const uint32_t box = kOffA + static_cast<uint32_t>(s) * kABytes + static_cast<uint32_t>(rr >> 5) * kPageBox +
+                         static_cast<uint32_t>(r) * 128u;
+    const int e2[2] = {ca, cb};
+    const uint4 v2[2] = {va, vb};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t half = static_cast<uint32_t>(e2[k] >> 6), c = static_cast<uint32_t>((e2[k] & 63) >> 3);
+      *reinterpret_cast<uint4*>(en.ptr + box + half * kAHalf + ((c ^ static_cast<uint32_t>(r & 7)) << 4)) = v2[k];
+    }
+  }
+  ptx::fence_proxy_async_shared();
+  return true;
+}
+
 // TMEM; every thread of the CTA calls it after engine_start (contains __syncthreads).
 // The caller has written the B operand (and fenced it for the async proxy) before.
 __device__ __forceinline__ uint32_t engine_setup(const Engine& en) {
