@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(kScoresThreads, kScoresCtasPerSm)
   if (warp == 0) {
     // the page entries of the whole run (their loads need not wait for the context
     // length), then the first tiles' copies, before the CTA barrier
+    if (tid == 0) ptx::prefetch_tensormap(&pool_map);  // its fetch overlaps the page-table loads
     stage_vpages(vpages, pool, b, g_begin, min(g_begin + run, max_blocks), tid, 32);
     __syncwarp();
     if (g_begin < n_vis) dtc::engine_start(en, &pool_map, vpages, pool.head_size, g_begin, g_end, dtc::kStages);

@@ -87,6 +87,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap pool_map, int32_t* __rest
   QHeadsIn qin{};
   CompressIn cin{};
   if (warp == 0) {
+    if (lane == 0) ptx::prefetch_tensormap(&pool_map);  // its fetch overlaps the page-table loads
     stage_vpages(vpages, pool, b, g_begin, min(g_begin + per_cta, max_blocks), tid, 32);
     __syncwarp();
     dtc::engine_start(en, &pool_map, vpages, pool.head_size, g_begin, g_end, pre_limit);
