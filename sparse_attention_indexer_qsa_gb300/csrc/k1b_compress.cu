@@ -14,15 +14,20 @@
 
 namespace qsa {
 
+// 128-thread CTAs, 6 an SM: small launches spread over more SMs than with 256-thread
+// CTAs (2048 blocks: 128 CTAs instead of 64)
+#ifndef QSA_K1B_THREADS
+#define QSA_K1B_THREADS 128
+#endif
 #ifndef QSA_K1B_MINB
-#define QSA_K1B_MINB 3
+#define QSA_K1B_MINB (768 / QSA_K1B_THREADS)
 #endif
 
 // PAGED (launchQsaIndexKCompressPaged): additionally copy every VALID block's kbar
 // row to the pool V-tail of token 4g when that page slot is usable; the dense
 // output is the same code path, so it is bit-identical to the unpaged kernel.
 template <class T, bool PAGED>
-__global__ void __launch_bounds__(256, QSA_K1B_MINB)
+__global__ void __launch_bounds__(QSA_K1B_THREADS, QSA_K1B_MINB)
 k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ index_qk,
                     const float* __restrict__ cos_sin, const int32_t* __restrict__ context_lengths,
                     const uint16_t* __restrict__ w_k, float eps, int32_t batch, int32_t seq_len,
@@ -103,7 +108,7 @@ k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ in
 }
 
 namespace {
-constexpr int kK1bThreads = 256;
+constexpr int kK1bThreads = QSA_K1B_THREADS;
 
 template <class T, bool PAGED>
 cudaError_t launch_t(const LaunchKCompress& a, const PoolDev& pool) {
