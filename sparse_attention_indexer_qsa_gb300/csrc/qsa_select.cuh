@@ -286,7 +286,7 @@ __device__ __forceinline__ void for_each_key(const K& keys, int32_t n, F&& f) {
 // candidate resolution read no key from memory again.
 template <int T, int MW, bool kRegs = false, class K>
 __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShared<T>& sh,
-                                           uint32_t* ghist = nullptr) {
+                                           uint32_t* ghist = nullptr, uint8_t* codes = nullptr) {
   static_assert(!kRegs || MW == 1, "keys in registers: one 32-key word a thread");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t k_sel = kTopK;
@@ -341,6 +341,29 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
 #pragma unroll
       for (int e = 0; e < 32; ++e)
         if (g0 + e < n_vis) atomicAdd(&sh.hist1[digit1(kr[e])], 1u);
+    } else if (codes != nullptr) {
+      // codes (n_vis <= 32 * T * MW bytes, 4-byte aligned): each key's first digit >> 2,
+      // so that the ordered pass reads one byte a key instead of the row
+      int32_t g = tid;
+      if (keys.vec) {
+        const int32_t nv = n_vis >> 2;
+        for (int32_t v = tid; v < nv; v += T) {
+          const float4 x = keys.ld4(4 * v);
+          const uint32_t d0 = digit1(orderable(x.x)), d1 = digit1(orderable(x.y));
+          const uint32_t d2 = digit1(orderable(x.z)), d3 = digit1(orderable(x.w));
+          atomicAdd(&sh.hist1[d0], 1u);
+          atomicAdd(&sh.hist1[d1], 1u);
+          atomicAdd(&sh.hist1[d2], 1u);
+          atomicAdd(&sh.hist1[d3], 1u);
+          reinterpret_cast<uint32_t*>(codes)[v] = (d0 >> 2) | ((d1 >> 2) << 8) | ((d2 >> 2) << 16) | ((d3 >> 2) << 24);
+        }
+        g = 4 * nv + tid;
+      }
+      for (; g < n_vis; g += T) {
+        const uint32_t d = digit1(orderable(keys.ld1(g)));
+        atomicAdd(&sh.hist1[d], 1u);
+        codes[g] = static_cast<uint8_t>(d >> 2);
+      }
     } else {
       for_each_key<T>(keys, n_vis, [&](uint32_t key) { atomicAdd(&sh.hist1[digit1(key)], 1u); });
     }
@@ -388,6 +411,51 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
       const uint32_t valid = nk >= 32 ? 0xFFFFFFFFu : (nk > 0 ? (1u << nk) - 1u : 0u);
       gtm[w] = gt & valid;
       cm[w] = in & valid;
+    } else if (codes != nullptr) {
+      // keys whose code is above b1's are selected, below it out; the few that share b1's
+      // code (four first-digit bins) are compared exactly, their keys reloaded
+      const uint32_t cb = b1 >> 2;
+      const int32_t nk = n_vis - gb;
+      const uint32_t valid = nk >= 32 ? 0xFFFFFFFFu : (nk > 0 ? (1u << nk) - 1u : 0u);
+      uint32_t gt = 0u, amb = 0u;
+      const uint4* c16 = reinterpret_cast<const uint4*>(codes + gb);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 c = c16[h];
+        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t code = (cw[q] >> (8 * j)) & 0xFFu;
+            gt |= static_cast<uint32_t>(code > cb) << (16 * h + 4 * q + j);
+            amb |= static_cast<uint32_t>(code == cb) << (16 * h + 4 * q + j);
+          }
+        }
+      }
+      gt &= valid;
+      amb &= valid;
+      uint32_t in = 0u;
+      while (amb != 0u) {  // up to four reloads in flight
+        int e4[4];
+        float x4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          e4[u] = amb != 0u ? __ffs(amb) - 1 : -1;
+          amb &= amb - 1u;
+          x4[u] = e4[u] >= 0 ? keys.ld1(gb + e4[u]) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (e4[u] >= 0) {
+            const uint32_t key = orderable(x4[u]);
+            gt |= static_cast<uint32_t>(key > hi1) << e4[u];
+            in |= static_cast<uint32_t>(key - lo1 <= span1) << e4[u];
+          }
+        }
+      }
+      gtm[w] = gt;
+      cm[w] = in;
     } else if (keys.vec && gb + 32 <= n_vis) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
