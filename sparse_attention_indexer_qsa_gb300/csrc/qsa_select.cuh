@@ -492,6 +492,15 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
 #pragma unroll
         for (int e = 0; e < 32; ++e)
           if ((cm[0] >> e) & 1u) sh.hist1[j++] = kr[e];
+      } else if (codes != nullptr) {  // the keys themselves, reloaded (L1 since the ordered pass)
+#pragma unroll
+        for (int w = 0; w < MW; ++w) {
+          uint32_t m = cm[w];
+          while (m) {
+            sh.hist1[j++] = orderable(keys.ld1(g0 + 32 * w + __ffs(m) - 1));
+            m &= m - 1u;
+          }
+        }
       } else {  // block ids; warp 0 loads their keys
 #pragma unroll
         for (int w = 0; w < MW; ++w) {
@@ -511,7 +520,7 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
     if (warp == 0) {
       const uint32_t nc = c1;
       const int nq = static_cast<int>((nc + 31u) >> 5);
-      if constexpr (!kRegs) {
+      if (!kRegs && codes == nullptr) {
         // candidates' keys, in place of their block ids: kGather loads in flight a lane
         // before their stores, so the L2 round trips overlap
         for (int q0 = 0; q0 < nq; q0 += kGather) {
