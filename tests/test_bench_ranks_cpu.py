@@ -11,6 +11,7 @@ import socket
 import sys
 from contextlib import redirect_stdout
 
+import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
@@ -209,7 +210,16 @@ def test_single_rank_helpers_need_no_process_group():
 
 def test_k2_traffic_profile_matches_the_kernel_source():
     """The bench line's roofline traffic comes from the committed K2 ncu summary, which
-    records the hash of the K2 source it was captured on: the two must still agree."""
+    records the hash of the K2 source it was captured on: the two must still agree, the
+    figure reported must be the one recorded, and it must be close to K2's algorithmic bytes
+    at B=8 (a little below them: the last logits are still dirty in L2 when the kernel ends)."""
     sys.path.insert(0, ROOT)
+    import re
     import bench
-    assert bench.k2_profiled_traffic(8) == 2168935424
+    got = bench.k2_profiled_traffic(8)
+    assert got is not None, "the K2 ncu summary was captured on another K2 source: recapture it"
+    with open(os.path.join(ROOT, "profiles", "k2_scores_tc_B4_S16384.md")) as f:
+        want = int(re.search(r"traffic_bytes_per_launch_B8: (\d+)", f.read()).group(1))
+    assert got == want
+    alg = bench.algorithmic_bytes(np.full(8, 16384, np.int32), 8, 16384, 4096)["k2"]
+    assert 0.9 * alg <= got <= 1.05 * alg
