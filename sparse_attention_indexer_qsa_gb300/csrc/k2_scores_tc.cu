@@ -324,6 +324,29 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The producer takes its first unit and prefetches that unit's q tile and first kbar
+  // tiles into L2, so the copies after the wait find them there.  A prefetch reads nothing
+  // into this CTA, and L2 keeps later writes of the previous kernel current, so it may run
+  // before the wait; it needs no context length.
+  uint32_t u_first = 0u;
+  if (warp == 0 && lane == 0) {
+    u_first = atomicAdd(p.sched, 1u);
+    if (u_first < static_cast<uint32_t>(p.units)) {
+      const int32_t tq = static_cast<int32_t>(u_first) / p.n_groups;
+      const int32_t grp = static_cast<int32_t>(u_first) - tq * p.n_groups;
+      const int32_t tile = p.tile_lo + tq;
+      const int32_t b = tile / p.tiles_per_batch;
+      const int32_t t0 = (tile - b * p.tiles_per_batch) * kTokTile;
+      ptx::tma_prefetch_3d(&tmap_q, 0, 4 * t0, b);
+      ptx::tma_prefetch_3d(&tmap_q, 64, 4 * t0, b);
+      const int32_t n_tiles = (p.n_gtiles - grp + p.n_groups - 1) / p.n_groups;
+      for (int i = 0; i < n_tiles && i < kKStages; ++i) {
+        const int32_t gt = grp + p.n_groups * i;
+        ptx::tma_prefetch_3d(&tmap_k, 0, gt * kGTile, b);
+        ptx::tma_prefetch_3d(&tmap_k, 64, gt * kGTile, b);
+      }
+    }
+  }
   // Everything above overlaps the previous kernel's tail when this launch is a
   // programmatic dependent; nothing below may read its inputs (q, kbar, ctx) or
   // overwrite the logits buffer before that kernel has completed.
@@ -335,8 +358,10 @@ k2_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       // Work units are taken in increasing order (increasing logits address) from a
       // device-wide counter, so the CTAs' write fronts advance together.
       int qcnt = 0, kcnt = 0, scnt = 0;
+      bool first = true;
       while (true) {
-        const uint32_t u = atomicAdd(p.sched, 1u);
+        const uint32_t u = first ? u_first : atomicAdd(p.sched, 1u);
+        first = false;
         Unit x;
         if (u < static_cast<uint32_t>(p.units)) {
           x = unit_info(p, static_cast<int32_t>(u));
