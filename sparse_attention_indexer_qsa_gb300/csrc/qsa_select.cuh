@@ -69,12 +69,17 @@ constexpr uint32_t kFineBins = (kFineHi - kFineLo) << (23 - kFineShift);
 static_assert(kFineLo + kFineBins + (511u - kFineHi) < static_cast<uint32_t>(kBins1) || !QSA_SEL_FINE_DIGIT,
               "the fine first digit does not fit the bins");
 
+// The three pieces (e below kFineLo, the fine bins, e - kFineHi + kFineLo + kFineBins from
+// kFineHi on) as min(max(e, fine), high): below kFineLo the fine term is the smaller (it
+// falls 2^(23 - kFineShift) a step of e, e by one), inside the fine range it is the larger,
+// and from kFineHi on the high term is below it.  Six integer operations, no selects.
 __device__ __forceinline__ uint32_t digit1(uint32_t key) {
 #if QSA_SEL_FINE_DIGIT
-  const uint32_t e = key >> 23;
-  const uint32_t fine = (key >> kFineShift) - (kFineLo << (23 - kFineShift)) + kFineLo;
-  const uint32_t high = e - kFineHi + kFineLo + kFineBins;
-  return e < kFineLo ? e : (e < kFineHi ? fine : high);
+  const int32_t e = static_cast<int32_t>(key >> 23);
+  const int32_t fine = static_cast<int32_t>(key >> kFineShift) -
+                       static_cast<int32_t>((kFineLo << (23 - kFineShift)) - kFineLo);
+  const int32_t high = e - static_cast<int32_t>(kFineHi - kFineLo - kFineBins);
+  return static_cast<uint32_t>(min(max(e, fine), high));
 #else
   return key >> kShift1;
 #endif
