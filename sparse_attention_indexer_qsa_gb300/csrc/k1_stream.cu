@@ -34,7 +34,7 @@ constexpr int kModeQK = 3;  // the one mode built: q heads and compressed k toge
 #define QSA_K1S_ROWS 16
 #endif
 #ifndef QSA_K1S_CTAS
-#define QSA_K1S_CTAS 6
+#define QSA_K1S_CTAS 7
 #endif
 constexpr int kRows = QSA_K1S_ROWS;       // token rows per unit (one CTA)
 constexpr int kWarps = 4;
