@@ -377,7 +377,9 @@ int qsa_topk_expand_decode(int32_t* outIdx, const float* logits, const int32_t* 
  * CTAs); the CTA that completes a sequence last runs its selection, so no CTA waits
  * for another.  For batches of up to 64 sequences, the scoring CTAs also count every
  * logit they write into the row's first-digit histogram of the selection, which the
- * last CTA copies instead of counting the row again (and leaves zeroed).  Sequences
+ * last CTA copies instead of counting the row again (and leaves zeroed); if the copied
+ * counts do not total the row's visible blocks (as after a launch whose waits ran out),
+ * that CTA counts the row itself.  Sequences
  * report completion through a device-side set of counters (and of histograms), one of
  * 16 taken in turn by each launch: at most 16 launches may be in flight on one device
  * at a time, and a CUDA graph that captured a launch keeps its set on every replay, so

@@ -53,6 +53,18 @@ int qsa_testing_bounded_wait_probe(int32_t timeoutMs, qsa_stream_t stream);
 int qsa_testing_stream_yardstick(void* dst, const void* src, int64_t units, int32_t rows, int64_t rowPitch,
                                  int64_t unitPitch, int64_t offset, int32_t bytes, qsa_stream_t stream);
 
+/*
+ * The one-launch decode step (qsa_indexer_decode_step) keeps, for batches of up to 64
+ * sequences, a first-digit histogram per sequence that its scoring CTAs fill and its
+ * selection copies and leaves zeroed.  The selection checks that the copied counts total
+ * the row's visible blocks and counts the row itself when they do not (as after a launch
+ * whose waits ran out).  This entry adds `add` (> 0) to bin 0 of every such histogram,
+ * in every one of the 16 launch slots, so that the next launches exercise that check; add
+ * = 0 zeroes them all again.  Enqueued on `stream`.
+ * Errors: QSA_E_RANGE (add < 0), QSA_E_CUDA.
+ */
+int qsa_testing_decode_step_histograms(int32_t add, qsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

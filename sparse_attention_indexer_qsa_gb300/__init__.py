@@ -24,7 +24,7 @@ __all__ = [
     "qsa_indexer_pre_decode", "qsa_index_scores_decode", "qsa_topk_expand_decode",
     "qsa_indexer_decode_step", "qsa_device_fault_flags",
     "qsa_testing_index_scores_cuda_core", "qsa_testing_bounded_wait_probe", "qsa_testing_stream_yardstick",
-    "LIB_PATH",
+    "qsa_testing_decode_step_histograms", "LIB_PATH",
 ]
 
 QSA_BF16 = 0
@@ -36,7 +36,8 @@ EXPORTED = ["qsa_abi_version", "qsa_last_error", "qsa_index_q_prep", "qsa_index_
             "qsa_index_scores_topk_expand", "qsa_index_k_compress_paged", "qsa_raw_k_tail_write_prefill", "qsa_indexer_pre_decode",
             "qsa_index_scores_decode", "qsa_topk_expand_decode", "qsa_indexer_decode_step",
             "qsa_index_scores", "qsa_index_scores_no_alloc", "qsa_device_fault_flags",
-            "qsa_testing_index_scores_cuda_core", "qsa_testing_bounded_wait_probe", "qsa_testing_stream_yardstick"]
+            "qsa_testing_index_scores_cuda_core", "qsa_testing_bounded_wait_probe", "qsa_testing_stream_yardstick",
+            "qsa_testing_decode_step_histograms"]
 
 
 class QsaError(RuntimeError):
@@ -116,6 +117,8 @@ def load():
     L.qsa_testing_index_scores_cuda_core.restype = ctypes.c_int
     L.qsa_testing_bounded_wait_probe.argtypes = [i32, p]
     L.qsa_testing_bounded_wait_probe.restype = ctypes.c_int
+    L.qsa_testing_decode_step_histograms.argtypes = [i32, p]
+    L.qsa_testing_decode_step_histograms.restype = ctypes.c_int
     i64 = ctypes.c_int64
     L.qsa_testing_stream_yardstick.argtypes = [p, p, i64, i32, i64, i64, i64, i32, p]
     L.qsa_testing_stream_yardstick.restype = ctypes.c_int
@@ -313,6 +316,12 @@ def qsa_testing_bounded_wait_probe(timeoutMs, stream=None):
     """A bounded wait that runs out on purpose (include/qsa_indexer_testing.h): sets a
     device fault bit after timeoutMs, faults nothing."""
     _check(load().qsa_testing_bounded_wait_probe(int(timeoutMs), _stream(stream)))
+
+
+def qsa_testing_decode_step_histograms(add, stream=None):
+    """Offset (add > 0) or zero (add = 0) the one-launch decode step's first-digit
+    histograms (include/qsa_indexer_testing.h), to exercise its count check."""
+    _check(load().qsa_testing_decode_step_histograms(int(add), _stream(stream)))
 
 
 def qsa_testing_stream_yardstick(dst, src, units, rows, rowPitch, unitPitch, offset, nbytes, stream=None):

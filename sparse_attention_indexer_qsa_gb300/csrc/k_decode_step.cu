@@ -247,6 +247,25 @@ cudaError_t launch_decode_step(bool bf16, int32_t* out_idx, float* logits, void*
   return cudaGetLastError();
 }
 
+namespace dec {
+// bin 0 of each of n histograms (kBins1 words apart) += add
+__global__ void hist_offset_kernel(uint32_t* __restrict__ hist, int32_t n, uint32_t add) {
+  const int32_t i = static_cast<int32_t>(blockIdx.x * blockDim.x + threadIdx.x);
+  if (i < n) hist[static_cast<int64_t>(i) * sel::kBins1] += add;
+}
+}  // namespace dec
+
+cudaError_t testing_decode_step_histograms(int32_t add, cudaStream_t stream) {
+  void* ptr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_decode_step_hist);
+  if (e != cudaSuccess) return e;
+  if (add == 0) return cudaMemsetAsync(ptr, 0, sizeof(g_decode_step_hist), stream);
+  constexpr int32_t n = kStepSlots * kHistBatch;
+  dec::hist_offset_kernel<<<(n + 255) / 256, 256, 0, stream>>>(static_cast<uint32_t*>(ptr), n,
+                                                              static_cast<uint32_t>(add));
+  return cudaGetLastError();
+}
+
 cudaError_t read_step_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream) {
   cudaError_t e = cudaMemcpyFromSymbolAsync(flags, g_step_fault_flags, sizeof(uint32_t), 0,
                                             cudaMemcpyDeviceToHost, stream);

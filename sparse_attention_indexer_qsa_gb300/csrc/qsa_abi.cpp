@@ -519,6 +519,15 @@ QSA_API int qsa_testing_stream_yardstick(void* dst, const void* src, int64_t uni
                                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+QSA_API int qsa_testing_decode_step_histograms(int32_t add, qsa_stream_t stream) {
+  static const char* fn = "qsa_testing_decode_step_histograms";
+  if (add < 0) return fail(QSA_E_RANGE, "%s: add must be >= 0", fn);
+  DeviceInfo d;
+  int st = current_device(fn, &d);
+  if (st != QSA_OK) return st;
+  return launched(fn, qsa::testing_decode_step_histograms(add, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 QSA_API int qsa_device_fault_flags(uint32_t* flags, int clear, qsa_stream_t stream) {
   static const char* fn = "qsa_device_fault_flags";
   if (!flags) return fail(QSA_E_NULL, "%s: null flags pointer", fn);

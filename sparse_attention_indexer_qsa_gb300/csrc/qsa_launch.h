@@ -155,6 +155,9 @@ cudaError_t read_dec_fault_flags(uint32_t* flags, bool clear, cudaStream_t strea
 // Test-only: one warp's bounded wait on an mbarrier nothing arrives on (k_decode.cu).
 cudaError_t launch_bounded_wait_probe(uint64_t limit_ns, cudaStream_t stream);
 cudaError_t read_step_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
+// Testing: add `add` to bin 0 of every first-digit histogram of the one-launch decode
+// step (every slot, every sequence), or zero them all when add == 0.
+cudaError_t testing_decode_step_histograms(int32_t add, cudaStream_t stream);
 cudaError_t read_fused_fault_flags(uint32_t* flags, bool clear, cudaStream_t stream);
 
 cudaError_t launch_scores_topk_fused(const LaunchScoresTopk& a);

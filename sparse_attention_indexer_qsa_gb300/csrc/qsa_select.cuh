@@ -126,6 +126,7 @@ struct SelShared {
   uint32_t warp_tot[T / 32];
   uint32_t thr_bin, thr_above, thr_count, ncand;
   int32_t rem;
+  uint32_t recount;  // given first-digit counts that do not total the row's keys
   __device__ __forceinline__ uint32_t* hist2() { return hist1 + kHist2Word; }
   __device__ __forceinline__ uint8_t* cls() { return reinterpret_cast<uint8_t*>(hist1 + kClsWord); }
   __device__ __forceinline__ int32_t* win() { return reinterpret_cast<int32_t*>(hist1); }
@@ -210,16 +211,20 @@ __device__ __forceinline__ Threshold walk_and_share(const uint32_t (&bins)[NB], 
 
 // One warp: walk the kBins1 bins from the highest down to where the running count
 // reaches k (1 <= k <= total).  128-bin super-bins are summed first (a 16-byte load
-// and a warp reduction each); the chosen one is searched 4 bins a lane.
-__device__ __forceinline__ Threshold find_first_digit(const uint32_t* hist, uint32_t k) {
+// and a warp reduction each); the chosen one is searched 4 bins a lane.  *total: the sum
+// of every bin.
+__device__ __forceinline__ Threshold find_first_digit(const uint32_t* hist, uint32_t k, uint32_t* total) {
   const int lane = threadIdx.x & 31;
   const uint4* h4 = reinterpret_cast<const uint4*>(hist);
   uint32_t ssum[kSuper];
+  uint32_t all = 0u;
 #pragma unroll
   for (int s = 0; s < kSuper; ++s) {
     const uint4 v = h4[s * 32 + lane];
     ssum[s] = __reduce_add_sync(0xffffffffu, v.x + v.y + v.z + v.w);
+    all += ssum[s];
   }
+  *total = all;
   uint32_t cum = 0;
   int sstar = 0;
   bool found = false;
@@ -341,7 +346,9 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
   }
   if (tid == 0) sh.ncand = 0;
   __syncthreads();
-  if (ghist == nullptr) {
+  // the row's own first-digit counts (when ghist gives none, or gives counts that do not
+  // total the row's keys: then the search below finds recount set, and the CTA counts here)
+  auto count_keys = [&]() {
     if constexpr (kRegs) {
 #pragma unroll
       for (int e = 0; e < 32; ++e)
@@ -372,17 +379,32 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
     } else {
       for_each_key<T>(keys, n_vis, [&](uint32_t key) { atomicAdd(&sh.hist1[digit1(key)], 1u); });
     }
+  };
+  auto search = [&]() {
+    if (warp == 0) {
+      uint32_t total;
+      const Threshold th = find_first_digit(sh.hist1, static_cast<uint32_t>(k_sel), &total);
+      if (lane == 0) {
+        sh.thr_bin = th.bin;
+        sh.thr_above = th.above;
+        sh.thr_count = th.count;
+        sh.recount = total != static_cast<uint32_t>(n_vis) ? 1u : 0u;
+      }
+    }
+    __syncthreads();
+  };
+  if (ghist == nullptr) {
+    count_keys();
     __syncthreads();
   }
-  if (warp == 0) {
-    const Threshold th = find_first_digit(sh.hist1, static_cast<uint32_t>(k_sel));
-    if (lane == 0) {
-      sh.thr_bin = th.bin;
-      sh.thr_above = th.above;
-      sh.thr_count = th.count;
-    }
+  search();
+  if (ghist != nullptr && sh.recount != 0u) {  // CTA-uniform
+    for (int k = tid; k < kBins1 / 4; k += T) reinterpret_cast<uint4*>(sh.hist1)[k] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    count_keys();
+    __syncthreads();
+    search();
   }
-  __syncthreads();
   const uint32_t b1 = sh.thr_bin;
   const uint32_t c1 = sh.thr_count;
   int32_t rem = k_sel - static_cast<int32_t>(sh.thr_above);

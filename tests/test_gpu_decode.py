@@ -521,6 +521,54 @@ def test_fused_decode_step_histogram_batch_edge(B):
     assert qsa.qsa_device_fault_flags() == 0
 
 
+def test_fused_decode_step_recounts_histograms_that_do_not_total_the_row():
+    """The one-launch step's selection checks that the first-digit counts it copies total
+    the row's visible blocks, and counts the row itself when they do not (as after a launch
+    whose waits ran out).  Every histogram offset by 7 in bin 0: two launches in a row still
+    equal the three separate calls bit for bit, and so does one after the reset."""
+    qsa = _qsa()
+    B, max_ctx = 8, 12000
+    pages = (max_ctx + 127) // 128
+    num_pages = B * pages
+    gen = torch.Generator(device="cuda").manual_seed(41)
+    pool0 = torch.randn((2 * num_pages, 128, 1, 128), device="cuda", generator=gen).to(torch.bfloat16)
+    perm = torch.randperm(num_pages, device="cuda", generator=gen).to(torch.int32).view(B, pages)
+    table = torch.stack([perm, perm + num_pages], dim=1).contiguous()
+    ctx = torch.randint(2100, max_ctx + 1, (B,), device="cuda", generator=gen, dtype=torch.int32)
+    rows = torch.randn((B, 640), device="cuda", generator=gen).to(torch.bfloat16)
+    cs = torch.randn((max_ctx, 64), device="cuda", generator=gen)
+    wq = (torch.randn(128, device="cuda", generator=gen) * 0.1).to(torch.bfloat16)
+    wk = (torch.randn(128, device="cuda", generator=gen) * 0.1).to(torch.bfloat16)
+    maxb = max_ctx // 4
+    pools = [pool0.clone(), pool0.clone()]
+    states = [qsa.pool_state(p_, table, num_pages, numKVHeads=1, poolHeadDim=128, headSize=0) for p_ in pools]
+
+    def bufs():
+        return dict(q=torch.empty((B, 1, 4, 128), dtype=torch.bfloat16, device="cuda"),
+                    logits=torch.full((B, maxb), float("nan"), device="cuda"),
+                    out=torch.empty((B, 2051), dtype=torch.int32, device="cuda"),
+                    split=torch.full((B, 2), 3, dtype=torch.int32, device="cuda"))
+    three, fused = bufs(), bufs()
+    qsa.qsa_indexer_pre_decode(three["q"], rows, cs, ctx, wq, wk, 1e-6, states[0], B)
+    qsa.qsa_index_scores_decode(three["logits"], three["q"], ctx, states[0], B, maxb)
+    qsa.qsa_topk_expand_decode(three["out"], three["logits"], ctx, three["split"], 2, B, maxb)
+    try:
+        qsa.qsa_testing_decode_step_histograms(7)
+        for n in range(3):
+            if n == 2:
+                qsa.qsa_testing_decode_step_histograms(0)
+            qsa.qsa_indexer_decode_step(fused["out"], fused["logits"], fused["q"], rows, cs, ctx, wq, wk, 1e-6,
+                                        states[1], fused["split"], 2, B, maxb)
+            torch.cuda.synchronize()
+            for name in ("q", "out", "split"):
+                assert torch.equal(three[name], fused[name]), (n, name)
+            assert torch.equal(pools[0], pools[1]), n
+    finally:
+        qsa.qsa_testing_decode_step_histograms(0)
+        torch.cuda.synchronize()
+    assert qsa.qsa_device_fault_flags() == 0
+
+
 def test_fused_decode_steps_in_flight_on_two_streams():
     """Launches of the one-launch step overlap on two streams (each launch takes its own
     arrival-counter set): 24 launches, alternating streams, on two independent problems,
