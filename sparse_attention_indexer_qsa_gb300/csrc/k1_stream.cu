@@ -29,7 +29,8 @@ __device__ uint32_t g_k1_fault_flags;
 
 namespace k1s {
 
-constexpr int kModeQK = 3;  // the one mode built: q heads and compressed k together
+constexpr int kModeQ = 1;   // q heads only (qsa_index_q_prep): each row's 1024-byte q part staged
+constexpr int kModeQK = 3;  // q heads and compressed k together (qsa_index_qk_prep): whole rows
 #ifndef QSA_K1S_ROWS
 #define QSA_K1S_ROWS 16
 #endif
@@ -45,8 +46,9 @@ constexpr uint32_t kCsBytes = kCsWidth * 4;  // 256-byte cos/sin row
 
 template <int MODE>
 struct Layout {
-  static_assert(MODE == kModeQK, "only the fused mode is built");
-  static constexpr uint32_t kRowBytes = kRowWidth * 2;  // whole 1280-byte indexQk rows
+  static_assert(MODE == kModeQK || MODE == kModeQ, "modes built: q, q and k");
+  // whole 1280-byte indexQk rows, or their 1024-byte q parts
+  static constexpr uint32_t kRowBytes = MODE == kModeQK ? kRowWidth * 2 : kNumQHeads * kHeadDim * 2;
   static constexpr uint32_t kRowsOff = 0;
   static constexpr uint32_t kCsOff = kRows * kRowBytes;
   static constexpr uint32_t kStageBytes = kCsOff + kRows * kCsBytes;
@@ -150,7 +152,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k1_stream_kernel(const P
     ptx::fence_barrier_init();
     ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nq) * (L::kRowBytes + kCsBytes));
     if (nq > 0) {
-      bulk_load(base + L::kRowsOff, p.index_qk + row0 * kRowWidth, nq * L::kRowBytes, bar);
+      if (MODE == kModeQK) {  // the unit's valid rows are contiguous: one copy
+        bulk_load(base + L::kRowsOff, p.index_qk + row0 * kRowWidth, nq * L::kRowBytes, bar);
+      } else {  // each row's q part (1280-byte pitch, 16-byte aligned)
+        for (int r = 0; r < nq; ++r)
+          bulk_load(base + L::kRowsOff + r * L::kRowBytes, p.index_qk + (row0 + r) * kRowWidth, L::kRowBytes, bar);
+      }
       bulk_load(base + L::kCsOff, p.cos_sin + static_cast<int64_t>(t0) * kCsWidth, nq * kCsBytes, bar);
     }
   }
@@ -265,6 +272,13 @@ k1s::Params make_params(void* q_normed, void* kbar, const void* index_qk, const 
 }
 
 }  // namespace
+
+cudaError_t launch_q_prep_staged(const LaunchQPrep& a) {
+  const k1s::Params p = make_params(a.q_normed, nullptr, a.index_qk, a.cos_sin, a.context_lengths, a.w_q,
+                                    nullptr, a.eps, a.batch, a.seq_len, 0);
+  return a.bf16 ? launch_mode<Bf16, k1s::kModeQ>(p, a.num_sms, a.stream)
+                : launch_mode<F16, k1s::kModeQ>(p, a.num_sms, a.stream);
+}
 
 cudaError_t launch_qk_prep(const LaunchQKPrep& a) {
   const k1s::Params p = make_params(a.q_normed, a.kbar, a.index_qk, a.cos_sin, a.context_lengths, a.w_q,

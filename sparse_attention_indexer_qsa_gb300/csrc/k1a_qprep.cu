@@ -3,9 +3,10 @@
 //
 // HBM-bound stream: a valid row reads its 1024-byte q part and writes 1024 bytes of
 // qNormed; a padding row (t >= contextLengths[b]) only writes 1024 zero bytes and
-// is never read.  One warp owns one row: 8-lane group h owns head h, each lane two
-// 16-byte chunks (its rope pairs stay in-lane, see qsa_common.cuh).  A persistent
-// grid-stride loop keeps ROWS rows of loads in flight per warp before any math.
+// is never read.  (Large launches go to the staged q mode of k1_stream.cu instead.)
+// One warp owns one row: 8-lane group h owns head h, each lane two 16-byte chunks
+// (its rope pairs stay in-lane, see qsa_common.cuh).  A persistent grid-stride loop
+// keeps ROWS rows of loads in flight per warp before any math.
 #include "qsa_common.cuh"
 #include "qsa_launch.h"
 
@@ -97,7 +98,17 @@ cudaError_t launch_t(const LaunchQPrep& a) {
 }
 }  // namespace
 
+// Launches of at least this many rows (batch x seqLen) run through the staged q mode of
+// k1_stream.cu (16-row units, each row's q part bulk-copied into shared memory): from 2^17
+// rows it streams faster (B=8, S=16384: 5.21 against 5.03 TB/s; 92 against 85 % of the
+// copy bandwidth at 2^22 rows), below it this kernel does (1x32768: 17.8 against 19.0 us).
+// Both give the same bits: the same norm_rope_group.
+#ifndef QSA_K1A_STAGED_MIN_ROWS
+#define QSA_K1A_STAGED_MIN_ROWS 131072
+#endif
+
 cudaError_t launch_q_prep(const LaunchQPrep& a) {
+  if (static_cast<int64_t>(a.batch) * a.seq_len >= QSA_K1A_STAGED_MIN_ROWS) return launch_q_prep_staged(a);
   return a.bf16 ? launch_t<Bf16>(a) : launch_t<F16>(a);
 }
 

@@ -107,6 +107,7 @@ struct LaunchScoresTopk {
 
 cudaError_t launch_q_prep(const LaunchQPrep& a);         // K1a (k1a_qprep.cu)
 cudaError_t launch_qk_prep(const LaunchQKPrep& a);       // fused K1a + prefill K1b (k1_stream.cu)
+cudaError_t launch_q_prep_staged(const LaunchQPrep& a);  // K1a through k1_stream.cu's staged q mode
 cudaError_t launch_k_compress(const LaunchKCompress& a);
 cudaError_t launch_scores_tc(const LaunchScores& a);
 cudaError_t launch_scores_cc(const LaunchScores& a);  // CUDA-core cross-check (testing only)
