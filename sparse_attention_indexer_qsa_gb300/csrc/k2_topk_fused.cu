@@ -566,6 +566,9 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           const uint32_t my_sel_gt = my.mode == kTakeAll ? my.lo - 1u : my.hi;
           // (a take-all row has lo > 0: all keys >= 0 taken would mean nVis = 512)
           const uint32_t my_in_lo = my.lo;
+          // the final pass's bin test starts at key 1: key 0 (a NaN pattern, never a visible
+          // logit's) marks the blocks a token does not see
+          const uint32_t my_in_lo1 = max(my.lo, 1u);
           for (int i = 0; i < x.n_gt; ++i) {
             const int as = acnt % kAccStages;
             if (!wait_bounded(bar(kBarAccFull + as), (acnt / kAccStages) & 1, abort_flag, kFaultEpilogue)) {
@@ -596,19 +599,22 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     // tokens) and, per lane, which tokens hold a key of their threshold bin
                     uint32_t wsel = 0u, cbits = 0u, key8[8];
 #pragma unroll
-                    for (int k = 0; k < 8; k += 2) {
-                      keys2(r, k, sc2, key8[k], key8[k + 1]);
+                    for (int k = 0; k < 8; k += 2) keys2(r, k, sc2, key8[k], key8[k + 1]);
+                    // on a diagonal g-tile, a block a token does not see gets key 0: never above a
+                    // threshold, never inside a bin (the test starts at key 1)
+                    if (!__all_sync(0xffffffffu, dvc <= 0)) {
 #pragma unroll
-                      for (int h = 0; h < 2; ++h) {
-                        const int j = 8 * c + k + h;       // token of this warp's slice
-                        const uint32_t key = key8[k + h];
-                        const uint32_t sel_gt = __shfl_sync(0xffffffffu, my_sel_gt, j);
-                        const uint32_t in_lo = __shfl_sync(0xffffffffu, my_in_lo, j);
-                        const bool vis = dvc <= k + h;
-                        const uint32_t ws = __ballot_sync(0xffffffffu, vis && key > sel_gt);
-                        wsel = lane == k + h ? ws : wsel;
-                        cbits |= (vis && key >= in_lo && key <= sel_gt) ? 1u << (k + h) : 0u;
-                      }
+                      for (int k = 0; k < 8; ++k) key8[k] = dvc <= k ? key8[k] : 0u;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                      const int j = 8 * c + k;       // token of this warp's slice
+                      const uint32_t key = key8[k];
+                      const uint32_t sel_gt = __shfl_sync(0xffffffffu, my_sel_gt, j);
+                      const uint32_t in_lo = __shfl_sync(0xffffffffu, my_in_lo1, j);
+                      const uint32_t ws = __ballot_sync(0xffffffffu, key > sel_gt);
+                      wsel = lane == k ? ws : wsel;
+                      cbits |= (key >= in_lo && key <= sel_gt) ? 1u << k : 0u;
                     }
                     // a row that is not in its final pass never reads this word again
                     if (lane < 8) reg_a[(tok0 + 8 * c + lane) * kWords + wi] = wsel;
