@@ -640,6 +640,8 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                       }
                     }
                   } else if (lvl0_any != 0u) {
+                    // tokens of the group that count this lane's block: active rows that see it
+                    const uint32_t cm8 = a8 & (dvc <= 0 ? 0xFFu : (dvc > 7 ? 0u : (0xFFu << dvc) & 0xFFu));
 #pragma unroll
                     for (int k = 0; k < 8; k += 2) {
                       uint32_t key[2];
@@ -650,11 +652,12 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                         const uint32_t b = bin0_of(key[h], base0);
                         // every lane adds: a key the row does not count adds 0 (no divergence);
                         // rows outside this pass never read their histogram again
-                        const bool cnt = ((a8 >> (k + h)) & 1u) && dvc <= k + h;
+                        const bool cnt = (cm8 >> (k + h)) & 1u;
                         atomicAdd(&reg_a[(tok0 + j) * kWords + (b >> 1)], cnt ? 1u << ((b & 1u) << 4) : 0u);
                       }
                     }
                   } else {
+                    const uint32_t cm8 = a8 & (dvc <= 0 ? 0xFFu : (dvc > 7 ? 0u : (0xFFu << dvc) & 0xFFu));
 #pragma unroll
                     for (int k = 0; k < 8; k += 2) {
                       uint32_t key[2];
@@ -665,7 +668,7 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                         const uint32_t lo = __shfl_sync(0xffffffffu, my.lo, j);
                         const uint32_t hi = __shfl_sync(0xffffffffu, my.hi, j);
                         const uint32_t sh = __shfl_sync(0xffffffffu, my.shift, j);
-                        const bool cnt = ((a8 >> (k + h)) & 1u) && dvc <= k + h && key[h] >= lo && key[h] <= hi;
+                        const bool cnt = ((cm8 >> (k + h)) & 1u) && key[h] >= lo && key[h] <= hi;
                         const uint32_t b = cnt ? (key[h] - lo) >> sh : 0u;
                         atomicAdd(&reg_a[(tok0 + j) * kWords + (b >> 1)], cnt ? 1u << ((b & 1u) << 4) : 0u);
                       }
