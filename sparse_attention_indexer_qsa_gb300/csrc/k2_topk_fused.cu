@@ -113,7 +113,9 @@ constexpr uint32_t kOffA = kOffK + kKStages * kKBytes;          // per row: hist
 constexpr uint32_t kOffB = kOffA + kTokTile * kWords * 4;        // per row: candidates or tie mask
 constexpr uint32_t kOffStage = kOffB + kTokTile * kWords * 4;    // per epilogue warp: 512 winners (u16)
 constexpr uint32_t kOffRows = kOffStage + kEpiWarps * sel::kTopK * 2;
-constexpr uint32_t kOffBar = kOffRows + kTokTile * sizeof(RowState);
+constexpr uint32_t kOffThr = kOffRows + kTokTile * sizeof(RowState);  // per epilogue warp: its tokens'
+                                                                      // final-pass (sel_gt, in_lo) pairs
+constexpr uint32_t kOffBar = kOffThr + kEpiWarps * kTokPerWarp * 8;
 constexpr int kBarQFull = 0;
 constexpr int kBarQEmpty = 1;
 constexpr int kBarKFull = 2;
@@ -515,6 +517,7 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     const int etid = threadIdx.x - 64;
     const uint64_t sc2 = pack2(p.scale, p.scale);
     uint16_t* stage = reinterpret_cast<uint16_t*>(base_ptr + kOffStage) + ew * sel::kTopK;
+    uint2* thr_w = reinterpret_cast<uint2*>(base_ptr + kOffThr) + ew * kTokPerWarp;
     int acnt = 0, scnt = 0, dcnt = 0;
     bool ok = true;
     while (ok) {
@@ -569,6 +572,11 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           // the final pass's bin test starts at key 1: key 0 (a NaN pattern, never a visible
           // logit's) marks the blocks a token does not see
           const uint32_t my_in_lo1 = max(my.lo, 1u);
+          // the final pass reads each token's pair with one broadcast shared load
+          if (final_pass) {
+            if (mine) thr_w[lane] = make_uint2(my_sel_gt, my_in_lo1);
+            __syncwarp();
+          }
           for (int i = 0; i < x.n_gt; ++i) {
             const int as = acnt % kAccStages;
             if (!wait_bounded(bar(kBarAccFull + as), (acnt / kAccStages) & 1, abort_flag, kFaultEpilogue)) {
@@ -610,11 +618,10 @@ k2_topk_fused_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     for (int k = 0; k < 8; ++k) {
                       const int j = 8 * c + k;       // token of this warp's slice
                       const uint32_t key = key8[k];
-                      const uint32_t sel_gt = __shfl_sync(0xffffffffu, my_sel_gt, j);
-                      const uint32_t in_lo = __shfl_sync(0xffffffffu, my_in_lo1, j);
-                      const uint32_t ws = __ballot_sync(0xffffffffu, key > sel_gt);
+                      const uint2 th = thr_w[j];     // (sel_gt, in_lo) of token j
+                      const uint32_t ws = __ballot_sync(0xffffffffu, key > th.x);
                       wsel = lane == k ? ws : wsel;
-                      cbits |= (key >= in_lo && key <= sel_gt) ? 1u << k : 0u;
+                      cbits |= (key >= th.y && key <= th.x) ? 1u << k : 0u;
                     }
                     // a row that is not in its final pass never reads this word again
                     if (lane < 8) reg_a[(tok0 + 8 * c + lane) * kWords + wi] = wsel;
