@@ -3,15 +3,18 @@
 //
 // grid (B, Y), kDecThreads threads; CTA (b, y) covers the run of blocks [y * perCta,
 // (y + 1) * perCta), perCta chosen so that the grid is about one wave.  CTA (b, y):
-//   - warp 0 stages the run's page entries and issues the first tiles' TMA copies at
-//     once (in the CTA that compresses block g below, none from g's tile on);
+//   - warp 0 stages the run's page entries (for the whole run, without waiting for the
+//     context length) and issues the first tiles' TMA copies at once;
 //   - warp 2 computes sequence b's q heads straight into the tensor-core B operand
 //     (CTA y = 0 also writes qNormed[b]); warp 3 either writes the new token's raw
 //     K-tail (CTA y = 0), or, in the CTA whose run holds the just-completed block g
 //     (the last CTA if g lies past maxBlocks), compresses g (the pre-decode
-//     routines) into the pool's V-tail;
+//     routines) into the pool's V-tail.  Both issue their loads before the gamma
+//     barrier.  If g's tile is one of the first copied, its copy holds g's stale
+//     V-tail row, and warp 3 writes the compressed row into that A stage once the copy
+//     has landed; a later tile is copied after the V-tail store and reads it from L2;
 //   - the tensor-core paged-scores engine scores the run's blocks of the valid prefix
-//     (the owning CTA's TMA copies read block g's fresh V-tail) into logits[b];
+//     into logits[b];
 //   - the last CTA of sequence b to finish (a per-sequence arrival counter, no waiting)
 //     runs the top-512 selection of row b on the logits at L2, writes outIdx[b], zeroes
 //     b's split counters and puts the counter back to zero.  Its shared memory for the

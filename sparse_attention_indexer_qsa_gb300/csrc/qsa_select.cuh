@@ -23,12 +23,16 @@ __device__ __forceinline__ uint32_t orderable(float f) {
 // ---------------------------------------------------------------------------
 // topk: one CTA of T threads per row.
 //
-//  1. histogram of the first digit (digit1) over the visible blocks (coalesced); warp 0
-//     finds the bin b1 holding the kSel-th largest key, the count above it and c1,
-//     its own count;
+//  1. histogram of the first digit (digit1) over the visible blocks (coalesced; or the
+//     counts a caller's kernel made, checked to total the row); warp 0 finds the bin b1
+//     holding the kSel-th largest key, the count above it and c1, its own count.  For
+//     rows of at most 32*T*MW blocks the pass also stores each key's digit >> 2 as one
+//     byte in shared memory (the codes);
 //  2. one ordered pass: thread k owns the 32*MW contiguous blocks from 32*MW*k and
-//     records, as bit masks, which lie above b1 (selected) and in b1 (candidates);
-//     candidates' block ids are listed, each thread's in ascending order;
+//     records, as bit masks, which lie above b1 (selected) and in b1 (candidates), from
+//     the keys in registers, from the codes (reloading only the keys that share b1's
+//     code), or from the row; candidates are listed (their keys, or their block ids),
+//     each thread's in ascending order;
 //  3. unless b1 is filled exactly, the threshold key T inside b1, and how many keys
 //     equal to T are still to be taken, are resolved by 8-bit radix passes: over
 //     the listed candidates by warp 0 alone (up to kWarpCap of them), otherwise by
@@ -37,9 +41,9 @@ __device__ __forceinline__ uint32_t orderable(float f) {
 //     order; one block scan of packed (selected, tied) counts gives each thread the
 //     position of its first winner; winners are written in ascending order and the
 //     row is expanded.
-// Keys are read from global memory (L1/L2 after the first pass).  Small CTAs (64
-// threads, 4.1 KB of shared memory, 24 a SM) keep many rows in flight: the warp-0
-// steps between the passes are serial and would otherwise leave the SM idle.
+// Keys are read from global memory.  Small CTAs (64 threads, 8.2 KB of shared memory
+// with the codes, 24 a SM) keep many rows in flight: the warp-0 steps between the
+// passes are serial and would otherwise leave the SM idle.
 #ifndef QSA_SEL_D1_BITS
 #define QSA_SEL_D1_BITS 10
 #endif
