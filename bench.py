@@ -405,6 +405,33 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
             e1.synchronize()
             pts.append(e0.elapsed_time(e1))
         ms[name] = statistics.median(pts)
+    # the same-size yardstick of the paged scores: a plain gathering kernel reading the
+    # same V-tails (256 B each at the pool's 6 KB block pitch; the V pages are consecutive
+    # here) and writing 4 B a block, timed like the kernels above
+    if ctx_len % 128 == 0:
+        blk_pitch = 4 * 2 * 384 * 2
+        v_first = num_pages * 128 * 2 * 384 * 2 + 256 * 2
+        y_out = torch.empty(B * nvis, dtype=torch.int32, device="cuda")
+
+        def yard(st):
+            return lib.qsa_testing_gather_yardstick(y_out.data_ptr(), pool.data_ptr(), B * nvis, blk_pitch, v_first,
+                                                    256, st)
+
+        for _ in range(3):
+            if yard(sp) != 0:
+                raise RuntimeError(qsa.qsa_last_error())
+        yts = []
+        for _ in range(n):
+            l2_flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            yard(sp)
+            e1.record(stream)
+            e1.synchronize()
+            yts.append(e0.elapsed_time(e1))
+        ms["yardstick_scores_decode"] = statistics.mean(yts)
+        alg["yardstick_scores_decode"] = B * nvis * (256 + 4)
+        del y_out
     valid_blocks = B * ((ctx_len - 1) // 4)
     alg["k_compress_paged"] = valid_blocks * (1024 + 256 + 256) + ((ctx_len - 1) // 4) * 256
     alg["raw_k_tail_write_prefill"] = B * ((ctx_len - 1) % 4) * 512
@@ -412,6 +439,9 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
     hbm_peak, _, _ = load_peaks()
     kernels = {k: {"ms": ms[k], "alg_bytes": alg[k], "gbs": alg[k] / (ms[k] * 1e-3) / 1e9,
                    "frac_of_measured_hbm": alg[k] / (ms[k] * 1e-3) / 1e9 / hbm_peak} for k in ms}
+    if "yardstick_scores_decode" in kernels:
+        kernels["scores_decode"]["frac_of_yardstick"] = (kernels["scores_decode"]["gbs"] /
+                                                         kernels["yardstick_scores_decode"]["gbs"])
     del pool
     torch.cuda.empty_cache()
     return {"workload": f"decode step, B={B} sequences at ctx={ctx_len}, paged pool (128-token pages), bf16",
@@ -424,7 +454,9 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
                       "kernels: CUDA events "
                       "per kernel over eagerly launched steps, each after an L2 flush; k_compress_paged and "
                       "raw_k_tail_write_prefill: the prefill persistence of the same B sequences (ctx-1 tokens "
-                      "each) into the pool, one launch after an L2 flush, median")}
+                      "each) into the pool, one launch after an L2 flush, median; yardstick_scores_decode: "
+                      "qsa_testing_gather_yardstick reading the same V-tails and writing 4 B a block, timed "
+                      "like scores_decode")}
 
 
 def _graph_ms(torch, launches, reps: int = 10) -> float:

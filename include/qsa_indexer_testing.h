@@ -54,6 +54,25 @@ int qsa_testing_stream_yardstick(void* dst, const void* src, int64_t units, int3
                                  int64_t unitPitch, int64_t offset, int32_t bytes, qsa_stream_t stream);
 
 /*
+ * A plain gathering kernel for same-size bandwidth comparisons with the paged decode
+ * scoring (qsa_index_scores_decode, "Qsa Indexer Kernels": launchQsaIndexScoresDecode),
+ * which reads one 256-byte V-tail a block at the pool's block pitch and writes one FP32
+ * logit a block.  Unit u < units reads `bytes` bytes at
+ *   src + u*unitPitch + offset
+ * and writes the XOR of their 32-bit words (4 bytes) at dst + 4u; bytes/16
+ * consecutive threads share a unit, and each such group issues the 16-byte loads of
+ * 4 consecutive units before using any.  With unitPitch = 6144, bytes = 256 and src +
+ * offset the first V-tail of a pool whose V pages are consecutive, it reads what
+ * qsa_index_scores_decode reads for units valid blocks.  The caller owns both buffers:
+ * every read must lie in src's allocation.
+ * Limits: bytes a power of two in [16, 512]; src, unitPitch and offset 16-byte
+ * aligned, dst 4-byte aligned.
+ * Errors: QSA_E_NULL, QSA_E_SHAPE, QSA_E_ALIGN, QSA_E_CUDA.
+ */
+int qsa_testing_gather_yardstick(void* dst, const void* src, int64_t units, int64_t unitPitch, int64_t offset,
+                                 int32_t bytes, qsa_stream_t stream);
+
+/*
  * The one-launch decode step (qsa_indexer_decode_step) keeps, for batches of up to 64
  * sequences, a first-digit histogram per sequence that its scoring CTAs fill and its
  * selection copies and leaves zeroed.  The selection checks that the copied counts total

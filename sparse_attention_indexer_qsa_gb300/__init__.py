@@ -24,7 +24,7 @@ __all__ = [
     "qsa_indexer_pre_decode", "qsa_index_scores_decode", "qsa_topk_expand_decode",
     "qsa_indexer_decode_step", "qsa_device_fault_flags",
     "qsa_testing_index_scores_cuda_core", "qsa_testing_bounded_wait_probe", "qsa_testing_stream_yardstick",
-    "qsa_testing_decode_step_histograms", "LIB_PATH",
+    "qsa_testing_gather_yardstick", "qsa_testing_decode_step_histograms", "LIB_PATH",
 ]
 
 QSA_BF16 = 0
@@ -37,7 +37,7 @@ EXPORTED = ["qsa_abi_version", "qsa_last_error", "qsa_index_q_prep", "qsa_index_
             "qsa_index_scores_decode", "qsa_topk_expand_decode", "qsa_indexer_decode_step",
             "qsa_index_scores", "qsa_index_scores_no_alloc", "qsa_device_fault_flags",
             "qsa_testing_index_scores_cuda_core", "qsa_testing_bounded_wait_probe", "qsa_testing_stream_yardstick",
-            "qsa_testing_decode_step_histograms"]
+            "qsa_testing_gather_yardstick", "qsa_testing_decode_step_histograms"]
 
 
 class QsaError(RuntimeError):
@@ -122,6 +122,8 @@ def load():
     i64 = ctypes.c_int64
     L.qsa_testing_stream_yardstick.argtypes = [p, p, i64, i32, i64, i64, i64, i32, p]
     L.qsa_testing_stream_yardstick.restype = ctypes.c_int
+    L.qsa_testing_gather_yardstick.argtypes = [p, p, i64, i64, i64, i32, p]
+    L.qsa_testing_gather_yardstick.restype = ctypes.c_int
     L.qsa_device_fault_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, p]
     L.qsa_device_fault_flags.restype = ctypes.c_int
     _lib = L
@@ -328,6 +330,13 @@ def qsa_testing_stream_yardstick(dst, src, units, rows, rowPitch, unitPitch, off
     """A plain streaming kernel with a K1 kernel's byte pattern (include/qsa_indexer_testing.h)."""
     _check(load().qsa_testing_stream_yardstick(_addr(dst), _addr(src), int(units), int(rows), int(rowPitch),
                                             int(unitPitch), int(offset), int(nbytes), _stream(stream)))
+
+
+def qsa_testing_gather_yardstick(dst, src, units, unitPitch, offset, nbytes, stream=None):
+    """A plain gathering kernel with the paged decode scoring's byte pattern
+    (include/qsa_indexer_testing.h)."""
+    _check(load().qsa_testing_gather_yardstick(_addr(dst), _addr(src), int(units), int(unitPitch), int(offset),
+                                            int(nbytes), _stream(stream)))
 
 
 def qsa_testing_index_scores_cuda_core(logits, qNormed, kbar, contextLengths, batchSize, seqLen,

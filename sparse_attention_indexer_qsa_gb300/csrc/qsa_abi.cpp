@@ -519,6 +519,25 @@ QSA_API int qsa_testing_stream_yardstick(void* dst, const void* src, int64_t uni
                                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+QSA_API int qsa_testing_gather_yardstick(void* dst, const void* src, int64_t units, int64_t unitPitch, int64_t offset,
+                                         int32_t bytes, qsa_stream_t stream) {
+  static const char* fn = "qsa_testing_gather_yardstick";
+  if (!dst || !src) return fail(QSA_E_NULL, "%s: null pointer argument", fn);
+  if (units < 0 || bytes < 16 || bytes > 512 || (bytes & (bytes - 1)) != 0 || unitPitch < 0 || offset < 0)
+    return fail(QSA_E_SHAPE, "%s: need units >= 0, bytes a power of two in [16, 512]", fn);
+  if (!aligned(dst, 4) || !aligned(src, 16) || unitPitch % 16 != 0 || offset % 16 != 0)
+    return fail(QSA_E_ALIGN, "%s: src, unitPitch and offset must be 16-byte aligned, dst 4-byte", fn);
+  if (units == 0) {
+    g_last_error[0] = '\0';
+    return QSA_OK;
+  }
+  DeviceInfo d;
+  int st = current_device(fn, &d);
+  if (st != QSA_OK) return st;
+  return launched(fn, qsa::launch_gather_yardstick(dst, src, units, unitPitch, offset, bytes,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 QSA_API int qsa_testing_decode_step_histograms(int32_t add, qsa_stream_t stream) {
   static const char* fn = "qsa_testing_decode_step_histograms";
   if (add < 0) return fail(QSA_E_RANGE, "%s: add must be >= 0", fn);

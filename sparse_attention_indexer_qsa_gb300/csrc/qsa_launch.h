@@ -168,6 +168,10 @@ int32_t scores_topk_max_blocks();
 cudaError_t launch_stream_yardstick(void* dst, const void* src, int64_t units, int rows, int64_t row_pitch,
                                     int64_t unit_pitch, int64_t offset, int bytes, cudaStream_t stream);
 int yardstick_max_rows();
+// Test-only plain kernel with the paged decode scoring's byte pattern (yardstick.cu);
+// bytes a power of two in [16, 512].
+cudaError_t launch_gather_yardstick(void* dst, const void* src, int64_t units, int64_t unit_pitch, int64_t offset,
+                                    int bytes, cudaStream_t stream);
 
 // TMA map (a CUtensorMap, 64-byte aligned) over the pool's V-tails for the tensor-core
 // decode scoring (k_decode.cu).

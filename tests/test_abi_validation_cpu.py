@@ -113,6 +113,24 @@ def test_stream_yardstick(qsa):
     assert f(*ok()) == E_CUDA
 
 
+def test_gather_yardstick(qsa):
+    L = qsa.load()
+    ok = lambda **o: [o.get(k, v) for k, v in dict(dst=P, src=P, units=8, up=6144, off=512, nb=256,
+                                                    st=None).items()]
+    f = L.qsa_testing_gather_yardstick
+    assert f(*ok(dst=None)) == E_NULL
+    assert f(*ok(nb=8)) == E_SHAPE
+    assert f(*ok(nb=768)) == E_SHAPE  # a multiple of 16 but not a power of two
+    assert f(*ok(nb=1024)) == E_SHAPE
+    assert f(*ok(units=-1)) == E_SHAPE
+    assert f(*ok(off=8)) == E_ALIGN
+    assert f(*ok(up=6152)) == E_ALIGN
+    assert f(*ok(src=P + 8)) == E_ALIGN
+    assert f(*ok(dst=P + 2)) == E_ALIGN
+    assert f(*ok(units=0)) == 0
+    assert f(*ok()) == E_CUDA
+
+
 def test_pool_state_is_checked_by_every_paged_entry(qsa):
     L = qsa.load()
     calls = {
