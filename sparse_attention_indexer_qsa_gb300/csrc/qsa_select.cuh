@@ -358,8 +358,11 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
       for (int e = 0; e < 32; ++e)
         if (g0 + e < n_vis) atomicAdd(&sh.hist1[digit1(kr[e])], 1u);
     } else if (codes != nullptr) {
-      // codes (n_vis <= 32 * T * MW bytes, 4-byte aligned): each key's first digit >> 2,
-      // so that the ordered pass reads one byte a key instead of the row
+      // codes (n_vis <= 32 * T * MW bytes, 16-byte aligned): each key's first digit >> 2,
+      // so that the ordered pass reads one byte a key instead of the row.  Key l of a
+      // 32-key block has its code at byte l >> 3 of the block's word l & 7: the ordered
+      // pass compares a word's four codes at once, and one shift a word puts their flags
+      // at bits l of the block's masks
       int32_t g = tid;
       if (keys.vec) {
         const int32_t nv = n_vis >> 2;
@@ -371,14 +374,19 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
           atomicAdd(&sh.hist1[d1], 1u);
           atomicAdd(&sh.hist1[d2], 1u);
           atomicAdd(&sh.hist1[d3], 1u);
-          reinterpret_cast<uint32_t*>(codes)[v] = (d0 >> 2) | ((d1 >> 2) << 8) | ((d2 >> 2) << 16) | ((d3 >> 2) << 24);
+          // keys 4v + j: byte ((v & 7) >> 1) of word 4 (v & 1) + j of their 32-key block
+          uint8_t* cp = codes + 32 * (v >> 3) + 16 * (v & 1) + ((v & 7) >> 1);
+          cp[0] = static_cast<uint8_t>(d0 >> 2);
+          cp[4] = static_cast<uint8_t>(d1 >> 2);
+          cp[8] = static_cast<uint8_t>(d2 >> 2);
+          cp[12] = static_cast<uint8_t>(d3 >> 2);
         }
         g = 4 * nv + tid;
       }
       for (; g < n_vis; g += T) {
         const uint32_t d = digit1(orderable(keys.ld1(g)));
         atomicAdd(&sh.hist1[d], 1u);
-        codes[g] = static_cast<uint8_t>(d >> 2);
+        codes[32 * (g >> 5) + 4 * (g & 7) + ((g >> 3) & 3)] = static_cast<uint8_t>(d >> 2);
       }
     } else {
       for_each_key<T>(keys, n_vis, [&](uint32_t key) { atomicAdd(&sh.hist1[digit1(key)], 1u); });
@@ -444,24 +452,31 @@ __device__ __forceinline__ void select_row(const K& keys, int32_t n_vis, SelShar
       cm[w] = in & valid;
     } else if (codes != nullptr) {
       // keys whose code is above b1's are selected, below it out; the few that share b1's
-      // code (four first-digit bins) are compared exactly, their keys reloaded
+      // code (four first-digit bins) are compared exactly, their keys reloaded.  Four
+      // codes a word at once: x > cb is the carry out of each byte of x + (255 - cb)
+      // (bit 7 of the byte sum of the low seven bits, then the majority of the three
+      // bit-7 inputs), x == cb a zero byte of x ^ cb (exact: (t & 0x7F) + 0x7F sets bit 7
+      // unless t's low bits are zero); byte b's flag of word q lands at bit 8b + q
       const uint32_t cb = b1 >> 2;
       const int32_t nk = n_vis - gb;
       const uint32_t valid = nk >= 32 ? 0xFFFFFFFFu : (nk > 0 ? (1u << nk) - 1u : 0u);
       uint32_t gt = 0u, amb = 0u;
       const uint4* c16 = reinterpret_cast<const uint4*>(codes + gb);
+      const uint32_t c4 = cb * 0x01010101u, nc4 = ~c4, ncl = nc4 & 0x7F7F7F7Fu;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint4 c = c16[h];
         const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t code = (cw[q] >> (8 * j)) & 0xFFu;
-            gt |= static_cast<uint32_t>(code > cb) << (16 * h + 4 * q + j);
-            amb |= static_cast<uint32_t>(code == cb) << (16 * h + 4 * q + j);
-          }
+        for (int qq = 0; qq < 4; ++qq) {
+          const uint32_t x = cw[qq];
+          const uint32_t s = (x & 0x7F7F7F7Fu) + ncl;  // bit 7 of a byte: carry into bit 7 of x + ~cb
+          const uint32_t g = ((x & nc4) | (x & s) | (nc4 & s)) & 0x80808080u;  // carry out: x > cb
+          const uint32_t t = x ^ c4;
+          const uint32_t y = (t & 0x7F7F7F7Fu) + 0x7F7F7F7Fu;
+          const uint32_t e = ~(y | t) & 0x80808080u;  // t's zero bytes: x == cb
+          gt |= g >> (7 - (4 * h + qq));
+          amb |= e >> (7 - (4 * h + qq));
         }
       }
       gt &= valid;
