@@ -6,7 +6,8 @@
 // is never read.  (Large launches go to the staged q mode of k1_stream.cu instead.)
 // One warp owns one row: 8-lane group h owns head h, each lane two 16-byte chunks
 // (its rope pairs stay in-lane, see qsa_common.cuh).  A persistent grid-stride loop
-// keeps ROWS rows of loads in flight per warp before any math.
+// keeps ROWS rows of loads in flight per warp before any math; a launch that fits one
+// wave issues them before the CTA stages its gamma.
 #include "qsa_common.cuh"
 #include "qsa_launch.h"
 
@@ -19,7 +20,10 @@ namespace qsa {
 #define QSA_K1A_MINB 3
 #endif
 
-template <class T, int ROWS>
+// ONE_WAVE: the grid holds a warp for every ROWS rows, so each warp takes one group and
+// issues its loads before the CTA stages its gamma (the two round trips overlap); else a
+// persistent grid strides over the groups after the gamma stage.
+template <class T, int ROWS, bool ONE_WAVE>
 __global__ void __launch_bounds__(256, QSA_K1A_MINB)
 k1a_qprep_kernel(uint16_t* __restrict__ q_normed, const uint16_t* __restrict__ index_qk,
                  const float* __restrict__ cos_sin, const int32_t* __restrict__ context_lengths,
@@ -30,14 +34,17 @@ k1a_qprep_kernel(uint16_t* __restrict__ q_normed, const uint16_t* __restrict__ i
   const int ca = chunk_a(j);
   const int cb = chunk_b(j);
   __shared__ __align__(16) float g1[kHeadDim];
-  stage_gamma<T>(w_q, g1);
-  __syncthreads();
+  if constexpr (!ONE_WAVE) {
+    stage_gamma<T>(w_q, g1);
+    __syncthreads();
+  }
 
   const int32_t rows = batch * seq_len;
   const int32_t warp = static_cast<int32_t>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int32_t nwarps = static_cast<int32_t>((gridDim.x * blockDim.x) >> 5);
 
-  for (int32_t base = warp * ROWS; base < rows; base += nwarps * ROWS) {
+  for (int32_t base = warp * ROWS;; base += nwarps * ROWS) {
+    if (!ONE_WAVE && base >= rows) break;
     uint4 va[ROWS], vb[ROWS];
     RopeCS cs[ROWS] = {};
     bool valid[ROWS];
@@ -57,6 +64,10 @@ k1a_qprep_kernel(uint16_t* __restrict__ q_normed, const uint16_t* __restrict__ i
         }
       }
     }
+    if constexpr (ONE_WAVE) {  // every warp of the CTA gets here once
+      stage_gamma<T>(w_q, g1);
+      __syncthreads();
+    }
 #pragma unroll
     for (int k = 0; k < ROWS; ++k) {
       const int32_t row = base + k;
@@ -73,6 +84,7 @@ k1a_qprep_kernel(uint16_t* __restrict__ q_normed, const uint16_t* __restrict__ i
       st_v4(dst + ca, oa);
       st_v4(dst + cb, ob);
     }
+    if (ONE_WAVE) break;
   }
 }
 
@@ -82,15 +94,17 @@ constexpr int kK1aThreads = 256;
 
 template <class T>
 cudaError_t launch_t(const LaunchQPrep& a) {
-  auto kern = k1a_qprep_kernel<T, kK1aRows>;
   const int64_t rows = static_cast<int64_t>(a.batch) * a.seq_len;
   const int64_t warps_needed = (rows + kK1aRows - 1) / kK1aRows;
   const int64_t blocks_needed = (warps_needed * 32 + kK1aThreads - 1) / kK1aThreads;
   int per_sm = 0;
-  cudaError_t e = occupancy_blocks_per_sm(reinterpret_cast<const void*>(kern), kK1aThreads, 0, &per_sm);
+  cudaError_t e = occupancy_blocks_per_sm(reinterpret_cast<const void*>(k1a_qprep_kernel<T, kK1aRows, false>),
+                                          kK1aThreads, 0, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t cap = static_cast<int64_t>(per_sm) * a.num_sms;
-  const int grid = static_cast<int>(blocks_needed < cap ? blocks_needed : cap);
+  const bool one_wave = blocks_needed <= cap;
+  auto kern = one_wave ? k1a_qprep_kernel<T, kK1aRows, true> : k1a_qprep_kernel<T, kK1aRows, false>;
+  const int grid = static_cast<int>(one_wave ? blocks_needed : cap);
   kern<<<grid, kK1aThreads, 0, a.stream>>>(
       static_cast<uint16_t*>(a.q_normed), static_cast<const uint16_t*>(a.index_qk), a.cos_sin,
       a.context_lengths, static_cast<const uint16_t*>(a.w_q), a.eps, a.batch, a.seq_len);

@@ -4,7 +4,8 @@
 // contract).
 //
 // One aligned 8-lane group owns one block (b, g): each lane loads its two 16-byte
-// chunks of the four K rows (8 loads in flight per lane), forms the fixed-order
+// chunks of the four K rows (8 loads in flight per lane; in a one-wave launch before
+// the CTA stages its gamma), forms the fixed-order
 // FP32 mean ((k0+k1)+k2)+k3 times 0.25, casts it to T and re-loads it, then runs
 // the same norm_rope_group as K1a.  The block math reads nothing but (b, g), the
 // rows and the tables, so a block's bits never depend on the range or pastLen of
@@ -26,7 +27,10 @@ namespace qsa {
 // PAGED (launchQsaIndexKCompressPaged): additionally copy every VALID block's kbar
 // row to the pool V-tail of token 4g when that page slot is usable; the dense
 // output is the same code path, so it is bit-identical to the unpaged kernel.
-template <class T, bool PAGED>
+// ONE_WAVE: the grid holds a warp for every unit group, so each warp takes one group and
+// issues its loads before the CTA stages its gamma (the two round trips overlap); else a
+// persistent grid strides over the groups after the gamma stage.
+template <class T, bool PAGED, bool ONE_WAVE>
 __global__ void __launch_bounds__(QSA_K1B_THREADS, QSA_K1B_MINB)
 k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ index_qk,
                     const float* __restrict__ cos_sin, const int32_t* __restrict__ context_lengths,
@@ -38,8 +42,10 @@ k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ in
   const int ca = chunk_a(j);
   const int cb = chunk_b(j);
   __shared__ __align__(16) float g1[kHeadDim];
-  stage_gamma<T>(w_k, g1);
-  __syncthreads();
+  if constexpr (!ONE_WAVE) {
+    stage_gamma<T>(w_k, g1);
+    __syncthreads();
+  }
 
   const int32_t nb = block_end - block_begin;
   const int64_t units = static_cast<int64_t>(batch) * nb;
@@ -47,7 +53,8 @@ k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ in
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
 
   // Warp-uniform trip count: all 32 lanes reach the shuffles in norm_rope_group.
-  for (int64_t base = warp * 4; base < units; base += nwarps * 4) {
+  for (int64_t base = warp * 4;; base += nwarps * 4) {
+    if (!ONE_WAVE && base >= units) break;
     const int64_t u = base + (lane >> 3);
     const bool active = u < units;
     bool valid = false;
@@ -61,16 +68,23 @@ k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ in
     }
     float a[8], bv[8];
     RopeCS cs{};
+    uint4 ka[kRatio], kb[kRatio];
     if (valid) {
       const uint16_t* src = index_qk +
           (static_cast<int64_t>(b) * seq_len + (static_cast<int64_t>(kRatio) * g - past_len)) * kRowWidth + kKCol;
-      uint4 ka[kRatio], kb[kRatio];
 #pragma unroll
       for (int r = 0; r < kRatio; ++r) {
         ka[r] = ld_stream_v4(src + r * kRowWidth + ca);
         kb[r] = ld_stream_v4(src + r * kRowWidth + cb);
       }
       if (j < 4) cs = load_rope(cos_sin + static_cast<int64_t>(kRatio) * g * kCsWidth, j);
+    }
+    if constexpr (ONE_WAVE) {  // every warp of the CTA gets here once
+      stage_gamma<T>(w_k, g1);
+      __syncthreads();
+      if (base >= units) break;  // warp-uniform
+    }
+    if (valid) {
       float fa[kRatio][8], fb[kRatio][8];
 #pragma unroll
       for (int r = 0; r < kRatio; ++r) {
@@ -104,6 +118,7 @@ k1b_compress_kernel(uint16_t* __restrict__ kbar, const uint16_t* __restrict__ in
         }
       }
     }
+    if (ONE_WAVE) break;
   }
 }
 
@@ -112,14 +127,16 @@ constexpr int kK1bThreads = QSA_K1B_THREADS;
 
 template <class T, bool PAGED>
 cudaError_t launch_t(const LaunchKCompress& a, const PoolDev& pool) {
-  auto kern = k1b_compress_kernel<T, PAGED>;
   const int64_t units = static_cast<int64_t>(a.batch) * (a.block_end - a.block_begin);
   const int64_t blocks_needed = (units * 8 + kK1bThreads - 1) / kK1bThreads;
   int per_sm = 0;
-  cudaError_t e = occupancy_blocks_per_sm(reinterpret_cast<const void*>(kern), kK1bThreads, 0, &per_sm);
+  cudaError_t e = occupancy_blocks_per_sm(reinterpret_cast<const void*>(k1b_compress_kernel<T, PAGED, false>),
+                                          kK1bThreads, 0, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t cap = static_cast<int64_t>(per_sm) * a.num_sms;
-  const int grid = static_cast<int>(blocks_needed < cap ? blocks_needed : cap);
+  const bool one_wave = blocks_needed <= cap;
+  auto kern = one_wave ? k1b_compress_kernel<T, PAGED, true> : k1b_compress_kernel<T, PAGED, false>;
+  const int grid = static_cast<int>(one_wave ? blocks_needed : cap);
   kern<<<grid, kK1bThreads, 0, a.stream>>>(
       static_cast<uint16_t*>(a.kbar), static_cast<const uint16_t*>(a.index_qk), a.cos_sin,
       a.context_lengths, static_cast<const uint16_t*>(a.w_k), a.eps, a.batch, a.seq_len,
