@@ -563,6 +563,11 @@ def k1_configs_leg(qsa, lib, hbm_peak: float, names=None, sweep: bool = True) ->
                          "copies": n_sets[name], "touched_bytes": touched[name]}
         for name in ("k1a", "k1b"):
             out[name]["frac_of_yardstick"] = out[name]["gbs"] / out["yardstick_" + name]["gbs"]
+            # the yardstick's time over the kernel's.  The yardstick moves every row's / block's
+            # q or K bytes, more than the kernel where rows or blocks lie past the context, and
+            # reads no rope rows: where contexts are short the GB/s ratio above understates the
+            # kernel, and this one is the fairer
+            out[name]["time_vs_yardstick"] = out["yardstick_" + name]["us"] / out[name]["us"]
         del bufs
         return out
 
