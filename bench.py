@@ -899,17 +899,23 @@ class PrefillStepGpu:
         return ClockSampler(smi_device_id(self.local))
 
     def time_steps(self, K: int) -> float:
-        """K steps on the device clock (CUDA events on the launching stream), with
-        per-kernel events inside each step."""
+        """K steps on the device clock (CUDA events on the launching stream), then K more
+        with per-kernel events inside each step.  An event between K1 and K2 makes K2
+        wait for it instead of launching as K1's programmatic dependent (about 9 us a
+        step), so the K timed steps carry no event between their kernels; the per-kernel
+        times come from the second pass, which runs right after them."""
         torch = self.torch
-        self.evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(self.stream)
-        for i in range(K):
-            self.step(self.evs[i])
+        for _ in range(K):
+            self.step()
         end.record(self.stream)
         end.synchronize()
+        self.evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for i in range(K):
+            self.step(self.evs[i])
+        self.evs[-1][-1].synchronize()
         return start.elapsed_time(end)
 
     def after_timed(self, args, world: int) -> dict:
@@ -1117,7 +1123,11 @@ class PrefillStepGpu:
             kernels[n] = {"ms": per_kernel[n], "alg_bytes": ab[n], "gbs": gbs,
                           "frac_of_measured_hbm": gbs / hbm_peak, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS}
         kernels["k1_fused"]["rows_per_s"] = rows / (per_kernel["k1_fused"] * 1e-3)
-        kernels["k1_fused"]["timed"] = "inside the step (CUDA events around the launch)"
+        kernels["k1_fused"]["timed"] = ("inside the step (CUDA events around the launch, over a second pass of "
+                                         "the timed steps run right after them)")
+        kernels["k2"]["timed"] = ("inside the step (CUDA events around the launch, over a second pass of the "
+                                  "timed steps run right after them: an event between K1 and K2 keeps K2 from "
+                                  "launching during K1's tail, so the timed steps carry none)")
         for n in ("k1a", "k1b"):
             kernels[n]["timed"] = "separate entry point after the step loop; each launch after an L2 flush, median"
         kernels["select"]["timed"] = ("separate entry point, back-to-back launches after the step loop "

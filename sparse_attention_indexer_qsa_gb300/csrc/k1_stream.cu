@@ -142,6 +142,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k1_stream_kernel(const P
   float* g1k = g1q + kHeadDim;
   const uint32_t bar = base + L::kBarOff;
 
+  // A kernel launched after this one as a programmatic dependent (K2 scoring these rows)
+  // may start launching once every CTA of this grid has started: its CTAs then take the
+  // SMs this grid's last CTAs leave and set up there, and wait for this grid to complete
+  // before they read its outputs.
+  ptx::launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int32_t b, t0, nq;
