@@ -248,6 +248,18 @@ def oracle_sample(wl, budget_s: float = 12.0, seed: int = 0, threads: int | None
 
 # ------------------------------------------------------------------ main legs
 
+def flush_l2(buf, clean: bool = False) -> None:
+    """Evict L2 before a timed launch: write `buf` (2x L2), then, when `clean`, read it
+    back.  After the write alone L2 holds the flush's dirty lines, and a timed launch
+    that reads new data writes them back as it evicts them (K1b at B=8, 43 MB read,
+    takes 15.0 us that way against 12.3 us after the read).  The read turns L2 into
+    clean lines, so the timed launch pays only for its own traffic."""
+    import torch
+    buf.fill_(1)
+    if clean:
+        buf.view(torch.int64).sum()
+
+
 def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
     """One decode step for B sequences of length ctx_len over a paged pool
     (pre-decode, paged scores, top-k + expand), timed with CUDA events per kernel.
@@ -305,7 +317,7 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
     n = max(20, K)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
     for i in range(n):
-        l2_flush.fill_(1)
+        flush_l2(l2_flush)
         step(evs[i])
     torch.cuda.synchronize()
     ms = {name: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
@@ -334,7 +346,7 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
     n_rep = max(200, K)
     gts = []
     for _ in range(n_rep):
-        l2_flush.fill_(1)
+        flush_l2(l2_flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         graph.replay()
@@ -362,7 +374,7 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
     torch.cuda.current_stream().wait_stream(fs)
     fts = []
     for _ in range(n_rep):
-        l2_flush.fill_(1)
+        flush_l2(l2_flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fgraph.replay()
@@ -371,6 +383,17 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
         fts.append(e0.elapsed_time(e1))
     fused_step_ms = statistics.mean(fts)
     fused_step_median_ms = statistics.median(fts)
+    # the same replays after a clean flush (written, then read), whose lines the step evicts
+    # without writing them back
+    fts_clean = []
+    for _ in range(n_rep):
+        flush_l2(l2_flush, clean=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fgraph.replay()
+        e1.record()
+        e1.synchronize()
+        fts_clean.append(e0.elapsed_time(e1))
     nvis = ctx_len // 4
     alg = {"pre_decode": B * (1280 + 1024 + 3 * 256 + 256 + 2 * 256),
            "scores_decode": B * (nvis * 256 + 1024 + nvis * 4),
@@ -397,7 +420,7 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
                 raise RuntimeError(qsa.qsa_last_error())
         pts = []
         for _ in range(20):
-            l2_flush.fill_(1)
+            flush_l2(l2_flush)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             fn(sp)
@@ -422,7 +445,7 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
                 raise RuntimeError(qsa.qsa_last_error())
         yts = []
         for _ in range(n):
-            l2_flush.fill_(1)
+            flush_l2(l2_flush)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             yard(sp)
@@ -446,9 +469,12 @@ def decode_leg(qsa, lib, stream, K, B=64, ctx_len=16384):
     torch.cuda.empty_cache()
     return {"workload": f"decode step, B={B} sequences at ctx={ctx_len}, paged pool (128-token pages), bf16",
             "ms_per_step": fused_step_ms, "ms_per_step_median": fused_step_median_ms,
+            "ms_per_step_after_clean_flush": statistics.mean(fts_clean),
             "tokens_per_s": B / (fused_step_ms * 1e-3),
             "ms_per_step_three_launches": graph_step_ms, "ms_per_step_eager": step_ms, "kernels": kernels,
-            "timed": ("step: qsa_indexer_decode_step (one launch) as a CUDA graph replayed after an L2 flush, "
+            "timed": ("step: qsa_indexer_decode_step (one launch) as a CUDA graph replayed after an L2 flush "
+                      "(a 2x-L2 buffer written; ms_per_step_after_clean_flush: written, then read, so that "
+                      "the step evicts clean lines), "
                       f"mean of {n_rep} replays (CUDA events resolve about 1 us; ms_per_step_median: their median); "
                       "ms_per_step_three_launches: the three separate launches timed the same way; "
                       "kernels: CUDA events "
@@ -1031,12 +1057,12 @@ class PrefillStepGpu:
         l2_flush = torch.empty(2 * torch.cuda.get_device_properties(self.local).L2_cache_size, dtype=torch.uint8,
                                device="cuda")
 
-        def cold_ms(fn, n):
+        def cold_ms(fn, n, clean=False):
             for _ in range(3):
                 fn()
             ts = []
             for _ in range(n):
-                l2_flush.fill_(1)
+                flush_l2(l2_flush, clean)
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -1048,6 +1074,8 @@ class PrefillStepGpu:
 
         ms_k1a = cold_ms(k1a_only, max(K // 4, 20))
         ms_k1b = cold_ms(k1b_only, max(K // 4, 20))
+        ms_k1a_clean = cold_ms(k1a_only, max(K // 4, 20), clean=True)
+        ms_k1b_clean = cold_ms(k1b_only, max(K // 4, 20), clean=True)
         # prefill selection on the step's logits (top-512 blocks per row -> 2051 token ids)
         out_idx = torch.empty((rows, 2051), dtype=torch.int32, device="cuda")
 
@@ -1128,8 +1156,13 @@ class PrefillStepGpu:
         kernels["k2"]["timed"] = ("inside the step (CUDA events around the launch, over a second pass of the "
                                   "timed steps run right after them: an event between K1 and K2 keeps K2 from "
                                   "launching during K1's tail, so the timed steps carry none)")
-        for n in ("k1a", "k1b"):
-            kernels[n]["timed"] = "separate entry point after the step loop; each launch after an L2 flush, median"
+        for n, ms_clean in (("k1a", ms_k1a_clean), ("k1b", ms_k1b_clean)):
+            kernels[n]["timed"] = ("separate entry point after the step loop; each launch after an L2 flush (a "
+                                   "2x-L2 buffer written), median; ms_after_clean_flush / gbs_after_clean_flush: "
+                                   "after the buffer is written, then read, so that the launch evicts clean lines "
+                                   "instead of writing the flush's dirty ones back")
+            kernels[n]["ms_after_clean_flush"] = ms_clean
+            kernels[n]["gbs_after_clean_flush"] = ab[n] / (ms_clean * 1e-3) / 1e9
         kernels["select"]["timed"] = ("separate entry point, back-to-back launches after the step loop "
                                       "(1 GB of logits)")
         kernels["select"]["rows_per_s"] = rows / (per_kernel["select"] * 1e-3)
